@@ -1,0 +1,296 @@
+"""Seeded synthetic decode-attention inputs.
+
+This module only *generates* inputs (random draws, dtype casts, FP8 quantisation
+and the placement of token rows into a contiguous or paged cache).  It holds no
+attention arithmetic: both the CPU oracle and the CUDA library read the arrays
+produced here, and neither is imported from here.
+
+Every array is produced by ``numpy.random.Generator(PCG64(seed))`` with a fixed
+draw order: sequence lengths, then Q, then K, then V, then the page permutation.
+
+Shapes and recipes follow the five decode workloads of the flash-decoding
+scope (tiny MQA; GQA bf16; FP8 ragged; FP8 paged; long-context MQA):
+
+* Q is ``[B, QH, D]``; K/V caches are token-major ``[rows, KVH, D]`` for the
+  contiguous layout (sequence ``b`` owns rows ``kv_start_idx[b] ...
+  kv_start_idx[b] + seq_len[b] - 1``) and ``[num_pages, page_size, KVH, D]``
+  for the paged layout, addressed through ``block_table[b, t // page_size]``.
+* f16/bf16 tensors are stored as their raw 16-bit patterns (``uint16``),
+  FP8-e4m3 tensors as raw bytes (``uint8``).
+* FP8 K and V are quantised per tensor: ``scale = amax / 448`` in fp32, codes
+  ``= e4m3fn(clamp(x / scale, -448, 448))`` rounded to nearest even.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+E4M3_MAX = 448.0
+
+# Values written where no sequence owns a row (gaps between contiguous
+# sequences, unused pages, page tails).  A kernel that reads such a row
+# produces a grossly wrong score or output, so parity fails loudly.
+POISON_E4M3 = 0x7E          # +448
+POISON_F16 = 30000.0
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    q_dtype: str              # 'f16' | 'bf16'  (out has the same dtype)
+    kv_dtype: str             # 'f16' | 'bf16' | 'e4m3'
+    softmax_scale: np.float32
+    k_scale: np.float32
+    v_scale: np.float32
+    seq_len: np.ndarray       # int32 [B]
+    q: np.ndarray             # uint16 [B, QH, D] raw bits
+    k_cache: np.ndarray       # uint16/uint8 [rows, KVH, D] or [pages, P, KVH, D]
+    v_cache: np.ndarray
+    page_size: int = 0        # 0 = contiguous layout
+    kv_start_idx: Optional[np.ndarray] = None   # int32 [B] (contiguous)
+    block_table: Optional[np.ndarray] = None    # int32 [B, stride] (paged)
+
+    @property
+    def paged(self) -> bool:
+        return self.page_size > 0
+
+    @property
+    def kv_rows(self) -> int:
+        """Number of token rows the K/V buffers hold."""
+        if self.paged:
+            return int(self.k_cache.shape[0] * self.k_cache.shape[1])
+        return int(self.k_cache.shape[0])
+
+    @property
+    def block_table_stride(self) -> int:
+        return int(self.block_table.shape[1]) if self.paged else 0
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.kv_dtype == "e4m3" else 2
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes one decode step must move: K and V rows of every sequence,
+        Q in, O out, and the index arrays it reads."""
+        B, QH, KVH, D = self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim
+        total = int(self.seq_len.astype(np.int64).sum())
+        kv = total * KVH * D * self.kv_elem_bytes * 2
+        qo = 2 * B * QH * D * 2
+        if self.paged:
+            pages = int(sum((int(t) + self.page_size - 1) // self.page_size for t in self.seq_len))
+            idx = 4 * B + 4 * pages
+        else:
+            idx = 8 * B
+        return kv + qo + idx
+
+
+# ----------------------------------------------------------------------------
+# dtype helpers (casts of random draws into the stored formats)
+# ----------------------------------------------------------------------------
+
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x.astype(np.float16)).view(np.uint16)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def f32_to_e4m3_bytes(x: np.ndarray, scale: np.float32) -> np.ndarray:
+    """Per-tensor quantisation to OCP e4m3fn codes (round to nearest even)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    t = (t / torch.tensor(float(scale), dtype=torch.float32)).clamp_(-E4M3_MAX, E4M3_MAX)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+
+
+def _cast16(x: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f16":
+        return f32_to_f16_bits(x)
+    if dtype == "bf16":
+        return f32_to_bf16_bits(x)
+    raise ValueError(dtype)
+
+
+def _poison_value(dtype: str):
+    if dtype == "e4m3":
+        return np.uint8(POISON_E4M3)
+    return _cast16(np.array([POISON_F16], np.float32), dtype)[0]
+
+
+def _quantise_pair(k: np.ndarray, v: np.ndarray, kv_dtype: str):
+    """Cast the logical K/V draws to the stored format; return codes and scales."""
+    if kv_dtype == "e4m3":
+        k_amax = np.float32(np.abs(k).max()) if k.size else np.float32(1.0)
+        v_amax = np.float32(np.abs(v).max()) if v.size else np.float32(1.0)
+        k_scale = np.float32(k_amax / np.float32(E4M3_MAX))
+        v_scale = np.float32(v_amax / np.float32(E4M3_MAX))
+        if k_scale == 0:
+            k_scale = np.float32(1.0)
+        if v_scale == 0:
+            v_scale = np.float32(1.0)
+        return f32_to_e4m3_bytes(k, k_scale), f32_to_e4m3_bytes(v, v_scale), k_scale, v_scale
+    return _cast16(k, kv_dtype), _cast16(v, kv_dtype), np.float32(1.0), np.float32(1.0)
+
+
+# ----------------------------------------------------------------------------
+# generic builders
+# ----------------------------------------------------------------------------
+
+def make_contiguous(name: str, seed: int, seq_len, num_q_heads: int, num_kv_heads: int,
+                    head_dim: int, q_dtype: str, kv_dtype: str, softmax_scale=None,
+                    gap: int = 0, lead: int = 0, tail: int = 0,
+                    rng: Optional[np.random.Generator] = None) -> Workload:
+    """Token-major contiguous cache.  ``gap`` poisoned rows separate consecutive
+    sequences, ``lead``/``tail`` poisoned rows sit before the first and after the
+    last one.  With all three zero, ``kv_start_idx`` is the exclusive prefix sum
+    of ``seq_len``."""
+    if rng is None:
+        rng = np.random.Generator(np.random.PCG64(seed))
+    seq_len = np.asarray(seq_len, dtype=np.int32)
+    B = int(seq_len.shape[0])
+    QH, KVH, D = num_q_heads, num_kv_heads, head_dim
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    total = int(seq_len.astype(np.int64).sum())
+
+    q32 = rng.standard_normal((B, QH, D), dtype=np.float32)
+    k32 = rng.standard_normal((total, KVH, D), dtype=np.float32)
+    v32 = rng.standard_normal((total, KVH, D), dtype=np.float32)
+    q = _cast16(q32, q_dtype)
+    kq, vq, k_scale, v_scale = _quantise_pair(k32, v32, kv_dtype)
+    del k32, v32
+
+    starts = np.zeros(B, np.int32)
+    rows = lead
+    for b in range(B):
+        starts[b] = rows
+        rows += int(seq_len[b]) + (gap if b + 1 < B else 0)
+    rows += tail
+    rows = max(rows, 1)
+    pv = _poison_value(kv_dtype)
+    k_cache = np.full((rows, KVH, D), pv, dtype=kq.dtype)
+    v_cache = np.full((rows, KVH, D), pv, dtype=vq.dtype)
+    off = 0
+    for b in range(B):
+        n = int(seq_len[b])
+        k_cache[starts[b]:starts[b] + n] = kq[off:off + n]
+        v_cache[starts[b]:starts[b] + n] = vq[off:off + n]
+        off += n
+    return Workload(name=name, batch=B, num_q_heads=QH, num_kv_heads=KVH, head_dim=D,
+                    q_dtype=q_dtype, kv_dtype=kv_dtype,
+                    softmax_scale=np.float32(softmax_scale), k_scale=k_scale, v_scale=v_scale,
+                    seq_len=seq_len, q=q, k_cache=k_cache, v_cache=v_cache,
+                    page_size=0, kv_start_idx=starts, block_table=None)
+
+
+def to_paged(w: Workload, page_size: int, seed: int, oversize: float = 1.2,
+             rng: Optional[np.random.Generator] = None,
+             extra_stride: int = 0) -> Workload:
+    """Re-lay the logical rows of a contiguous workload into a paged pool.
+
+    The pool holds ``ceil(oversize * sum_b ceil(T_b / page_size))`` pages; a
+    seeded permutation of the pool's page ids is drawn and its first entries
+    are handed to the sequences in order.  Unused pages and page tails are
+    poisoned; block-table entries past a sequence's last page are -1."""
+    assert not w.paged
+    if rng is None:
+        rng = np.random.Generator(np.random.PCG64(seed))
+    P = int(page_size)
+    B = w.batch
+    npages = [(int(t) + P - 1) // P for t in w.seq_len]
+    used = int(sum(npages))
+    pool = max(1, int(math.ceil(oversize * used)))
+    perm = rng.permutation(pool).astype(np.int32)
+    stride = max(1, max(npages) if npages else 1) + extra_stride
+    table = np.full((B, stride), -1, dtype=np.int32)
+    pv = _poison_value(w.kv_dtype)
+    shape = (pool, P, w.num_kv_heads, w.head_dim)
+    k_pool = np.full(shape, pv, dtype=w.k_cache.dtype)
+    v_pool = np.full(shape, pv, dtype=w.v_cache.dtype)
+    nxt = 0
+    for b in range(B):
+        T = int(w.seq_len[b])
+        s = int(w.kv_start_idx[b])
+        for j in range(npages[b]):
+            phys = int(perm[nxt])
+            nxt += 1
+            table[b, j] = phys
+            lo, hi = j * P, min(T, (j + 1) * P)
+            k_pool[phys, : hi - lo] = w.k_cache[s + lo:s + hi]
+            v_pool[phys, : hi - lo] = w.v_cache[s + lo:s + hi]
+    return dataclasses.replace(w, name=w.name + f"-paged{P}", k_cache=k_pool, v_cache=v_pool,
+                               page_size=P, kv_start_idx=None, block_table=table)
+
+
+# ----------------------------------------------------------------------------
+# the five decode workloads
+# ----------------------------------------------------------------------------
+
+def tiny_mqa() -> Workload:
+    """B=2, seq_len {7, 33}, 4 query heads / 1 KV head, D=64, fp16 everywhere,
+    contiguous (kv_start_idx {0, 7}), softmax_scale 1/8, seed 0."""
+    return make_contiguous("tiny-mqa-f16", 0, [7, 33], 4, 1, 64, "f16", "f16",
+                           softmax_scale=1.0 / 8.0)
+
+
+def gqa_bf16(batch: int = 16, seq: int = 4096) -> Workload:
+    """B=16, seq_len 4096, 32/8 heads, D=128, bf16, contiguous, seed 1."""
+    return make_contiguous(f"gqa-bf16-B{batch}-T{seq}", 1, [seq] * batch, 32, 8, 128,
+                           "bf16", "bf16")
+
+
+def fp8_ragged(batch: int = 32, lo: int = 512, hi: int = 32768) -> Workload:
+    """B=32, seq_len ~ U{512..32768}, 32/8 heads, D=128, fp16 Q, e4m3 KV,
+    contiguous, seed 2."""
+    rng = np.random.Generator(np.random.PCG64(2))
+    seq = rng.integers(lo, hi, size=batch, endpoint=True).astype(np.int32)
+    return make_contiguous(f"fp8-ragged-B{batch}", 2, seq, 32, 8, 128, "f16", "e4m3", rng=rng)
+
+
+def lognormal_lengths(rng: np.random.Generator, batch: int, median: float = 2048.0,
+                      lo: int = 16, hi: int = 16384) -> np.ndarray:
+    z = rng.standard_normal(batch)
+    return np.clip(np.rint(median * np.exp(z)), lo, hi).astype(np.int32)
+
+
+def fp8_paged(batch: int = 64, page_size: int = 64) -> Workload:
+    """B=64, seq_len lognormal (median 2048, sigma 1, clipped to [16, 16384]),
+    64/8 heads, D=128, fp16 Q, e4m3 KV, page_size 64, 1.2x pool, seed 3."""
+    rng = np.random.Generator(np.random.PCG64(3))
+    seq = lognormal_lengths(rng, batch)
+    w = make_contiguous(f"fp8-paged-B{batch}", 3, seq, 64, 8, 128, "f16", "e4m3", rng=rng)
+    return to_paged(w, page_size, 3, rng=rng)
+
+
+def long_mqa(batch: int = 4, seq: int = 131072) -> Workload:
+    """B=4, seq_len 131072, 16/1 heads, D=128, fp16 Q, e4m3 KV, contiguous, seed 4."""
+    return make_contiguous(f"long-mqa-fp8-B{batch}-T{seq}", 4, [seq] * batch, 16, 1, 128,
+                           "f16", "e4m3")
+
+
+CONFIGS = {
+    1: tiny_mqa,
+    2: gqa_bf16,
+    3: fp8_ragged,
+    4: fp8_paged,
+    5: long_mqa,
+}
+
+CONFIG_NAMES = {
+    1: "tiny MQA decode fp16: B=2, seq_len {7,33}, 4/1 heads, D=64, contiguous",
+    2: "GQA decode bf16: B=16, seq_len 4096, 32/8 heads, D=128, contiguous",
+    3: "FP8 ragged decode: B=32, seq_len U[512,32768], 32/8 heads, D=128, e4m3 KV, contiguous",
+    4: "FP8 paged decode: B=64, seq_len lognormal(median 2048) in [16,16384], 64/8 heads, "
+       "D=128, e4m3 KV, page 64, 1.2x permuted pool",
+    5: "long-context MQA split-KV: B=4, seq_len 131072, 16/1 heads, D=128, e4m3 KV, contiguous",
+}

@@ -1,0 +1,243 @@
+/*
+ * fd_oracle.c -- plain CPU fp64 oracle for decode-step (single query token)
+ * attention over a contiguous or paged KV cache.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg load this file.  It shares no code, header,
+ * table or constant with the CUDA library; the two only read the same input
+ * arrays.
+ *
+ * What it computes is the plain definition of softmax attention for one query
+ * row per (sequence, query head), with a full two-pass softmax and no
+ * blocking, splitting or online rescaling:
+ *
+ *   kvh      = qh / (num_q_heads / num_kv_heads)        (consecutive query
+ *                                                        heads share a KV head)
+ *   row(t)   = kv_start_idx[b] + t                       (contiguous cache)
+ *            = block_table[b][t / P] * P + t % P         (paged cache)
+ *   k_t[d]   = k_scale * dec(K[row(t)][kvh][d])
+ *   v_t[d]   = v_scale * dec(V[row(t)][kvh][d])
+ *   s_t      = softmax_scale * sum_d q[b][qh][d] * k_t[d]
+ *   M        = max_t s_t,  w_t = exp(s_t - M),  Z = sum_t w_t
+ *   out[d]   = sum_t (w_t / Z) * v_t[d]
+ *   lse      = M + ln Z           (natural log of sum_t exp(s_t))
+ *
+ * Sources, by page and section:
+ *  - scaled dot product, softmax and the weighted sum of V rows: "SGLang
+ *    Prefill optimisation: dissecting FlashAttention kernel bottlenecks with
+ *    GPU Trace", section 2.2 (the score is dot(q, k) times a scale; the
+ *    weights are the exponentials normalised by their sum; the output is
+ *    the weighted sum of V);
+ *  - per-sequence start index and length of a variable-length batch: "From
+ *    SGLang kernel source to GPU trace: DeepSeek V4.1 Flash-Decode",
+ *    section 3.1 (kernel arguments kv_start_idx and seq_len);
+ *  - page addressing: "Learn CUDA from scratch, chapter 15: GPU profiling and
+ *    LLM inference", section 15.26 (physical page from the block table, then
+ *    (page * page_size + offset) rows into a [page, offset, head, dim] pool);
+ *  - GQA grouping (group = QH / KVH query heads per KV head): same chapter,
+ *    section 15.12;
+ *  - per-tensor FP8 scales: the decoded code times a fp32 scale, the KV
+ *    quantisation of section 15.11 of the same chapter with one scale per
+ *    tensor.
+ *
+ * Readings where the pages are silent: the contiguous cache is token-major
+ * [rows, KVH, D] with kv_start_idx in rows; LSE is in natural log of the
+ * scaled scores (softmax_scale and k_scale included); seq_len = 0 gives
+ * out = 0 and lse = -inf.  FP8 is OCP e4m3fn (bias 7, no infinities, S.1111.111
+ * is NaN and is rejected).
+ *
+ * All arithmetic is IEEE fp64 (build without -ffast-math).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { FDO_F16 = 0, FDO_BF16 = 1, FDO_E4M3 = 2 };
+
+enum {
+  FDO_OK = 0,
+  FDO_BAD_ARG = 1,
+  FDO_ROW_OUT_OF_RANGE = 2,
+  FDO_NAN_CODE = 3,
+  FDO_NO_MEMORY = 4,
+};
+
+/* OCP 8-bit floating point, E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits.  Exponent field 0 holds subnormals m/8 * 2^-6;
+ * S.1111.111 is NaN and there is no infinity. */
+double fdo_e4m3_value(uint8_t code) {
+  int s = (code >> 7) & 1;
+  int e = (code >> 3) & 0xF;
+  int m = code & 0x7;
+  double mag;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    mag = ldexp((double)m / 8.0, -6);
+  else
+    mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+/* IEEE 754 binary16: 1 sign, 5 exponent bits with bias 15, 10 mantissa bits. */
+double fdo_f16_value(uint16_t bits) {
+  int s = (bits >> 15) & 1;
+  int e = (bits >> 10) & 0x1F;
+  int m = bits & 0x3FF;
+  double mag;
+  if (e == 0x1F) mag = m ? NAN : INFINITY;
+  else if (e == 0) mag = ldexp((double)m / 1024.0, -14);
+  else mag = ldexp(1.0 + (double)m / 1024.0, e - 15);
+  return s ? -mag : mag;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32 (8 exponent bits, bias 127,
+ * 7 mantissa bits). */
+double fdo_bf16_value(uint16_t bits) {
+  int s = (bits >> 15) & 1;
+  int e = (bits >> 7) & 0xFF;
+  int m = bits & 0x7F;
+  double mag;
+  if (e == 0xFF) mag = m ? NAN : INFINITY;
+  else if (e == 0) mag = ldexp((double)m / 128.0, -126);
+  else mag = ldexp(1.0 + (double)m / 128.0, e - 127);
+  return s ? -mag : mag;
+}
+
+static double decode_elem(const void *base, int dtype, size_t idx) {
+  if (dtype == FDO_E4M3) return fdo_e4m3_value(((const uint8_t *)base)[idx]);
+  if (dtype == FDO_BF16) return fdo_bf16_value(((const uint16_t *)base)[idx]);
+  return fdo_f16_value(((const uint16_t *)base)[idx]);
+}
+
+/* Row of the cache holding token t of sequence b, or -1 if out of range. */
+static int64_t cache_row(const int32_t *kv_start_idx, const int32_t *block_table,
+                         int block_table_stride, int page_size, int b, int t,
+                         int64_t kv_rows) {
+  int64_t row;
+  if (block_table) {
+    int64_t phys = block_table[(int64_t)b * block_table_stride + t / page_size];
+    row = phys * page_size + t % page_size;
+  } else {
+    row = (int64_t)kv_start_idx[b] + t;
+  }
+  if (row < 0 || row >= kv_rows) return -1;
+  return row;
+}
+
+/*
+ * Computes out[B][QH][D] and lse[B][QH] in fp64.
+ *
+ * q: [B][QH][D] 16-bit patterns of q_dtype.
+ * k_cache, v_cache: [rows][KVH][D] (contiguous) or [pages][P][KVH][D] (paged)
+ *   elements of kv_dtype; kv_rows = number of token rows they hold.
+ * Exactly one of kv_start_idx / block_table is non-NULL.
+ * pairs: NULL for every (b, qh), else n_pairs entries of (b, qh) to compute;
+ *   the other outputs are left untouched.
+ * weights: NULL, or [B][QH][weights_stride] receiving w_t / Z.
+ * threads_used: NULL, or receives the number of threads that ran.
+ */
+int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const void *v_cache,
+                         int kv_dtype, const int32_t *kv_start_idx, const int32_t *block_table,
+                         int block_table_stride, const int32_t *seq_len, int64_t kv_rows,
+                         int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                         int page_size, double softmax_scale, double k_scale, double v_scale,
+                         const int32_t *pairs, int n_pairs, int nthreads, double *out,
+                         double *lse, double *weights, int weights_stride, int *threads_used) {
+  if (!q || !k_cache || !v_cache || !seq_len || !out || !lse) return FDO_BAD_ARG;
+  if ((kv_start_idx == NULL) == (block_table == NULL)) return FDO_BAD_ARG;
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return FDO_BAD_ARG;
+  if (num_q_heads % num_kv_heads != 0) return FDO_BAD_ARG;
+  if (block_table && page_size <= 0) return FDO_BAD_ARG;
+  if (q_dtype != FDO_F16 && q_dtype != FDO_BF16) return FDO_BAD_ARG;
+  if (kv_dtype != FDO_F16 && kv_dtype != FDO_BF16 && kv_dtype != FDO_E4M3) return FDO_BAD_ARG;
+
+  const int group = num_q_heads / num_kv_heads;
+  const int n_work = pairs ? n_pairs : batch * num_q_heads;
+  int status = FDO_OK;
+  int used = 1;
+
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+  {
+#pragma omp single
+    used = omp_get_num_threads();
+  }
+#endif
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int w = 0; w < n_work; ++w) {
+    int b = pairs ? pairs[2 * w] : w / num_q_heads;
+    int qh = pairs ? pairs[2 * w + 1] : w % num_q_heads;
+    if (b < 0 || b >= batch || qh < 0 || qh >= num_q_heads) {
+#pragma omp atomic write
+      status = FDO_BAD_ARG;
+      continue;
+    }
+    int kvh = qh / group;
+    int T = seq_len[b];
+    double *o = out + ((size_t)b * num_q_heads + qh) * head_dim;
+    double *l = lse + (size_t)b * num_q_heads + qh;
+    if (T <= 0) {
+      for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+      *l = -INFINITY;
+      continue;
+    }
+    double *s = (double *)malloc(sizeof(double) * (size_t)T);
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)T);
+    double *qv = (double *)malloc(sizeof(double) * (size_t)head_dim);
+    if (!s || !rows || !qv) {
+      free(s); free(rows); free(qv);
+#pragma omp atomic write
+      status = FDO_NO_MEMORY;
+      continue;
+    }
+    int bad = 0;
+    for (int d = 0; d < head_dim; ++d)
+      qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + d);
+
+    /* scores s_t = softmax_scale * q . (k_scale * dec(k_t)) */
+    for (int t = 0; t < T && !bad; ++t) {
+      rows[t] = cache_row(kv_start_idx, block_table, block_table_stride, page_size, b, t, kv_rows);
+      if (rows[t] < 0) { bad = FDO_ROW_OUT_OF_RANGE; break; }
+      size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;
+      double dot = 0.0;
+      for (int d = 0; d < head_dim; ++d) {
+        double kd = decode_elem(k_cache, kv_dtype, base + d);
+        if (isnan(kd)) { bad = FDO_NAN_CODE; break; }
+        dot += qv[d] * (k_scale * kd);
+      }
+      s[t] = softmax_scale * dot;
+    }
+    if (!bad) {
+      /* two-pass softmax: max, then normalised exponentials */
+      double M = s[0];
+      for (int t = 1; t < T; ++t) if (s[t] > M) M = s[t];
+      double Z = 0.0;
+      for (int t = 0; t < T; ++t) { s[t] = exp(s[t] - M); Z += s[t]; }
+      for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+      for (int t = 0; t < T && !bad; ++t) {
+        double wt = s[t] / Z;
+        if (weights) weights[((size_t)b * num_q_heads + qh) * weights_stride + t] = wt;
+        size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;
+        for (int d = 0; d < head_dim; ++d) {
+          double vd = decode_elem(v_cache, kv_dtype, base + d);
+          if (isnan(vd)) { bad = FDO_NAN_CODE; break; }
+          o[d] += wt * (v_scale * vd);
+        }
+      }
+      *l = M + log(Z);
+    }
+    if (bad) {
+#pragma omp atomic write
+      status = bad;
+    }
+    free(s); free(rows); free(qv);
+  }
+  if (threads_used) *threads_used = used;
+  return status;
+}

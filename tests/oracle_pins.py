@@ -1,0 +1,400 @@
+"""Pins for the CPU oracle: checks that tie it to things other than itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` instance and raises AssertionError
+(or the oracle's own error) when the oracle disagrees with
+
+* the number formats' definitions, decoded by independent library routines
+  (numpy float16, torch bfloat16 and float8_e4m3fn);
+* closed forms of softmax attention (identical rows, one key, two keys,
+  uniform weights, a dominant key, the empty sequence);
+* invariants (weights sum to one, key permutation, GQA == MHA with
+  replicated KV heads, paged == contiguous, scaling and shifting);
+* an independent fp64 recomputation by the chunked online-softmax recurrence
+  (running max, running sum, rescaled accumulator) over random chunk
+  boundaries, with the two halves of each sequence merged by their
+  log-sum-exp -- the recurrence of the online softmax loop in "SGLang Prefill
+  optimisation: dissecting FlashAttention kernel bottlenecks with GPU Trace",
+  section 2.2, and the split merge it implies.
+
+The pins are collected in ``ALL_PINS`` so that a mutation test can run them
+against deliberately broken copies of the oracle.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+import fd_workloads as fw
+
+
+# ----------------------------------------------------------------------------
+# independent decoders (library routines, not the oracle's)
+# ----------------------------------------------------------------------------
+
+def lib_decode(arr: np.ndarray, dtype: str) -> np.ndarray:
+    arr = np.ascontiguousarray(arr)
+    if dtype == "f16":
+        return arr.view(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        t = torch.from_numpy(arr.view(np.int16).copy()).view(torch.bfloat16)
+        return t.to(torch.float64).numpy()
+    if dtype == "e4m3":
+        t = torch.from_numpy(arr.view(np.uint8).copy()).view(torch.float8_e4m3fn)
+        return t.to(torch.float64).numpy()
+    raise ValueError(dtype)
+
+
+def custom(q32, k32, v32, seq_len, q_dtype="f16", kv_dtype="f16", softmax_scale=0.125,
+           k_scale=1.0, v_scale=1.0, kv_start_idx=None, name="custom") -> fw.Workload:
+    """A contiguous workload from explicit float arrays (cast to the stored
+    formats; e4m3 codes are taken from the values with scale 1)."""
+    q32 = np.asarray(q32, np.float32)
+    k32 = np.asarray(k32, np.float32)
+    v32 = np.asarray(v32, np.float32)
+    seq_len = np.asarray(seq_len, np.int32)
+    B, QH, D = q32.shape
+    KVH = k32.shape[1]
+    if kv_start_idx is None:
+        kv_start_idx = np.concatenate([[0], np.cumsum(seq_len)[:-1]]).astype(np.int32)
+    q = fw._cast16(q32, q_dtype)
+    if kv_dtype == "e4m3":
+        k = fw.f32_to_e4m3_bytes(k32, np.float32(1.0))
+        v = fw.f32_to_e4m3_bytes(v32, np.float32(1.0))
+    else:
+        k = fw._cast16(k32, kv_dtype)
+        v = fw._cast16(v32, kv_dtype)
+    return fw.Workload(name=name, batch=B, num_q_heads=QH, num_kv_heads=KVH, head_dim=D,
+                       q_dtype=q_dtype, kv_dtype=kv_dtype,
+                       softmax_scale=np.float32(softmax_scale), k_scale=np.float32(k_scale),
+                       v_scale=np.float32(v_scale), seq_len=seq_len, q=q, k_cache=k, v_cache=v,
+                       page_size=0, kv_start_idx=np.asarray(kv_start_idx, np.int32))
+
+
+# ----------------------------------------------------------------------------
+# independent recomputation: chunked online softmax + LSE merge
+# ----------------------------------------------------------------------------
+
+def _online_state(scores: np.ndarray, vals: np.ndarray, rng, chunk_max: int):
+    """Running max m, running sum l and rescaled accumulator acc over random
+    chunks of the score sequence."""
+    D = vals.shape[1]
+    m, l, acc = -math.inf, 0.0, np.zeros(D)
+    i = 0
+    n = scores.shape[0]
+    while i < n:
+        j = min(n, i + int(rng.integers(1, chunk_max + 1)))
+        s = scores[i:j]
+        m_new = max(m, float(s.max()))
+        alpha = math.exp(m - m_new) if m != -math.inf else 0.0
+        p = np.exp(s - m_new)
+        l = l * alpha + float(p.sum())
+        acc = acc * alpha + p @ vals[i:j]
+        m = m_new
+        i = j
+    return m, l, acc
+
+
+def _merge(states, D):
+    ms = [s[0] for s in states if s[1] > 0]
+    if not ms:
+        return -math.inf, 0.0, np.zeros(D)
+    M = max(ms)
+    l = 0.0
+    acc = np.zeros(D)
+    for m, li, ai in states:
+        if li > 0:
+            f = math.exp(m - M)
+            l += li * f
+            acc = acc + ai * f
+    return M, l, acc
+
+
+def online_reference(w: fw.Workload, rng, chunk_max: int = 7):
+    """fp64 out/lse by the online-softmax recurrence, each sequence cut at a
+    random point into two partial states that are merged afterwards."""
+    B, QH, KVH, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    g = QH // KVH
+    qf = lib_decode(w.q, w.q_dtype).reshape(B, QH, D)
+    kf = lib_decode(w.k_cache, w.kv_dtype).reshape(-1, KVH, D) * float(w.k_scale)
+    vf = lib_decode(w.v_cache, w.kv_dtype).reshape(-1, KVH, D) * float(w.v_scale)
+    out = np.zeros((B, QH, D))
+    lse = np.zeros((B, QH))
+    for b in range(B):
+        T = int(w.seq_len[b])
+        t = np.arange(T)
+        if w.paged:
+            P = w.page_size
+            rows = w.block_table[b, t // P].astype(np.int64) * P + t % P
+        else:
+            rows = int(w.kv_start_idx[b]) + t
+        for qh in range(QH):
+            kvh = qh // g
+            if T == 0:
+                out[b, qh] = 0.0
+                lse[b, qh] = -math.inf
+                continue
+            scores = float(w.softmax_scale) * (kf[rows, kvh, :] @ qf[b, qh])
+            vals = vf[rows, kvh, :]
+            cut = int(rng.integers(0, T + 1))
+            st = [_online_state(scores[:cut], vals[:cut], rng, chunk_max),
+                  _online_state(scores[cut:], vals[cut:], rng, chunk_max)]
+            m, l, acc = _merge(st, D)
+            out[b, qh] = acc / l
+            lse[b, qh] = m + math.log(l)
+    return out, lse
+
+
+# ----------------------------------------------------------------------------
+# pins
+# ----------------------------------------------------------------------------
+
+def _close(a, b, rtol, atol=0.0, what=""):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    err = np.abs(a - b)
+    lim = atol + rtol * np.abs(b)
+    assert np.all(err <= lim), f"{what}: max err {err.max():.3e}"
+
+
+def pin_e4m3_codes(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    ref = lib_decode(codes, "e4m3")
+    got = np.array([orc.e4m3_value(c) for c in range(256)])
+    nan = (codes & 0x7F) == 0x7F
+    assert np.all(np.isnan(got[nan])), "S.1111.111 must decode to NaN"
+    assert np.array_equal(got[~nan], ref[~nan]), "e4m3 decode differs from float8_e4m3fn"
+    # values fixed by the format: largest normal, smallest subnormal,
+    # smallest normal, one, negative zero
+    assert orc.e4m3_value(0x7E) == 448.0
+    assert orc.e4m3_value(0x01) == 2.0 ** -9
+    assert orc.e4m3_value(0x08) == 2.0 ** -6
+    assert orc.e4m3_value(0x38) == 1.0
+    assert orc.e4m3_value(0xB8) == -1.0
+    assert math.copysign(1.0, orc.e4m3_value(0x80)) == -1.0 and orc.e4m3_value(0x80) == 0.0
+
+
+def pin_f16_codes(orc):
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = lib_decode(codes, "f16")
+    got = np.array([orc.f16_value(int(c)) for c in codes])
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[np.isinf(ref)], ref[np.isinf(ref)])
+
+
+def pin_bf16_codes(orc):
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = lib_decode(codes, "bf16")
+    got = np.array([orc.bf16_value(int(c)) for c in codes])
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+
+
+def pin_identical_v_rows(orc):
+    rng = np.random.default_rng(11)
+    T, D = 37, 64
+    q = rng.standard_normal((1, 4, D))
+    k = rng.standard_normal((T, 2, D))
+    row = rng.standard_normal((1, 2, D))
+    v = np.repeat(row, T, axis=0)
+    w = custom(q, k, v, [T], v_scale=0.75)
+    out, lse = orc.decode_attention(w)
+    expect = lib_decode(w.v_cache[0], "f16") * 0.75      # [KVH, D]
+    for qh in range(4):
+        _close(out[0, qh], expect[qh // 2], 1e-14, 1e-300, "identical V rows")
+
+
+def pin_single_key(orc):
+    """seq_len = 1: the only weight is 1, so out = v_0 and lse = s_0.  With a
+    one-hot q and k the score is known exactly."""
+    D = 64
+    q = np.zeros((1, 1, D)); q[0, 0, 5] = 1.5
+    k = np.zeros((3, 1, D)); k[1, 0, 5] = -2.0; k[1, 0, 6] = 7.0
+    v = np.zeros((3, 1, D)); v[1, 0, :] = np.arange(D) / 8.0
+    w = custom(q, k, v, [1], kv_start_idx=[1], softmax_scale=0.25, k_scale=0.5, v_scale=2.0)
+    out, lse = orc.decode_attention(w)
+    assert lse[0, 0] == 0.25 * 1.5 * (-2.0 * 0.5)
+    assert np.array_equal(out[0, 0], 2.0 * np.arange(D) / 8.0)
+
+
+def pin_zero_query(orc):
+    """q = 0: all scores are 0, weights are 1/T, out = mean of V, lse = ln T."""
+    rng = np.random.default_rng(12)
+    T, D = 50, 128
+    q = np.zeros((1, 2, D))
+    k = rng.standard_normal((T, 1, D))
+    v = rng.standard_normal((T, 1, D))
+    w = custom(q, k, v, [T])
+    out, lse = orc.decode_attention(w)
+    vf = lib_decode(w.v_cache, "f16")[:, 0, :]
+    for qh in range(2):
+        _close(out[0, qh], vf.mean(axis=0), 1e-13, 1e-15, "zero query mean")
+        _close(lse[0, qh], math.log(T), 1e-15, 0, "zero query lse")
+
+
+def pin_identical_k_rows(orc):
+    """All K rows equal: uniform weights, out = mean V, lse = s + ln T, where
+    s is exact for a one-hot key."""
+    rng = np.random.default_rng(13)
+    T, D = 21, 64
+    q = rng.standard_normal((1, 1, D)).astype(np.float32)
+    q[0, 0, 3] = 0.625
+    k = np.zeros((T, 1, D)); k[:, 0, 3] = 4.0
+    v = rng.standard_normal((T, 1, D))
+    w = custom(q, k, v, [T], softmax_scale=0.5)
+    out, lse = orc.decode_attention(w)
+    vf = lib_decode(w.v_cache, "f16")[:, 0, :]
+    _close(out[0, 0], vf.mean(axis=0), 1e-13, 1e-15, "identical K mean")
+    _close(lse[0, 0], 0.5 * 0.625 * 4.0 + math.log(T), 1e-15, 0, "identical K lse")
+
+
+def pin_two_keys(orc):
+    """T = 2: out = sigma(s0 - s1) v0 + sigma(s1 - s0) v1 and
+    lse = logaddexp(s0, s1), with exact one-hot scores."""
+    D = 64
+    q = np.zeros((1, 1, D)); q[0, 0, 0] = 1.0; q[0, 0, 1] = 1.0
+    k = np.zeros((2, 1, D)); k[0, 0, 0] = 3.0; k[1, 0, 1] = -1.25
+    v = np.zeros((2, 1, D)); v[0, 0, :] = 1.0; v[1, 0, :] = -2.0; v[1, 0, 7] = 5.0
+    w = custom(q, k, v, [2], softmax_scale=1.0)
+    out, lse = orc.decode_attention(w)
+    s0, s1 = 3.0, -1.25
+    a0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    a1 = 1.0 / (1.0 + math.exp(s0 - s1))
+    expect = a0 * lib_decode(w.v_cache, "f16")[0, 0] + a1 * lib_decode(w.v_cache, "f16")[1, 0]
+    _close(out[0, 0], expect, 1e-14, 1e-15, "two keys out")
+    _close(lse[0, 0], np.logaddexp(s0, s1), 1e-15, 0, "two keys lse")
+
+
+def pin_dominant_key(orc):
+    """One score exceeds all others by at least 40: out equals that key's V
+    row to within e^-40 times the spread of V."""
+    rng = np.random.default_rng(14)
+    T, D = 64, 64
+    q = np.zeros((1, 1, D)); q[0, 0, 9] = 8.0
+    k = rng.uniform(-0.5, 0.5, (T, 1, D)); k[17, 0, 9] = 6.0
+    v = rng.standard_normal((T, 1, D))
+    w = custom(q, k, v, [T], softmax_scale=1.0)
+    out, lse = orc.decode_attention(w)
+    v17 = lib_decode(w.v_cache, "f16")[17, 0]
+    assert np.max(np.abs(out[0, 0] - v17)) < 64 * math.exp(-40) * 10
+    _close(lse[0, 0], 8.0 * float(lib_decode(w.k_cache, "f16")[17, 0, 9]), 1e-12, 0, "dominant lse")
+
+
+def pin_empty_sequence(orc):
+    rng = np.random.default_rng(15)
+    D = 64
+    q = rng.standard_normal((2, 2, D))
+    k = rng.standard_normal((5, 1, D))
+    v = rng.standard_normal((5, 1, D))
+    w = custom(q, k, v, [0, 5], kv_start_idx=[0, 0])
+    out, lse = orc.decode_attention(w)
+    assert np.all(out[0] == 0.0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(out[1])) and np.all(np.isfinite(lse[1]))
+
+
+def pin_weights_sum_to_one(orc):
+    w = fw.make_contiguous("ws", 16, [1, 9, 130], 8, 2, 64, "f16", "e4m3", gap=3)
+    out, lse, weights = orc.decode_attention(w, want_weights=True)
+    for b, T in enumerate(w.seq_len):
+        s = weights[b, :, :T].sum(axis=-1)
+        assert np.all(np.abs(s - 1.0) < 1e-14), s
+        assert np.all(weights[b, :, :T] >= 0)
+
+
+def pin_key_permutation(orc):
+    rng = np.random.default_rng(17)
+    w = fw.make_contiguous("perm", 17, [45, 12], 4, 2, 128, "bf16", "bf16")
+    out, lse = orc.decode_attention(w)
+    k = w.k_cache.copy(); v = w.v_cache.copy()
+    for b in range(w.batch):
+        s, T = int(w.kv_start_idx[b]), int(w.seq_len[b])
+        p = rng.permutation(T)
+        k[s:s + T] = w.k_cache[s:s + T][p]
+        v[s:s + T] = w.v_cache[s:s + T][p]
+    out2, lse2 = orc.decode_attention(dataclasses.replace(w, k_cache=k, v_cache=v))
+    _close(out2, out, 1e-12, 1e-14, "permutation out")
+    _close(lse2, lse, 1e-13, 0, "permutation lse")
+
+
+def pin_gqa_equals_replicated_mha(orc):
+    w = fw.make_contiguous("gqa", 18, [33, 7], 8, 2, 64, "f16", "f16", gap=2)
+    out, lse = orc.decode_attention(w)
+    g = 4
+    k = np.repeat(w.k_cache, g, axis=1)
+    v = np.repeat(w.v_cache, g, axis=1)
+    mha = dataclasses.replace(w, num_kv_heads=8, k_cache=k, v_cache=v)
+    out2, lse2 = orc.decode_attention(mha)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def pin_paged_equals_contiguous(orc):
+    w = fw.make_contiguous("pg", 19, [1, 16, 17, 70], 4, 2, 64, "f16", "e4m3", gap=5)
+    out, lse = orc.decode_attention(w)
+    for P in (1, 4, 16):
+        wp = fw.to_paged(w, P, 19 + P)
+        out2, lse2 = orc.decode_attention(wp)
+        assert np.array_equal(out, out2) and np.array_equal(lse, lse2), P
+
+
+def pin_scale_factors(orc):
+    """v_scale scales out and leaves lse; doubling k_scale equals doubling
+    softmax_scale (both exact in fp64)."""
+    w = fw.make_contiguous("sc", 20, [25, 3], 4, 1, 64, "f16", "e4m3")
+    out, lse = orc.decode_attention(w)
+    out2, lse2 = orc.decode_attention(dataclasses.replace(w, v_scale=np.float32(w.v_scale * 4)))
+    assert np.array_equal(out2, 4 * out) and np.array_equal(lse2, lse)
+    a = orc.decode_attention(dataclasses.replace(w, k_scale=np.float32(w.k_scale * 2)))
+    b = orc.decode_attention(dataclasses.replace(w, softmax_scale=np.float32(w.softmax_scale * 2)))
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert not np.allclose(a[1], lse)
+
+
+def pin_score_shift(orc):
+    """A component shared by every key shifts all scores of a head by the
+    same amount: out is unchanged and lse moves by exactly that amount."""
+    rng = np.random.default_rng(21)
+    T, D = 40, 64
+    q = rng.standard_normal((1, 1, D)); q[0, 0, 0] = 0.0
+    k = rng.standard_normal((T, 1, D)); k[:, 0, 0] = 2.0
+    v = rng.standard_normal((T, 1, D))
+    w = custom(q, k, v, [T], softmax_scale=0.25)
+    out, lse = orc.decode_attention(w)
+    q2 = q.copy(); q2[0, 0, 0] = 1.5
+    w2 = custom(q2, k, v, [T], softmax_scale=0.25)
+    out2, lse2 = orc.decode_attention(w2)
+    _close(out2, out, 1e-12, 1e-14, "shift out")
+    _close(lse2, lse + 0.25 * 1.5 * 2.0, 1e-13, 0, "shift lse")
+
+
+def pin_online_recurrence(orc):
+    """Brute force on small inputs: the oracle equals the chunked online
+    softmax with a split merge to 1e-12 (relative, fp64)."""
+    rng = np.random.default_rng(22)
+    cases = [
+        fw.tiny_mqa(),
+        fw.make_contiguous("a", 23, [1, 2, 63, 64, 65, 200], 8, 2, 128, "f16", "e4m3", gap=4, lead=3),
+        fw.make_contiguous("b", 24, [129, 5], 32, 8, 64, "bf16", "bf16", gap=1),
+        fw.to_paged(fw.make_contiguous("c", 25, [3, 64, 100], 16, 1, 128, "f16", "e4m3"), 16, 26),
+        fw.make_contiguous("d", 27, [0, 31, 0], 4, 4, 64, "f16", "f16"),
+    ]
+    for w in cases:
+        out, lse = orc.decode_attention(w)
+        ref_out, ref_lse = online_reference(w, rng)
+        _close(out, ref_out, 1e-12, 1e-13, f"online out {w.name}")
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(fin, np.isfinite(lse))
+        _close(lse[fin], ref_lse[fin], 1e-12, 1e-13, f"online lse {w.name}")
+
+
+ALL_PINS = [
+    pin_e4m3_codes, pin_f16_codes, pin_bf16_codes, pin_identical_v_rows, pin_single_key,
+    pin_zero_query, pin_identical_k_rows, pin_two_keys, pin_dominant_key, pin_empty_sequence,
+    pin_weights_sum_to_one, pin_key_permutation, pin_gqa_equals_replicated_mha,
+    pin_paged_equals_contiguous, pin_scale_factors, pin_score_shift, pin_online_recurrence,
+]

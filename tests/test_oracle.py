@@ -1,0 +1,66 @@
+"""CPU tests of the fp64 oracle against its pins, plus mutation checks that a
+plausible mistake anywhere in the oracle makes at least one pin fail."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(orc, pin):
+    pin(orc)
+
+
+# (text in fd_oracle.c, replacement, what the mistake is)
+MUTATIONS = [
+    ("dot += qv[d] * (k_scale * kd);", "dot += qv[d] * kd;", "k_scale dropped"),
+    ("s[t] = softmax_scale * dot;", "s[t] = dot;", "softmax_scale dropped"),
+    ("o[d] += wt * (v_scale * vd);", "o[d] += wt * vd;", "v_scale dropped"),
+    ("o[d] += wt * (v_scale * vd);", "o[d] += s[t] * (v_scale * vd);", "weights not normalised"),
+    ("*l = M + log(Z);", "*l = log(Z);", "lse misses the max"),
+    ("*l = M + log(Z);", "*l = M + log(Z) / 2;", "lse wrong log"),
+    ("int kvh = qh / group;", "int kvh = qh % num_kv_heads;", "GQA head map interleaved"),
+    ("row = phys * page_size + t % page_size;", "row = phys * page_size + (t + 1) % page_size;",
+     "page offset shifted"),
+    ("int64_t phys = block_table[(int64_t)b * block_table_stride + t / page_size];",
+     "int64_t phys = block_table[(int64_t)b * block_table_stride];", "always first page"),
+    ("row = (int64_t)kv_start_idx[b] + t;", "row = (int64_t)kv_start_idx[b] + t + 1;",
+     "contiguous row off by one"),
+    ("mag = ldexp(1.0 + (double)m / 8.0, e - 7);", "mag = ldexp(1.0 + (double)m / 8.0, e - 8);",
+     "e4m3 bias"),
+    ("mag = ldexp((double)m / 8.0, -6);", "mag = ldexp((double)m / 8.0, -7);", "e4m3 subnormal"),
+    ("else mag = ldexp(1.0 + (double)m / 128.0, e - 127);",
+     "else mag = ldexp(1.0 + (double)m / 256.0, e - 127);", "bf16 mantissa"),
+    ("for (int t = 0; t < T; ++t) { s[t] = exp(s[t] - M); Z += s[t]; }",
+     "for (int t = 0; t < T; ++t) { s[t] = exp(s[t] - M); Z += s[t] * s[t]; }", "wrong sum"),
+    ("size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;\n        for (int d = 0; d < head_dim; ++d) {\n          double vd",
+     "size_t base = ((size_t)rows[t] * num_kv_heads + 0) * head_dim;\n        for (int d = 0; d < head_dim; ++d) {\n          double vd",
+     "V read from head 0"),
+    ("qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + d);",
+     "qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + (head_dim - 1 - d));",
+     "q transposed"),
+]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[2] for m in MUTATIONS])
+def test_mutated_oracle_fails_a_pin(tmp_path, mutation):
+    old, new, what = mutation
+    src = open(oracle.SOURCE).read()
+    assert old in src, f"mutation anchor missing: {what}"
+    mutated = src.replace(old, new, 1)
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    lib = oracle.compile_source(str(path), str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(orc)
+        except (AssertionError, oracle.OracleError, FloatingPointError, ValueError):
+            caught.append(pin.__name__)
+            break
+    assert caught, f"no pin catches the mutation: {what}"
