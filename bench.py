@@ -1,0 +1,378 @@
+"""Decode-step benchmark: effective HBM GB/s and microseconds per decode step.
+
+One step = one fd_decode_attention call (split kernel + combine kernel) over
+one batch of synthetic, seeded inputs already resident in HBM.  Default
+workload: FP8 paged decode (B=64, lognormal lengths with median 2048 clipped
+to [16, 16384], 64 query / 8 KV heads, D=128, page 64, e4m3 K/V with
+per-tensor scales, fp16 Q/out).  `--config N` picks another of the five
+decode workloads.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the host cores instead (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import fd_workloads as fw  # noqa: E402
+
+METRIC = "decode-attention effective HBM GB/s (% of GB300 peak) and us per decode step"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"])
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w: fw.Workload, budget_s: float):
+    """Times the oracle on whole sequences (all query heads) of the workload,
+    taken in order until about `budget_s` seconds of wall time; returns
+    (GB/s by the algorithmic-bytes formula, threads used, description)."""
+    import oracle
+    orc = oracle.default()
+    done_bytes = 0
+    elapsed = 0.0
+    threads = 0
+    nseq = 0
+    heads = w.num_q_heads
+    per_seq_qo = 2 * heads * w.head_dim * 2
+    for b in range(w.batch):
+        pairs = [(b, h) for h in range(heads)]
+        t0 = time.perf_counter()
+        _, _, _, threads = orc.decode_attention_raw(
+            w.q, w.q_dtype, w.k_cache, w.v_cache, w.kv_dtype, w.seq_len, w.num_q_heads,
+            w.num_kv_heads, w.head_dim, w.softmax_scale, w.k_scale, w.v_scale,
+            kv_start_idx=w.kv_start_idx, block_table=w.block_table, page_size=w.page_size,
+            kv_rows=w.kv_rows, pairs=pairs)
+        elapsed += time.perf_counter() - t0
+        T = int(w.seq_len[b])
+        idx = (4 + 4 * (-(-T // w.page_size))) if w.paged else 8
+        done_bytes += T * w.num_kv_heads * w.head_dim * w.kv_elem_bytes * 2 + per_seq_qo + idx
+        nseq += 1
+        if elapsed >= budget_s:
+            break
+    gbs = done_bytes / elapsed / 1e9 if elapsed > 0 else 0.0
+    desc = (f"{nseq} of {w.batch} sequences (all {heads} query heads each), "
+            f"{done_bytes / 1e6:.1f} MB algorithmic, {elapsed:.2f} s")
+    return gbs, threads, desc, elapsed
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = fw.CONFIGS[args.config]()
+    per_step = []
+    gbs_all = []
+    threads = 0
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        gbs, threads, desc, el = oracle_sample(w, budget_s=2.0)
+        if i >= args.warmup:
+            per_step.append(el)
+            gbs_all.append(gbs)
+    value = statistics.median(gbs_all)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.median(per_step), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": fw.CONFIG_NAMES[args.config]},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": "per step: " + desc},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled: bool):
+        self.proc = None
+        self.path = None
+        self.index = index
+        if not enabled:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ln in open(self.path):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "flash_decoding_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except (ValueError, OSError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel_name: str, config: int):
+    """DRAM bytes per launch of the split kernel from the committed ncu
+    summary, if it was taken on the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except ValueError:
+        return None
+    e = d.get(f"{kernel_name}/config{config}")
+    if not e or e.get("source_digest") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_gpu(args):
+    import torch
+    import flash_decoding_attention_gb300 as fda
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    fda.load_library()
+    fda.fd_set_kernel({"auto": 0, "simt": 1, "mma": 2}[args.kernel])
+
+    w = fw.CONFIGS[args.config]()
+    t = fw.to_torch(w, dev)
+    B, QH, KVH, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    out = torch.empty_like(t["q"])
+    lse = torch.empty((B, QH), dtype=torch.float32, device=dev)
+    ws = fda.alloc_workspace(B, QH, KVH, D, dev)
+    stream = torch.cuda.current_stream(dev)
+    sel = fda.fd_selected_kernel(QH, KVH, D, 0 if w.q_dtype == "f16" else 1,
+                                 {"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype], w.paged,
+                                 max(w.page_size, 1))
+    kname = {1: "simt", 2: "mma"}.get(sel, "none")
+
+    def step():
+        fda.fd_decode_attention(t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"],
+                                t["seq_len"], w.kv_rows, QH, KVH, D, w.page_size,
+                                float(w.softmax_scale), float(w.k_scale), float(w.v_scale), out,
+                                lse, ws, stream)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(2 * l2 // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        flush_r.max()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, info = fda.fd_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error {fda.fd_status_string(st)} info={info}")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    clocks = ClockSampler(local, not args.no_clocks)
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush()
+        fda.fd_set_split_events(*sev[i])
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        fda.fd_set_split_events(None, None)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    split_ms = [a.elapsed_time(b) for a, b in sev]
+    total_ms = sum(step_ms)
+    if pg:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / K
+    alg = w.algorithmic_bytes()
+    value = alg * world / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the public API: pinned host inputs in, result out
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(K, 50))
+    h = fw.to_torch(w, "cpu", pin=True)
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in h.items()}
+    h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
+    def e2e_step():
+        for k, v in h.items():
+            if v is not None:
+                dev_in[k].copy_(v, non_blocking=True)
+        fda.decode_attention(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["seq_len"],
+                             kv_start_idx=dev_in["kv_start_idx"], block_table=dev_in["block_table"],
+                             softmax_scale=float(w.softmax_scale), k_scale=float(w.k_scale),
+                             v_scale=float(w.v_scale), workspace=ws, out=out, lse=lse)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if pg:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_val = alg * world / (e2e_ms * 1e-3) / 1e9
+
+    st, info = fda.fd_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error {fda.fd_status_string(st)} info={info}")
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+    split_avg = sum(split_ms) / K
+    achieved = alg / (split_avg * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "us_per_step_p10_p50_p90": [round(float(np.percentile(step_ms, q)) * 1e3, 2)
+                                    for q in (10, 50, 90)],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3->f16 mma, f32 acc" if w.kv_dtype == "e4m3" else f"{w.kv_dtype} mma, f32 acc",
+        "data": "synthetic",
+        "config": {"workload": fw.CONFIG_NAMES[args.config], "kernel": kname,
+                   "algorithmic_bytes_per_step": alg, "sum_seq_len": int(w.seq_len.sum()),
+                   "l2": "flushed between steps (write then read of 2x L2 buffers, outside the "
+                         "timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": 2 * K,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(kname, args.config),
+                     "kernel": f"split ({kname})", "split_us": round(split_avg * 1e3, 2)},
+        "e2e": {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and args.gpus == 1:
+        gbs, threads, desc, _ = oracle_sample(w, budget_s=15.0)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -294,3 +294,42 @@ CONFIG_NAMES = {
        "D=128, e4m3 KV, page 64, 1.2x permuted pool",
     5: "long-context MQA split-KV: B=4, seq_len 131072, 16/1 heads, D=128, e4m3 KV, contiguous",
 }
+
+
+# ----------------------------------------------------------------------------
+# device copies (marshalling only)
+# ----------------------------------------------------------------------------
+
+def torch_dtypes(w: Workload):
+    import torch
+    qd = torch.float16 if w.q_dtype == "f16" else torch.bfloat16
+    kd = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.uint8}[w.kv_dtype]
+    return qd, kd
+
+
+def to_torch(w: Workload, device="cuda", pin: bool = False) -> dict:
+    """The workload's arrays as torch tensors on ``device`` (16-bit patterns
+    reinterpreted as float16/bfloat16, e4m3 codes as uint8).  With
+    ``device='cpu', pin=True`` the tensors are in pinned host memory."""
+    import torch
+    qd, kd = torch_dtypes(w)
+
+    def mk(a, d=None):
+        a = np.ascontiguousarray(a)
+        if d is not None and a.dtype == np.uint16:
+            t = torch.from_numpy(a.view(np.int16)).view(d)
+        else:
+            t = torch.from_numpy(a)
+        if pin:
+            return t.pin_memory()
+        return t.to(device)
+
+    out = {"q": mk(w.q, qd), "k": mk(w.k_cache, kd), "v": mk(w.v_cache, kd),
+           "seq_len": mk(w.seq_len)}
+    if w.paged:
+        out["block_table"] = mk(w.block_table)
+        out["kv_start_idx"] = None
+    else:
+        out["kv_start_idx"] = mk(w.kv_start_idx)
+        out["block_table"] = None
+    return out

@@ -1,0 +1,323 @@
+// fd_api.cu -- the C ABI: argument validation, kernel choice, workspace
+// sizing, launches and the test/debug hooks declared in fd_attention.h.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "fd_common.cuh"
+
+namespace fd {
+
+// Tensor-core kernel entry points (fd_split_mma.cu).
+bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv_dtype,
+                  int paged, int page_size);
+void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms, int* hc,
+                int* tile, int* grid);
+
+namespace {
+
+std::atomic<int> g_kernel{FD_KERNEL_AUTO};
+thread_local cudaEvent_t t_ev_before = nullptr;
+thread_local cudaEvent_t t_ev_after = nullptr;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int g_dev_sms[kMaxDevices] = {0};
+
+int current_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev_sms[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_dev_sms[dev] = sms;
+  }
+  return g_dev_sms[dev];
+}
+
+struct Config {
+  int kernel;   // FD_KERNEL_SIMT or FD_KERNEL_MMA
+  int hc, hg, hq, tile, grid;
+};
+
+constexpr int kSimtTile = 32;
+
+bool dtypes_ok(int q_dtype, int kv_dtype) {
+  if (q_dtype != FD_F16 && q_dtype != FD_BF16) return false;
+  if (kv_dtype == FD_E4M3) return true;
+  return kv_dtype == q_dtype;
+}
+
+// Chooses the split kernel and its plan shape; false if unsupported.
+bool choose(int pref, int num_q_heads, int num_kv_heads, int head_dim, int q_dtype, int kv_dtype,
+            int paged, int page_size, int sms, Config* c) {
+  if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return false;
+  const int group = num_q_heads / num_kv_heads;
+  if (!dtypes_ok(q_dtype, kv_dtype) || (head_dim != 64 && head_dim != 128)) return false;
+  const bool mma_ok = mma_supports(group, num_kv_heads, head_dim, q_dtype, kv_dtype, paged, page_size);
+  if (pref == FD_KERNEL_MMA || (pref == FD_KERNEL_AUTO && mma_ok)) {
+    if (!mma_ok) return false;
+    c->kernel = FD_KERNEL_MMA;
+    mma_config(group, num_kv_heads, head_dim, kv_dtype, sms, &c->hc, &c->tile, &c->grid);
+    c->hg = num_kv_heads / c->hc;
+    c->hq = c->hc * group;
+    return true;
+  }
+  if (!simt_supports(group, head_dim)) return false;
+  c->kernel = FD_KERNEL_SIMT;
+  c->hc = 1;
+  c->hq = simt_heads_per_stream(group);
+  c->hg = num_q_heads / c->hq;
+  c->tile = kSimtTile;
+  c->grid = sms * simt_ctas_per_sm();
+  return true;
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int log2i(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Gather of the stored K or V slice of every token, with the kernels'
+// addressing (test hook).  CTA b copies sequence b; its destination offset
+// is the sum of the earlier sequences' lengths.
+__global__ void gather_kernel(const Params p, uint8_t* dst, int row_bytes) {
+  const int b = blockIdx.x;
+  long long off = 0;
+  for (int i = 0; i < b; ++i) {
+    int t = __ldg(p.seq_len + i);
+    off += t > 0 ? t : 0;
+  }
+  int T = __ldg(p.seq_len + b);
+  if (T < 0) T = 0;
+  const uint8_t* src = static_cast<const uint8_t*>(p.k);
+  for (int t = 0; t < T; ++t) {
+    const long long row = cache_row(p, b, t);
+    uint8_t* d = dst + (off + t) * row_bytes;
+    for (int x = threadIdx.x; x < row_bytes; x += blockDim.x)
+      d[x] = row >= 0 ? src[row * row_bytes + x] : 0;
+  }
+}
+
+}  // namespace
+}  // namespace fd
+
+using namespace fd;
+
+extern "C" {
+
+const char* fd_status_string(fd_status status) {
+  switch (status) {
+    case FD_OK: return "ok";
+    case FD_ERR_INVALID_ARG: return "invalid argument";
+    case FD_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FD_ERR_CUDA: return "CUDA error";
+    case FD_ERR_DEVICE_BOUNDS: return "device: cache row or page id out of range";
+    case FD_ERR_DEVICE_TIMEOUT: return "device: bounded wait expired";
+  }
+  return "unknown status";
+}
+
+fd_status fd_set_kernel(fd_kernel kernel) {
+  if (kernel != FD_KERNEL_AUTO && kernel != FD_KERNEL_SIMT && kernel != FD_KERNEL_MMA)
+    return FD_ERR_INVALID_ARG;
+  g_kernel.store(kernel);
+  return FD_OK;
+}
+
+int fd_selected_kernel(int num_q_heads, int num_kv_heads, int head_dim, fd_dtype q_dtype,
+                       fd_dtype kv_dtype, int paged, int page_size) {
+  Config c;
+  const int sms = current_sms();
+  if (sms <= 0) return -1;
+  if (!choose(g_kernel.load(), num_q_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, paged,
+              page_size, sms, &c))
+    return -1;
+  return c.kernel;
+}
+
+fd_status fd_set_split_events(fd_event_t before, fd_event_t after) {
+  if ((before == nullptr) != (after == nullptr)) return FD_ERR_INVALID_ARG;
+  t_ev_before = reinterpret_cast<cudaEvent_t>(before);
+  t_ev_after = reinterpret_cast<cudaEvent_t>(after);
+  return FD_OK;
+}
+
+size_t fd_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim) {
+  if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
+    return 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
+  const int sms = current_sms();
+  if (sms <= 0) return 0;
+  size_t need = 0;
+  // Largest layout over every kernel and dtype choice for these sizes.
+  const int dts[4][2] = {{FD_F16, FD_F16}, {FD_BF16, FD_BF16}, {FD_F16, FD_E4M3}, {FD_BF16, FD_E4M3}};
+  for (int pref : {FD_KERNEL_SIMT, FD_KERNEL_MMA}) {
+    for (auto& dt : dts) {
+      for (int paged : {0, 1}) {
+        Config c;
+        if (!choose(pref, num_q_heads, num_kv_heads, head_dim, dt[0], dt[1], paged, 64, sms, &c))
+          continue;
+        WsLayout L = ws_layout(batch * c.hg, c.grid, c.hq, head_dim);
+        if (L.total > need) need = L.total;
+      }
+    }
+  }
+  return need;
+}
+
+fd_status fd_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* kv_start_idx, const int32_t* block_table,
+                              int block_table_stride, const int32_t* seq_len, int64_t kv_rows,
+                              int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                              int page_size, float softmax_scale, float k_scale, float v_scale,
+                              fd_dtype q_dtype, fd_dtype kv_dtype, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, fd_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !seq_len || !out || !workspace) return FD_ERR_INVALID_ARG;
+  if ((kv_start_idx == nullptr) == (block_table == nullptr)) return FD_ERR_INVALID_ARG;
+  if (batch <= 0 || batch > (1 << 24)) return FD_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return FD_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > 128 || num_q_heads > 4096) return FD_ERR_UNSUPPORTED;
+  if (kv_rows <= 0 || kv_rows > (int64_t(1) << 40)) return FD_ERR_INVALID_ARG;
+  const int paged = block_table != nullptr;
+  if (paged) {
+    if (!is_pow2(page_size) || page_size > 256) return FD_ERR_UNSUPPORTED;
+    if (block_table_stride <= 0 || kv_rows % page_size != 0) return FD_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return FD_ERR_INVALID_ARG;
+  if (q_dtype != FD_F16 && q_dtype != FD_BF16) return FD_ERR_INVALID_ARG;
+  if (kv_dtype != FD_F16 && kv_dtype != FD_BF16 && kv_dtype != FD_E4M3) return FD_ERR_INVALID_ARG;
+  if (!dtypes_ok(q_dtype, kv_dtype)) return FD_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return FD_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
+    return FD_ERR_INVALID_ARG;
+
+  const int sms = current_sms();
+  if (sms <= 0) return FD_ERR_CUDA;
+  Config c;
+  if (!choose(g_kernel.load(), num_q_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, paged,
+              page_size, sms, &c))
+    return FD_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(batch * c.hg, c.grid, c.hq, head_dim);
+  if (workspace_bytes < L.total) return FD_ERR_WORKSPACE_TOO_SMALL;
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.kv_start = kv_start_idx;
+  p.block_table = block_table;
+  p.seq_len = seq_len;
+  p.out = out;
+  p.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws = reinterpret_cast<WsHeader*>(ws);
+  p.prefix = reinterpret_cast<int32_t*>(ws + L.prefix_off);
+  p.part_ml = reinterpret_cast<float2*>(ws + L.ml_off);
+  p.part_acc = reinterpret_cast<float*>(ws + L.acc_off);
+  p.kv_rows = kv_rows;
+  p.bt_stride = paged ? block_table_stride : 0;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.page_size = paged ? page_size : 1;
+  p.page_shift = paged ? log2i(page_size) : 0;
+  p.group = num_q_heads / num_kv_heads;
+  p.hc = c.hc;
+  p.hg = c.hg;
+  p.hq = c.hq;
+  p.tile = c.tile;
+  p.grid = c.grid;
+  p.kernel = c.kernel;
+  p.q_dtype = q_dtype;
+  p.kv_dtype = kv_dtype;
+  p.score_scale = softmax_scale * k_scale * kLog2e;
+  p.v_scale = v_scale;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool timed = t_ev_before != nullptr;
+  if (timed && cudaEventRecord(t_ev_before, st) != cudaSuccess) return FD_ERR_CUDA;
+  cudaError_t e = c.kernel == FD_KERNEL_MMA ? launch_split_mma(p, st) : launch_split_simt(p, st);
+  if (e != cudaSuccess) return FD_ERR_CUDA;
+  if (timed && cudaEventRecord(t_ev_after, st) != cudaSuccess) return FD_ERR_CUDA;
+  e = launch_combine(p, st);
+  if (e != cudaSuccess) return FD_ERR_CUDA;
+  return FD_OK;
+}
+
+fd_status fd_check_device_error(void* workspace, fd_stream_t stream, int64_t* info) {
+  if (!workspace) return FD_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  WsHeader h;
+  if (cudaMemcpyAsync(&h, workspace, 16, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FD_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 16, st) != cudaSuccess) return FD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FD_ERR_CUDA;
+  if (info) *info = h.error_info ? (int64_t)(h.error_info - 1) : 0;
+  if (h.error_bits & kErrTimeout) return FD_ERR_DEVICE_TIMEOUT;
+  if (h.error_bits & (kErrBounds | kErrPlan)) return FD_ERR_DEVICE_BOUNDS;
+  return FD_OK;
+}
+
+fd_status fd_debug_read_plan(const void* workspace, fd_stream_t stream, int32_t* plan,
+                             int capacity) {
+  if (!workspace || !plan || capacity < 8) return FD_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  WsHeader h;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FD_ERR_CUDA;
+  std::memcpy(plan, h.plan, sizeof(h.plan));
+  const int S = h.plan[0];
+  if (S < 0 || 8 + S + 1 > capacity) return FD_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(plan + 8, static_cast<const uint8_t*>(workspace) + sizeof(WsHeader),
+                      sizeof(int32_t) * (S + 1), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FD_ERR_CUDA;
+  return FD_OK;
+}
+
+fd_status fd_debug_gather_kv(const void* cache, const int32_t* kv_start_idx,
+                             const int32_t* block_table, int block_table_stride,
+                             const int32_t* seq_len, int64_t kv_rows, int batch,
+                             int num_kv_heads, int head_dim, int page_size, fd_dtype kv_dtype,
+                             void* dst, void* workspace, fd_stream_t stream) {
+  if (!cache || !seq_len || !dst || !workspace || batch <= 0 || num_kv_heads <= 0 ||
+      head_dim <= 0 || kv_rows <= 0)
+    return FD_ERR_INVALID_ARG;
+  if ((kv_start_idx == nullptr) == (block_table == nullptr)) return FD_ERR_INVALID_ARG;
+  if (block_table && (!is_pow2(page_size) || page_size > 256 || block_table_stride <= 0))
+    return FD_ERR_INVALID_ARG;
+  if (kv_dtype != FD_F16 && kv_dtype != FD_BF16 && kv_dtype != FD_E4M3) return FD_ERR_INVALID_ARG;
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.k = cache;
+  p.kv_start = kv_start_idx;
+  p.block_table = block_table;
+  p.bt_stride = block_table ? block_table_stride : 0;
+  p.seq_len = seq_len;
+  p.kv_rows = kv_rows;
+  p.page_size = block_table ? page_size : 1;
+  p.page_shift = block_table ? log2i(page_size) : 0;
+  p.ws = static_cast<WsHeader*>(workspace);
+  const int row_bytes = num_kv_heads * head_dim * (kv_dtype == FD_E4M3 ? 1 : 2);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  gather_kernel<<<batch, 128, 0, st>>>(p, static_cast<uint8_t*>(dst), row_bytes);
+  return cudaGetLastError() == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,285 @@
+// fd_common.cuh -- pieces shared by the split and combine kernels: workspace
+// layout, the device-side split plan, cache addressing, device error flags.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "fd_attention.h"
+
+namespace fd {
+
+// ---------------------------------------------------------------------------
+// Device error word (sticky, in the workspace header)
+// ---------------------------------------------------------------------------
+enum : uint32_t {
+  kErrBounds = 1u,   // cache row or page id outside the cache
+  kErrTimeout = 2u,  // a bounded wait expired
+  kErrPlan = 4u,     // plan does not fit the workspace (more tiles than int32)
+};
+
+struct WsHeader {
+  uint32_t error_bits;
+  uint32_t pad0;
+  unsigned long long error_info;   // first offending value (+1, so 0 = none)
+  int32_t plan[8];                 // see fd_debug_read_plan
+  uint8_t pad[256 - 16 - 32];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace = header | prefix int32[num_streams + 1] | ml float2[2*grid][hq] |
+// acc float[2*grid][hq][head_dim].  Every partial slot belongs to one CTA:
+// slot 2c holds the CTA's first segment when that segment continues a stream
+// begun by an earlier CTA, slot 2c+1 its last segment when a later CTA
+// continues it.
+struct WsLayout {
+  size_t prefix_off, ml_off, acc_off, total;
+};
+
+__host__ __device__ inline WsLayout ws_layout(int num_streams, int grid, int hq, int head_dim) {
+  WsLayout L;
+  L.prefix_off = sizeof(WsHeader);
+  L.ml_off = align_up(L.prefix_off + sizeof(int32_t) * (size_t)(num_streams + 1), 256);
+  L.acc_off = align_up(L.ml_off + sizeof(float2) * 2 * (size_t)grid * hq, 256);
+  L.total = align_up(L.acc_off + sizeof(float) * 2 * (size_t)grid * hq * head_dim, 256);
+  return L;
+}
+
+__device__ inline void raise_error(WsHeader* h, uint32_t bit, long long info) {
+  atomicOr(&h->error_bits, bit);
+  atomicCAS(&h->error_info, 0ull, (unsigned long long)(info + 1));
+}
+
+// ---------------------------------------------------------------------------
+// Parameters of one decode call (same struct for every kernel)
+// ---------------------------------------------------------------------------
+struct Params {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* kv_start;
+  const int32_t* block_table;
+  const int32_t* seq_len;
+  void* out;
+  float* lse;
+  WsHeader* ws;
+  int32_t* prefix;
+  float2* part_ml;
+  float* part_acc;
+  long long kv_rows;
+  int bt_stride;
+  int batch, num_q_heads, num_kv_heads, head_dim, page_size, page_shift;
+  int group;        // query heads per KV head
+  int hc;           // KV heads per work stream (tensor-core kernel; 1 otherwise)
+  int hg;           // work streams per sequence
+  int hq;           // query heads per work stream; stream j of a sequence
+                    // serves query heads [j * hq, (j + 1) * hq)
+  int tile;         // tokens per plan tile
+  int grid;         // CTAs of the split kernel
+  int kernel;       // fd_kernel of the split kernel
+  int q_dtype, kv_dtype;   // fd_dtype
+  float score_scale;   // softmax_scale * k_scale * log2(e)  (scores in log2 units)
+  float v_scale;
+};
+
+// ---------------------------------------------------------------------------
+// Split plan ("stream-K" over tiles).  A work stream is (sequence b, a run of
+// hq consecutive query heads and the KV heads they read); stream s = b * hg + j.  Stream s has n_s = ceil(T_b / tile)
+// tiles; the streams' tiles are concatenated in stream order and CTA c takes
+// global tiles [c * L, min(N, (c + 1) * L)) with N = sum n_s and
+// L = ceil(N / grid).  The piece of a stream inside one CTA is a segment.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int stream_tokens(const Params& p, int s) {
+  int t = __ldg(p.seq_len + s / p.hg);
+  return t > 0 ? t : 0;
+}
+
+__device__ __forceinline__ int stream_tiles(const Params& p, int s) {
+  return (stream_tokens(p, s) + p.tile - 1) / p.tile;
+}
+
+struct PlanResult {
+  long long total;      // N
+  long long per_cta;    // L
+  int s_first;          // first stream with a tile in this CTA (or num_streams)
+  long long p_first;    // prefix of s_first
+};
+
+// Block-wide; every thread gets the same result.  CTA 0 also writes the
+// prefix array and the plan words of the header.  `red` is >= 34 long longs
+// of shared memory.
+__device__ inline PlanResult compute_plan(const Params& p, long long* red) {
+  const int S = p.batch * p.hg;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  // pass 1: total tiles
+  long long acc = 0;
+  for (int s = tid; s < S; s += blockDim.x) acc += stream_tiles(p, s);
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  long long total = 0;
+  for (int w = 0; w < nwarps; ++w) total += red[w];
+  __syncthreads();
+  PlanResult r;
+  r.total = total;
+  r.per_cta = total > 0 ? (total + p.grid - 1) / p.grid : 0;
+  const long long target = (long long)blockIdx.x * r.per_cta;
+  const bool has_work = target < total;
+  // pass 2: exclusive prefix, position of this CTA's first tile
+  if (tid == 0) { red[32] = S; }
+  long long carry = 0;
+  for (int base = 0; base < S; base += blockDim.x) {
+    int s = base + tid;
+    long long v = s < S ? stream_tiles(p, s) : 0;
+    long long x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      long long y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) red[warp] = x;
+    __syncthreads();
+    long long woff = 0, ctot = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      if (w < warp) woff += red[w];
+      ctot += red[w];
+    }
+    long long excl = carry + woff + x - v;
+    if (s < S) {
+      if (blockIdx.x == 0) p.prefix[s] = (int32_t)excl;
+      if (has_work && v > 0 && excl <= target && target < excl + v) {
+        red[32] = s;
+        red[33] = excl;
+      }
+    }
+    carry += ctot;
+    __syncthreads();
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    p.prefix[S] = (int32_t)total;
+    p.ws->plan[0] = S;
+    p.ws->plan[1] = p.hg;
+    p.ws->plan[2] = p.tile;
+    p.ws->plan[3] = p.grid;
+    p.ws->plan[4] = (int32_t)total;
+    p.ws->plan[5] = (int32_t)r.per_cta;
+    p.ws->plan[6] = p.kernel;
+    p.ws->plan[7] = 0;
+    if (total > 0x7fffffffLL) raise_error(p.ws, kErrPlan, total);
+  }
+  r.s_first = has_work ? (int)red[32] : S;
+  r.p_first = has_work ? red[33] : total;
+  __syncthreads();
+  return r;
+}
+
+// One segment: stream s, tokens [t_begin, t_end), global tiles [g_begin, g_end).
+struct Segment {
+  int s;
+  int t_begin, t_end;
+  int T;                // stream length
+  bool complete;        // the whole stream is inside this CTA
+  int slot;             // partial slot if !complete
+};
+
+// Iterates the segments of one CTA; every thread of a warp (or block) that
+// uses it sees the same sequence.
+struct SegmentIter {
+  long long g, g_end;   // next global tile, end of this CTA's range
+  int s;                // stream holding tile g
+  long long ps;         // prefix of s
+  int S;
+
+  __device__ void init(const Params& p, const PlanResult& r) {
+    S = p.batch * p.hg;
+    g = (long long)blockIdx.x * r.per_cta;
+    g_end = g + r.per_cta;
+    if (g_end > r.total) g_end = r.total;
+    s = r.s_first;
+    ps = r.p_first;
+  }
+  // Returns false when the CTA has no more segments.
+  __device__ bool next(const Params& p, Segment& seg) {
+    if (g >= g_end || s >= S) return false;
+    int ns = stream_tiles(p, s);
+    while (g >= ps + ns) {   // skip empty / finished streams
+      ps += ns;
+      ++s;
+      if (s >= S) return false;
+      ns = stream_tiles(p, s);
+    }
+    long long a = g, e = ps + ns < g_end ? ps + ns : g_end;
+    seg.s = s;
+    seg.T = stream_tokens(p, s);
+    seg.t_begin = (int)((a - ps) * p.tile);
+    long long te = (e - ps) * p.tile;
+    seg.t_end = te < seg.T ? (int)te : seg.T;
+    bool starts_mid = a > ps;
+    bool ends_mid = e < ps + ns;
+    seg.complete = !starts_mid && !ends_mid;
+    seg.slot = 2 * (int)blockIdx.x + (starts_mid ? 0 : 1);
+    g = e;
+    return true;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Cache addressing (the one place the library maps tokens to rows)
+// ---------------------------------------------------------------------------
+// Row of token t of sequence b, or -1 (recorded as a device error) when the
+// row or page id lies outside the cache.
+__device__ __forceinline__ long long cache_row(const Params& p, int b, int t) {
+  long long row;
+  if (p.block_table) {
+    int page = __ldg(p.block_table + (long long)b * p.bt_stride + (t >> p.page_shift));
+    row = ((long long)page << p.page_shift) + (t & (p.page_size - 1));
+    if (page < 0 || row >= p.kv_rows) {
+      raise_error(p.ws, kErrBounds, page);
+      return -1;
+    }
+  } else {
+    row = (long long)__ldg(p.kv_start + b) + t;
+    if (row < 0 || row >= p.kv_rows) {
+      raise_error(p.ws, kErrBounds, row);
+      return -1;
+    }
+  }
+  return row;
+}
+
+// ---------------------------------------------------------------------------
+// Small math helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <typename T> struct QType;
+template <> struct QType<__half> {
+  static __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ __half from_f32(float x) { return __float2half_rn(x); }
+};
+template <> struct QType<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
+};
+
+// Launchers (defined in their .cu files).
+cudaError_t launch_split_simt(const Params& p, cudaStream_t stream);
+cudaError_t launch_split_mma(const Params& p, cudaStream_t stream);
+cudaError_t launch_combine(const Params& p, cudaStream_t stream);
+int simt_ctas_per_sm();
+bool simt_supports(int group, int head_dim);
+int simt_heads_per_stream(int group);
+
+}  // namespace fd

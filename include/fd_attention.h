@@ -1,0 +1,198 @@
+/*
+ * fd_attention.h -- C ABI of the GB300 (sm_103a) flash-decoding library.
+ *
+ * One decode step of attention: every sequence b of a batch contributes one
+ * query token per query head, which attends over that sequence's cached
+ * keys and values.  The cache is token-major and either contiguous (a
+ * sequence owns a run of rows starting at kv_start_idx[b]) or paged (a block
+ * table maps the sequence's logical pages to physical pages of a pool).
+ * K and V are fp16, bf16 or FP8-e4m3 with one fp32 scale per tensor.
+ *
+ * The computation is split-KV partial attention with an online softmax
+ * (running max, running sum, rescaled accumulator) followed by a
+ * log-sum-exp merge of the partial states, for MHA, GQA and MQA head layouts.
+ *
+ * Passages that define the operation:
+ *  - "From SGLang kernel source to GPU trace: DeepSeek V4.1 Flash-Decode",
+ *    section 3.1: the decode kernel's arguments (q, FP8 k_cache/v_cache,
+ *    output, kv_start_idx and seq_len per sequence, head count, head
+ *    dimension, softmax scale, batch); section 2.2: FP8 KV converted inside
+ *    the load stage, not by a separate pass;
+ *  - "SGLang Prefill optimisation: dissecting FlashAttention kernel
+ *    bottlenecks with GPU Trace", section 2.2: the online softmax loop
+ *    (scores = dot(q, k) * scale, running max, rescale factor
+ *    exp(m_old - m_new), running sum, accumulator update);
+ *  - "Learn CUDA from scratch, chapter 15: GPU profiling and LLM inference",
+ *    section 15.26: paged addressing (physical page from the block table,
+ *    row = page * page_size + offset in a [page, offset, head, dim] pool);
+ *    section 15.12: one pass over a KV head serves its group of
+ *    QH / KVH query heads; section 15.13: a ragged batch scans each
+ *    sequence's real length only.
+ *
+ * Conventions (readings where the pages are silent):
+ *  - q and out are dense [batch, num_q_heads, head_dim]; lse is dense fp32
+ *    [batch, num_q_heads];
+ *  - contiguous K/V: [kv_rows, num_kv_heads, head_dim], kv_start_idx in rows;
+ *    paged K/V: [num_pages, page_size, num_kv_heads, head_dim],
+ *    block_table row-major [batch, block_table_stride] of int32 page ids;
+ *  - query head qh reads KV head qh / (num_q_heads / num_kv_heads);
+ *  - k = k_scale * stored(k), v = v_scale * stored(v) (pass 1.0 for 16-bit
+ *    caches); score = softmax_scale * dot(q, k);
+ *  - lse = natural log of sum_t exp(score_t); a sequence with seq_len 0
+ *    gets out = 0 and lse = -inf;
+ *  - out is rounded once, to nearest even, into q's dtype.
+ *
+ * Ownership and synchronisation: every pointer argument is device memory
+ * owned by the caller (except where a function says "host").  The library
+ * allocates, frees and synchronises nothing inside fd_decode_attention; all
+ * of its work is enqueued on `stream`.  The workspace is caller-owned scratch
+ * memory of at least fd_workspace_bytes(...) bytes; it holds no state that
+ * the caller must keep between calls except the sticky device-error word
+ * read by fd_check_device_error.  Calls that share one workspace must be
+ * ordered on one stream.
+ */
+#ifndef FD_ATTENTION_H_
+#define FD_ATTENTION_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as a cudaStream_t / CUstream (NULL = the legacy default stream). */
+typedef struct CUstream_st *fd_stream_t;
+/* Same object as a cudaEvent_t / CUevent. */
+typedef struct CUevent_st *fd_event_t;
+
+typedef enum {
+  FD_OK = 0,
+  FD_ERR_INVALID_ARG = 1,          /* bad pointer, size or layout; nothing launched */
+  FD_ERR_UNSUPPORTED = 2,          /* valid but not implemented (head_dim, dtype pair, ...) */
+  FD_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < fd_workspace_bytes(...) */
+  FD_ERR_CUDA = 4,                 /* a CUDA runtime call or launch failed */
+  FD_ERR_DEVICE_BOUNDS = 5,        /* a kernel met a cache row / page id out of range */
+  FD_ERR_DEVICE_TIMEOUT = 6        /* a kernel's bounded wait expired */
+} fd_status;
+
+typedef enum { FD_F16 = 0, FD_BF16 = 1, FD_E4M3 = 2 } fd_dtype;
+
+/* Kernel selection for the split (partial attention) phase. */
+typedef enum {
+  FD_KERNEL_AUTO = 0,  /* tensor-core kernel where supported, else CUDA-core kernel */
+  FD_KERNEL_SIMT = 1,  /* CUDA-core FMA kernel (every supported shape) */
+  FD_KERNEL_MMA = 2    /* tensor-core kernel; FD_ERR_UNSUPPORTED where it does not apply */
+} fd_kernel;
+
+/*
+ * Scratch bytes fd_decode_attention needs for these sizes on the current
+ * device (host function, no device work).  Returns 0 for invalid sizes.
+ * The figure covers the partial (m, l, acc) states of the split phase, the
+ * per-stream tile prefix of the split plan and a 256-byte header; it grows
+ * with the device's SM count, not with sequence lengths.
+ */
+size_t fd_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim);
+
+/*
+ * One decode step of attention (see the file comment for the definition).
+ *
+ * q            [batch, num_q_heads, head_dim] of q_dtype (FD_F16 or FD_BF16).
+ * k_cache, v_cache
+ *              contiguous: [kv_rows, num_kv_heads, head_dim] of kv_dtype;
+ *              paged: [kv_rows / page_size, page_size, num_kv_heads, head_dim].
+ *              Base addresses 16-byte aligned.
+ * kv_start_idx int32 [batch] first row of each sequence (contiguous mode), or NULL.
+ * block_table  int32 [batch, block_table_stride] page ids (paged mode), or NULL.
+ *              Exactly one of kv_start_idx / block_table is non-NULL.  Entries
+ *              past ceil(seq_len[b] / page_size) are never read.
+ * seq_len      int32 [batch] tokens per sequence (0 allowed; negative = 0).
+ * kv_rows      number of token rows K and V hold (paged: pages * page_size).
+ *              Rows outside [0, kv_rows) are never read: the kernel records
+ *              FD_ERR_DEVICE_BOUNDS in the workspace and treats the token as
+ *              absent.
+ * num_q_heads, num_kv_heads
+ *              num_q_heads % num_kv_heads == 0; group = num_q_heads / num_kv_heads <= 128.
+ * head_dim     64 or 128.
+ * page_size    paged mode: power of two in [1, 256]; contiguous mode: ignored.
+ * softmax_scale, k_scale, v_scale
+ *              finite fp32 factors (scores use softmax_scale * k_scale).
+ * kv_dtype     FD_F16 (with q FD_F16), FD_BF16 (with q FD_BF16) or FD_E4M3
+ *              (OCP e4m3fn, with either q dtype).
+ * out          [batch, num_q_heads, head_dim] of q_dtype.
+ * lse          fp32 [batch, num_q_heads], or NULL if not wanted.
+ * workspace    device scratch of workspace_bytes >= fd_workspace_bytes(...),
+ *              256-byte aligned.
+ *
+ * Returns FD_OK once the work is enqueued; argument errors return before any
+ * launch.  Device-side index errors surface through fd_check_device_error.
+ */
+fd_status fd_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *kv_start_idx, const int32_t *block_table,
+                              int block_table_stride, const int32_t *seq_len, int64_t kv_rows,
+                              int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                              int page_size, float softmax_scale, float k_scale, float v_scale,
+                              fd_dtype q_dtype, fd_dtype kv_dtype, void *out, float *lse,
+                              void *workspace, size_t workspace_bytes, fd_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads and clears the workspace's sticky device-error
+ * word.  Returns FD_OK, FD_ERR_DEVICE_BOUNDS, FD_ERR_DEVICE_TIMEOUT or
+ * FD_ERR_CUDA.  If info is not NULL it receives the first offending value
+ * (a row or page id) or 0.
+ */
+fd_status fd_check_device_error(void *workspace, fd_stream_t stream, int64_t *info);
+
+/* Static English text for a status code. */
+const char *fd_status_string(fd_status status);
+
+/* Process-wide choice of the split kernel (default FD_KERNEL_AUTO). */
+fd_status fd_set_kernel(fd_kernel kernel);
+
+/*
+ * Kernel that fd_decode_attention would run for these sizes under the
+ * current fd_set_kernel choice: FD_KERNEL_SIMT or FD_KERNEL_MMA, or -1 if
+ * the sizes are unsupported.  Host function.
+ */
+int fd_selected_kernel(int num_q_heads, int num_kv_heads, int head_dim, fd_dtype q_dtype,
+                       fd_dtype kv_dtype, int paged, int page_size);
+
+/*
+ * Profiling hook: when both events are non-NULL, fd_decode_attention records
+ * `before` immediately before and `after` immediately after the split
+ * kernel's launch on its stream, so that the split kernel can be timed by
+ * itself.  NULL, NULL switches it off.  The setting is per host thread.
+ */
+fd_status fd_set_split_events(fd_event_t before, fd_event_t after);
+
+/*
+ * Test hook: copies the split plan of the last fd_decode_attention call that
+ * used this workspace into host memory (synchronises `stream`).
+ * plan[0..7] = {num_streams, streams_per_sequence, tile_tokens, grid,
+ * total_tiles, tiles_per_cta, kernel, 0}; stream j of sequence b serves
+ * query heads [j * h, (j + 1) * h) with h = num_q_heads / streams_per_sequence;
+ * plan[8 .. 8 + num_streams] = exclusive prefix of tiles per stream
+ * (num_streams + 1 values).  capacity = number of int32 that fit in plan.
+ */
+fd_status fd_debug_read_plan(const void *workspace, fd_stream_t stream, int32_t *plan,
+                             int capacity);
+
+/*
+ * Test hook: gathers, with the kernels' own addressing, the stored K (or V)
+ * row slice of every token of every sequence into dst, a dense device array
+ * [sum_b seq_len[b], num_kv_heads, head_dim] of the cache element type,
+ * sequences in order.  Rows out of range are written as zero bytes and
+ * recorded like in fd_decode_attention.  Same layout arguments as
+ * fd_decode_attention; workspace needs only the 256-byte header.
+ */
+fd_status fd_debug_gather_kv(const void *cache, const int32_t *kv_start_idx,
+                             const int32_t *block_table, int block_table_stride,
+                             const int32_t *seq_len, int64_t kv_rows, int batch,
+                             int num_kv_heads, int head_dim, int page_size, fd_dtype kv_dtype,
+                             void *dst, void *workspace, fd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_ATTENTION_H_ */

@@ -1,0 +1,69 @@
+"""Independent restatement of the library's split plan (stream-K over tiles).
+
+A work stream is (sequence b, one group of `hc` KV heads); there are
+hg = num_kv_heads / hc streams per sequence, numbered s = b * hg + j.
+Stream s has n_s = ceil(max(T_b, 0) / tile) tiles.  The tiles of all streams,
+concatenated in stream order, are dealt to `grid` CTAs in equal contiguous
+runs of L = ceil(N / grid) tiles (N = sum n_s).  The part of a stream inside
+one CTA is a segment; a segment that is not the whole stream stores a partial
+state in slot 2c (it continues a stream begun in an earlier CTA) or 2c + 1
+(its stream continues in a later CTA).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List
+
+
+@dataclass
+class Seg:
+    cta: int
+    stream: int
+    t_begin: int
+    t_end: int
+    complete: bool
+    slot: int
+
+
+def tiles_per_stream(seq_len, hg: int, tile: int) -> List[int]:
+    out = []
+    for T in seq_len:
+        T = max(int(T), 0)
+        n = -(-T // tile)
+        out.extend([n] * hg)
+    return out
+
+
+def plan(seq_len, hg: int, tile: int, grid: int):
+    """Returns (prefix [S+1], total, per_cta, segments)."""
+    n = tiles_per_stream(seq_len, hg, tile)
+    prefix = [0]
+    for x in n:
+        prefix.append(prefix[-1] + x)
+    total = prefix[-1]
+    per_cta = -(-total // grid) if total else 0
+    segs = []
+    for c in range(grid):
+        g0, g1 = c * per_cta, min(total, (c + 1) * per_cta)
+        for s in range(len(n)):
+            a, e = max(g0, prefix[s]), min(g1, prefix[s + 1])
+            if a >= e:
+                continue
+            T = max(int(seq_len[s // hg]), 0)
+            starts_mid = a > prefix[s]
+            ends_mid = e < prefix[s + 1]
+            segs.append(Seg(c, s, (a - prefix[s]) * tile, min((e - prefix[s]) * tile, T),
+                            not starts_mid and not ends_mid, 2 * c + (0 if starts_mid else 1)))
+    return prefix, total, per_cta, segs
+
+
+def merge_slots(prefix, total, grid, s):
+    """Slots the combine step merges for stream s ([] if the stream is empty
+    or held by one CTA)."""
+    if prefix[s + 1] == prefix[s]:
+        return []
+    per_cta = -(-total // grid)
+    c0, c1 = prefix[s] // per_cta, (prefix[s + 1] - 1) // per_cta
+    if c0 == c1:
+        return []
+    return [2 * c0 + 1] + [2 * c for c in range(c0 + 1, c1 + 1)]

@@ -1,0 +1,90 @@
+"""CPU checks of the C ABI: the library builds and loads, exports every
+function include/fd_attention.h declares, and rejects bad arguments on the
+host before any launch (these calls never reach the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fd_attention.h")
+
+
+@pytest.fixture(scope="module")
+def fda():
+    from flash_decoding_attention_gb300 import build
+    build.build()
+    import flash_decoding_attention_gb300 as m
+    m.load_library()
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ["fd_decode_attention", "fd_workspace_bytes", "fd_check_device_error",
+              "fd_status_string", "fd_debug_read_plan", "fd_debug_gather_kv"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fda):
+    lib = ctypes.CDLL(fda.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert sorted(fda.EXPORTED) == declared_functions()
+
+
+def test_status_strings(fda):
+    for st in range(7):
+        assert fda.fd_status_string(st)
+    assert fda.fd_status_string(99) == "unknown status"
+
+
+def _call(fda, **over):
+    """fd_decode_attention with fake (never dereferenced) device pointers."""
+    lib = fda.load_library()
+    a = dict(q=0x1000, k=0x2000, v=0x3000, kv_start=0x4000, bt=None, bt_stride=0,
+             seq_len=0x5000, kv_rows=100, batch=2, qh=8, kvh=2, d=128, page=0,
+             ss=0.125, ks=1.0, vs=1.0, qdt=0, kvdt=0, out=0x6000, lse=0x7000, ws=0x8000,
+             wsb=1 << 20, stream=None)
+    a.update(over)
+    return lib.fd_decode_attention(a["q"], a["k"], a["v"], a["kv_start"], a["bt"], a["bt_stride"],
+                                   a["seq_len"], a["kv_rows"], a["batch"], a["qh"], a["kvh"],
+                                   a["d"], a["page"], a["ss"], a["ks"], a["vs"], a["qdt"],
+                                   a["kvdt"], a["out"], a["lse"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=None), 1),
+    (dict(k=None), 1),
+    (dict(seq_len=None), 1),
+    (dict(out=None), 1),
+    (dict(ws=None), 1),
+    (dict(bt=0x9000, bt_stride=4, page=16), 1),          # both layouts given
+    (dict(kv_start=None), 1),                              # neither layout
+    (dict(batch=0), 1),
+    (dict(qh=6, kvh=4), 1),                                # heads not divisible
+    (dict(d=96), 2),                                       # unsupported head_dim
+    (dict(kv_start=None, bt=0x9000, bt_stride=4, page=48, kv_rows=96), 2),   # page not pow2
+    (dict(kv_start=None, bt=0x9000, bt_stride=0, page=16, kv_rows=96), 1),   # bad stride
+    (dict(kv_start=None, bt=0x9000, bt_stride=4, page=16, kv_rows=100), 1),  # rows % page
+    (dict(kv_rows=0), 1),
+    (dict(qdt=2), 1),                                      # q cannot be e4m3
+    (dict(qdt=0, kvdt=1), 2),                              # f16 q with bf16 cache
+    (dict(ss=float("nan")), 1),
+    (dict(q=0x1001), 1),                                   # misaligned q
+    (dict(ws=0x8010), 1),                                  # misaligned workspace
+])
+def test_host_validation(fda, over, status):
+    assert _call(fda, **over) == status
+
+
+def test_set_kernel_rejects_unknown(fda):
+    assert fda.load_library().fd_set_kernel(7) == 1
+    assert fda.load_library().fd_set_kernel(0) == 0

@@ -1,0 +1,136 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs, for the five decode workloads at full size and for
+edge cases (empty and one-token sequences, lengths around tile and page
+boundaries, poisoned gaps and pages, every head grouping, both head
+dimensions, every dtype pair, page sizes 1 .. 256)."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import fd_workloads as fw
+import oracle
+from gpu_util import lib, parity, run
+
+pytestmark = pytest.mark.gpu
+
+SIMT, MMA = 1, 2
+
+
+def kernels_for(w):
+    fda = lib()
+    ks = []
+    for k in (SIMT, MMA):
+        fda.fd_set_kernel(k)
+        sel = fda.fd_selected_kernel(w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                     0 if w.q_dtype == "f16" else 1,
+                                     {"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype], w.paged,
+                                     max(w.page_size, 1))
+        fda.fd_set_kernel(0)
+        if sel == k:
+            ks.append(k)
+    return ks
+
+
+@functools.lru_cache(maxsize=None)
+def config(n):
+    return fw.CONFIGS[n]()
+
+
+@functools.lru_cache(maxsize=None)
+def oracle_of(n):
+    return oracle.decode_attention(config(n))
+
+
+def check_workload(w, ref=None, label=""):
+    if ref is None:
+        ref = oracle.decode_attention(w)
+    ks = kernels_for(w)
+    assert ks, "no kernel supports this case"
+    for k in ks:
+        out, lse, _, _ = run(w, k)
+        parity(w, out, lse, ref[0], ref[1], label=f"{label or w.name} kernel={k}")
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_config_full_size(n):
+    check_workload(config(n), oracle_of(n), label=f"config{n}")
+
+
+EDGE_LENGTHS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 1000]
+
+
+@pytest.mark.parametrize("q_dtype,kv_dtype", [("f16", "f16"), ("bf16", "bf16"), ("f16", "e4m3"),
+                                              ("bf16", "e4m3")])
+@pytest.mark.parametrize("D", [64, 128])
+def test_edge_lengths_with_poisoned_gaps(q_dtype, kv_dtype, D):
+    w = fw.make_contiguous(f"edge-{q_dtype}-{kv_dtype}-{D}", 100 + D, EDGE_LENGTHS, 8, 2, D,
+                           q_dtype, kv_dtype, gap=3, lead=5, tail=7)
+    check_workload(w)
+
+
+@pytest.mark.parametrize("qh,kvh", [(8, 8), (8, 4), (16, 4), (32, 4), (64, 8), (16, 1), (32, 1),
+                                    (64, 1), (128, 1), (12, 3), (40, 5)])
+def test_head_groupings(qh, kvh):
+    w = fw.make_contiguous(f"heads-{qh}-{kvh}", 200 + qh + kvh, [5, 130, 777], qh, kvh, 128,
+                           "f16", "e4m3", gap=2)
+    check_workload(w)
+
+
+@pytest.mark.parametrize("P", [1, 2, 16, 32, 64, 128, 256])
+def test_paged_page_sizes(P):
+    lens = [1, P - 1 if P > 1 else 2, P, P + 1, 3 * P + 5, 700]
+    base = fw.make_contiguous(f"paged{P}", 300 + P, lens, 16, 2, 128, "f16", "e4m3")
+    w = fw.to_paged(base, P, 301 + P, extra_stride=2)
+    check_workload(w)
+
+
+def test_all_sequences_empty():
+    w = fw.make_contiguous("empty", 7, [0, 0, 0], 8, 2, 128, "f16", "f16")
+    ref = oracle.decode_attention(w)
+    for k in kernels_for(w):
+        out, lse, _, _ = run(w, k)
+        assert np.all(out == 0) and np.all(np.isneginf(lse))
+        parity(w, out, lse, ref[0], ref[1], label=f"empty kernel={k}")
+
+
+def test_many_short_sequences():
+    rng = np.random.default_rng(8)
+    lens = rng.integers(0, 40, size=600)
+    w = fw.make_contiguous("many-short", 8, lens, 32, 8, 128, "bf16", "e4m3", gap=1)
+    check_workload(w)
+
+
+def test_one_long_sequence_many_splits():
+    w = fw.make_contiguous("one-long", 9, [200_003], 16, 1, 128, "f16", "e4m3")
+    check_workload(w)
+
+
+def test_paged_equals_contiguous_bitwise():
+    base = fw.make_contiguous("pc", 10, [1, 64, 65, 1000, 4097], 64, 8, 128, "f16", "e4m3")
+    paged = fw.to_paged(base, 64, 11)
+    for k in kernels_for(base):
+        if k not in kernels_for(paged):
+            continue
+        _, _, o1, l1 = run(base, k)
+        _, _, o2, l2 = run(paged, k)
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)), f"kernel={k}"
+        assert torch.equal(l1.view(torch.int32), l2.view(torch.int32)), f"kernel={k}"
+
+
+def test_repeated_calls_are_bitwise_identical():
+    w = config(4)
+    for k in kernels_for(w):
+        _, _, o1, l1 = run(w, k)
+        _, _, o2, l2 = run(w, k)
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+        assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_nondefault_stream():
+    w = fw.make_contiguous("stream", 12, [100, 2000], 16, 2, 128, "f16", "e4m3")
+    ref = oracle.decode_attention(w)
+    s = torch.cuda.Stream()
+    out, lse, _, _ = run(w, 0, stream=s)
+    parity(w, out, lse, ref[0], ref[1], label="side stream")
