@@ -258,6 +258,9 @@ def run_gpu(args):
           for _ in range(K)]
     sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
+    for a, b in sev:           # torch creates the CUDA events on first record
+        a.record(stream)
+        b.record(stream)
     clocks = ClockSampler(local, not args.no_clocks)
     time.sleep(0.3)
     if pg:

@@ -1,16 +1,843 @@
-// fd_split_mma.cu -- split kernel on tensor cores (placeholder until written).
+// fd_split_mma.cu -- split (partial attention) kernel on tensor cores, fed by
+// TMA through a multi-stage shared-memory pipeline.
+//
+// What it computes is the same online softmax state as the CUDA-core kernel
+// (running max m in log2 units, running sum l, rescaled V accumulator) for
+// each segment of the stream-K split plan: the online softmax loop of
+// "SGLang Prefill optimisation: dissecting FlashAttention kernel bottlenecks
+// with GPU Trace", section 2.2, with one query row per head.  One pass over
+// a KV tile serves all query heads of its group ("Learn CUDA from scratch,
+// chapter 15", section 15.12), and FP8 K/V are converted inside the load
+// path ("From SGLang kernel source to GPU trace: DeepSeek V4.1
+// Flash-Decode", section 2.2).
+//
+// Work split inside a CTA (one persistent CTA per SM, 8 warps):
+//  - thread 0 also walks the CTA's tiles ahead of the others and, per stage,
+//    issues TMA tensor loads of the K and V rows of `tile` tokens for the
+//    stream's hc KV heads into shared memory (128-byte swizzle, or 64-byte
+//    for 64-byte rows), completing on the stage's "full" mbarrier; it refills
+//    a stage once all 8 warps have released it on its "empty" mbarrier;
+//  - warp w owns head tile w / wph (16 query heads of one KV head) and the
+//    w % wph-th run of 16 * r tokens of every stage.
+//    Per 16-token sub-tile it computes S = Q K^T with m16n8k16 MMAs (query
+//    heads are the M rows, tokens the N columns, head dims the K depth),
+//    the online softmax update in registers, and O += P V with P taken
+//    straight from the S accumulators (tokens become the K depth), then
+//    releases the stage on its "empty" mbarrier.
+// FP8 bytes are widened to f16 (or bf16) pairs in registers right before the
+// MMAs.  The head-dim order inside each MMA is permuted consistently on Q and
+// K (a dot product does not depend on it), and the token and head-dim orders
+// of the V operand are chosen so that every shared-memory load is a 16-byte,
+// bank-conflict-free access under the TMA swizzle.
+//
+// Every wait is bounded (about one second); on expiry the kernel records
+// kErrTimeout, stops issuing copies, drains the copies it issued and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
 #include "fd_common.cuh"
 
 namespace fd {
+namespace {
 
-bool mma_supports(int, int, int, int, int, int, int) { return false; }
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 225 * 1024;
+constexpr unsigned long long kWaitNs = 1000000000ull;
 
-void mma_config(int, int, int, int, int sms, int* hc, int* tile, int* grid) {
-  *hc = 1;
-  *tile = 16;
+struct Shape {
+  int mt;            // 16-row head tiles per KV head (power of two)
+  int hc;            // KV heads per stream
+  int wph;           // consumer warps per head tile
+  int r;             // 16-token sub-tiles per warp per stage
+  int tile;          // tokens per stage = 16 * wph * r
+  int box_rows;      // rows per TMA box
+  int row_bytes;     // bytes of one swizzled row of a box (128 or 64)
+  int nx;            // boxes across head_dim (head_dim * elem / row_bytes)
+  int region_bytes;  // tile * row_bytes
+  int kv_bytes;      // K (or V) bytes of one stage = hc * nx * region_bytes
+  int stages;
+  int merge_bytes;
+  int smem_bytes;
+};
+
+__host__ __device__ inline int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int page_size) {
+  Shape s;
+  const int elem = kv_dtype == FD_E4M3 ? 1 : 2;
+  s.mt = next_pow2((group + 15) / 16);
+  int hc = kWarps / s.mt;
+  while (hc > 1 && num_kv_heads % hc != 0) hc >>= 1;
+  s.hc = hc;
+  s.wph = kWarps / (s.mt * s.hc);
+  const int row_elems_bytes = head_dim * elem;
+  s.row_bytes = row_elems_bytes >= 128 ? 128 : 64;
+  s.nx = row_elems_bytes / s.row_bytes;
+  const int per_subtile = 16 * s.wph * s.hc * row_elems_bytes * 2;   // K+V bytes per r step
+  const int target = elem == 1 ? 32768 : 65536;
+  s.r = target / per_subtile;
+  if (s.r < 1) s.r = 1;
+  if (s.r > 4) s.r = 4;
+  while (16 * s.wph * s.r > 256) s.r >>= 1;   // TMA box height <= 256
+  s.tile = 16 * s.wph * s.r;
+  s.box_rows = page_size > 0 && page_size < s.tile ? page_size : s.tile;
+  s.region_bytes = s.tile * s.row_bytes;
+  s.kv_bytes = s.hc * s.nx * s.region_bytes;
+  s.merge_bytes = s.wph > 1 ? kWarps * 16 * (head_dim + 2) * 4 : 0;
+  int st = (kSmemBudget - 1024 - s.merge_bytes) / (2 * s.kv_bytes);
+  if (st > kMaxStages) st = kMaxStages;
+  s.stages = st;
+  s.smem_bytes = 1024 + st * 2 * s.kv_bytes + s.merge_bytes;
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, TMA, MMA
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on a barrier phase; false on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 255u) == 0 && global_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int h, int row,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(h), "r"(row), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+        " {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+        " {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// Two e4m3 codes (low byte first) -> two f16 (or bf16) in one register, exact.
+template <bool BF16>
+__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t pair16) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair16 & 0xffffu),
+                                              __NV_E4M3);
+  if constexpr (BF16) {
+    float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+    __nv_bfloat162 b = __float22bfloat162_rn(f);
+    return *reinterpret_cast<uint32_t*>(&b);
+  } else {
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_f32x2(float lo, float hi, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&b);
+  }
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// Operand layouts (per D and element size)
+// ---------------------------------------------------------------------------
+// K operand: k-step kk of lane quad position q covers the 4 head dims
+// kdim(kk, q) .. +3 (pairs {0,1} -> b0, {2,3} -> b1; Q uses the same dims).
+template <int D, int ELEM>
+__device__ __forceinline__ int kdim(int kk, int q) {
+  if constexpr (D == 128 && ELEM == 1) return 32 * q + 4 * kk;
+  else if constexpr (D == 128 && ELEM == 2) return (kk >> 2) * 64 + 16 * q + 4 * (kk & 3);
+  else return 16 * q + 4 * kk;
+}
+
+// V operand / O accumulator: n-tile j, column n <-> head dim vdim(j, n).
+template <int D, int ELEM>
+__device__ __forceinline__ int vdim(int j, int n) {
+  if constexpr (D == 128 && ELEM == 1) return 16 * n + j;
+  else if constexpr (D == 128 && ELEM == 2) return j < 8 ? 8 * n + j : 64 + 8 * n + (j - 8);
+  else return 8 * n + j;
+}
+
+// Byte address of 16-byte chunk c of row tt in a swizzled box region.
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t region, int tt, int c, int row_bytes) {
+  const int swz = row_bytes == 128 ? (tt & 7) : ((tt >> 1) & 3);
+  return region + tt * row_bytes + ((c ^ swz) << 4);
+}
+
+// Cache row of TMA box i of the tile starting at token t0 of sequence b
+// (boxes of box_rows tokens; `valid` tokens of the tile belong to the
+// segment).  -1: the box holds no token of the segment; -2: its rows fall
+// outside the cache (recorded as a device error when `record`).
+__device__ __forceinline__ long long box_row(const Params& p, int box_rows, int b, int t0, int i,
+                                             int valid, bool record) {
+  const int t = t0 + i * box_rows;
+  if (t - t0 >= valid) return -1;
+  const int nval = min(box_rows, valid - (t - t0));
+  if (p.block_table) {
+    const int page = __ldg(p.block_table + (long long)b * p.bt_stride + (t >> p.page_shift));
+    const long long row = ((long long)page << p.page_shift) + (t & (p.page_size - 1));
+    if (page < 0 || row + nval > p.kv_rows) {
+      if (record) raise_error(p.ws, kErrBounds, page);
+      return -2;
+    }
+    return row;
+  }
+  const long long row = (long long)__ldg(p.kv_start + b) + t;
+  if (row < 0 || row + nval > p.kv_rows) {
+    if (record) raise_error(p.ws, kErrBounds, row < 0 ? row : row + nval - 1);
+    return -2;
+  }
+  return row;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+struct Shared {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  int bad[kMaxStages];
+  int abort_flag;
+  long long red[34];
+};
+
+// Walks the CTA's tiles in plan order and issues, per tile, the TMA loads of
+// its K and V rows into stage n % stages (the caller makes sure the stage is
+// free).  Used by one thread.
+template <int ELEM>
+struct Issuer {
+  SegmentIter it;
+  Segment seg;
+  bool live;
+  int t0;
+  long long n;
+
+  __device__ void init(const Params& p, const PlanResult& plan) {
+    it.init(p, plan);
+    live = it.next(p, seg);
+    t0 = live ? seg.t_begin : 0;
+    n = 0;
+  }
+
+  // Returns false when the CTA has no tile left.
+  __device__ bool issue(const Params& p, const Shape& sh, Shared& sm, uint8_t* base,
+                        const CUtensorMap* tmk, const CUtensorMap* tmv) {
+    while (live && t0 >= seg.t_end) {
+      live = it.next(p, seg);
+      if (live) t0 = seg.t_begin;
+    }
+    if (!live) return false;
+    const int stg = (int)(n % sh.stages);
+    const int b = seg.s / p.hg;
+    const int kvh0 = (seg.s - b * p.hg) * sh.hc;
+    const int valid = min(sh.tile, seg.t_end - t0);
+    const int nbox = sh.tile / sh.box_rows;
+    int bad = 0;
+    uint32_t bytes = 0;
+#pragma unroll 1
+    for (int i = 0; i < nbox; ++i) {
+      const long long row = box_row(p, sh.box_rows, b, t0, i, valid, true);
+      if (row == -2) bad = 1;
+      if (row >= 0) bytes += 2u * sh.hc * sh.nx * sh.box_rows * sh.row_bytes;
+    }
+    sm.bad[stg] = bad;
+    mbar_arrive_tx(&sm.full[stg], bytes);
+    uint8_t* kst = base + (size_t)stg * 2 * sh.kv_bytes;
+    uint8_t* vst = kst + sh.kv_bytes;
+#pragma unroll 1
+    for (int i = 0; i < nbox; ++i) {
+      const long long row = box_row(p, sh.box_rows, b, t0, i, valid, false);
+      if (row < 0) continue;
+      for (int h = 0; h < sh.hc; ++h) {
+        for (int x = 0; x < sh.nx; ++x) {
+          const size_t off = (size_t)(h * sh.nx + x) * sh.region_bytes +
+                             (size_t)i * sh.box_rows * sh.row_bytes;
+          const int xc = x * (sh.row_bytes / ELEM);
+          tma_load_3d(kst + off, tmk, xc, kvh0 + h, (int)row, &sm.full[stg]);
+          tma_load_3d(vst + off, tmv, xc, kvh0 + h, (int)row, &sm.full[stg]);
+        }
+      }
+    }
+    t0 += sh.tile;
+    ++n;
+    return true;
+  }
+};
+
+template <int KVT, typename QT, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    mma_split_kernel(const Params p, const Shape sh, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv) {
+  constexpr int ELEM = KVT == FD_E4M3 ? 1 : 2;
+  constexpr bool BF16 = std::is_same<QT, __nv_bfloat16>::value;
+  constexpr int KSTEPS = D / 16;
+  constexpr int NT = D / 8;     // n-tiles of the PV product
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ Shared sm;
+
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage0 = smem_u32(base);
+  float* merge = reinterpret_cast<float*>(base + sh.stages * 2 * sh.kv_bytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < sh.stages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kWarps);
+    }
+    sm.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const PlanResult plan = compute_plan(p, sm.red);   // contains __syncthreads
+
+  const int S = sh.stages;
+  // Thread 0 also issues the TMA copies: it fills all stages up front, then
+  // refills a stage as soon as every warp has released it.
+  const bool issuer = threadIdx.x == 0;
+  Issuer<ELEM> iss;
+  if (issuer) {
+    prefetch_map(&tmk);
+    prefetch_map(&tmv);
+    iss.init(p, plan);
+    for (int i = 0; i < S; ++i)
+      if (!iss.issue(p, sh, sm, base, &tmk, &tmv)) break;
+  }
+
+  const int ht = warp / sh.wph, ts = warp - ht * sh.wph;
+  const int kvl = ht / sh.mt, mtile = ht - kvl * sh.mt;
+  const int r = lane >> 2, q = lane & 3;
+  const int G = p.group;
+  const QT* qg = static_cast<const QT*>(p.q);
+  // local query heads (within the stream) of rows r and r + 8
+  const int h0 = mtile * 16 + r, h1 = h0 + 8;
+  const bool v0 = h0 < G, v1 = h1 < G;
+  const int li0 = kvl * G + h0, li1 = kvl * G + h1;   // slot rows
+
+  SegmentIter it;
+  it.init(p, plan);
+  Segment seg;
+  long long n = 0;
+    while (it.next(p, seg)) {
+      const int b = seg.s / p.hg;
+      const int j = seg.s - b * p.hg;
+      const long long qrow0 = (long long)b * p.num_q_heads + j * p.hq;   // first head of stream
+      // Q fragments (A operand), head dims permuted as kdim()
+      uint32_t qa[KSTEPS][4];
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        const int dd = kdim<D, ELEM>(kk, q);   // same dims as the K operand
+        uint2 x0 = make_uint2(0, 0), x1 = make_uint2(0, 0);
+        if (v0) x0 = __ldg(reinterpret_cast<const uint2*>(qg + (qrow0 + li0) * D + dd));
+        if (v1) x1 = __ldg(reinterpret_cast<const uint2*>(qg + (qrow0 + li1) * D + dd));
+        qa[kk][0] = x0.x;
+        qa[kk][1] = x1.x;
+        qa[kk][2] = x0.y;
+        qa[kk][3] = x1.y;
+      }
+      float o[NT][4];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+      for (int t0 = seg.t_begin; t0 < seg.t_end; t0 += sh.tile, ++n) {
+        const int stg = (int)(n % S);
+        const uint32_t ph = (uint32_t)((n / S) & 1);
+        bool ok = !*(volatile int*)&sm.abort_flag;
+        if (ok && !mbar_wait(&sm.full[stg], ph)) {
+          raise_error(p.ws, kErrTimeout, 2);
+          *(volatile int*)&sm.abort_flag = 1;
+          ok = false;
+        }
+        if (ok && !sm.bad[stg]) {
+          const uint32_t kreg = stage0 + stg * 2 * sh.kv_bytes + kvl * sh.nx * sh.region_bytes;
+          const uint32_t vreg = kreg + sh.kv_bytes;
+#pragma unroll 1
+          for (int rr = 0; rr < sh.r; ++rr) {
+            const int sub = ts * 16 * sh.r + 16 * rr;     // first token of the sub-tile in the tile
+            const int left = seg.t_end - (t0 + sub);      // valid tokens from the sub-tile start
+            if (left <= 0) break;
+            // ---- S = Q K^T  (2 n-tiles of 8 tokens)
+            float s[2][4];
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn) {
+              s[jn][0] = s[jn][1] = s[jn][2] = s[jn][3] = 0.f;
+              const int tt = sub + 8 * jn + r;
+              if constexpr (ELEM == 1 && D == 128) {
+                const uint4 c0 = lds128(chunk_addr(kreg, tt, 2 * q, sh.row_bytes));
+                const uint4 c1 = lds128(chunk_addr(kreg, tt, 2 * q + 1, sh.row_bytes));
+                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                  mma16816<BF16>(s[jn], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
+                                 widen_e4m3x2<BF16>(w[kk]), widen_e4m3x2<BF16>(w[kk] >> 16));
+              } else if constexpr (ELEM == 1) {   // D == 64, 64-byte rows
+                const uint4 c0 = lds128(chunk_addr(kreg, tt, q, sh.row_bytes));
+                const uint32_t w[4] = {c0.x, c0.y, c0.z, c0.w};
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma16816<BF16>(s[jn], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
+                                 widen_e4m3x2<BF16>(w[kk]), widen_e4m3x2<BF16>(w[kk] >> 16));
+              } else if constexpr (D == 128) {    // 16-bit, two 128-byte regions
+                uint4 c[4];
+                c[0] = lds128(chunk_addr(kreg, tt, 2 * q, sh.row_bytes));
+                c[1] = lds128(chunk_addr(kreg, tt, 2 * q + 1, sh.row_bytes));
+                c[2] = lds128(chunk_addr(kreg + sh.region_bytes, tt, 2 * q, sh.row_bytes));
+                c[3] = lds128(chunk_addr(kreg + sh.region_bytes, tt, 2 * q + 1, sh.row_bytes));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                  const uint4 cc = c[kk >> 1];
+                  const uint32_t b0 = (kk & 1) ? cc.z : cc.x;
+                  const uint32_t b1 = (kk & 1) ? cc.w : cc.y;
+                  mma16816<BF16>(s[jn], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                }
+              } else {                            // 16-bit, D == 64, one region
+                uint4 c[2];
+                c[0] = lds128(chunk_addr(kreg, tt, 2 * q, sh.row_bytes));
+                c[1] = lds128(chunk_addr(kreg, tt, 2 * q + 1, sh.row_bytes));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint4 cc = c[kk >> 1];
+                  const uint32_t b0 = (kk & 1) ? cc.z : cc.x;
+                  const uint32_t b1 = (kk & 1) ? cc.w : cc.y;
+                  mma16816<BF16>(s[jn], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                }
+              }
+            }
+            // ---- online softmax (rows r and r + 8; this lane holds tokens
+            //      8*jn + 2q + {0,1})
+            float x[2][4];
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int tok = 8 * jn + 2 * q + (e & 1);
+                float v = s[jn][e] * p.score_scale;
+                if (tok >= left) v = -INFINITY;
+                x[jn][e] = v;
+              }
+              mx0 = fmaxf(mx0, fmaxf(x[jn][0], x[jn][1]));
+              mx1 = fmaxf(mx1, fmaxf(x[jn][2], x[jn][3]));
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float a0 = fast_exp2(m0 - base0), a1 = fast_exp2(m1 - base1);
+            m0 = mn0;
+            m1 = mn1;
+            float pr[2][4];
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn) {
+              pr[jn][0] = fast_exp2(x[jn][0] - base0);
+              pr[jn][1] = fast_exp2(x[jn][1] - base0);
+              pr[jn][2] = fast_exp2(x[jn][2] - base1);
+              pr[jn][3] = fast_exp2(x[jn][3] - base1);
+              ps0 += pr[jn][0] + pr[jn][1];
+              ps1 += pr[jn][2] + pr[jn][3];
+            }
+            l0 = fmaf(l0, a0, ps0);
+            l1 = fmaf(l1, a1, ps1);
+            if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {
+#pragma unroll
+              for (int t = 0; t < NT; ++t) {
+                o[t][0] *= a0;
+                o[t][1] *= a0;
+                o[t][2] *= a1;
+                o[t][3] *= a1;
+              }
+            }
+            const uint32_t pa0 = pack_f32x2(pr[0][0], pr[0][1], BF16);
+            const uint32_t pa1 = pack_f32x2(pr[0][2], pr[0][3], BF16);
+            const uint32_t pa2 = pack_f32x2(pr[1][0], pr[1][1], BF16);
+            const uint32_t pa3 = pack_f32x2(pr[1][2], pr[1][3], BF16);
+            // ---- O += P V ; this lane's B fragments: tokens 2q, 2q+1 (b0)
+            //      and 2q+8, 2q+9 (b1), head dims vdim(j, r)
+            const int u0 = sub + 2 * q, u1 = u0 + 1, u2 = u0 + 8, u3 = u0 + 9;
+            if constexpr (ELEM == 1 && D == 128) {
+              const uint4 w0 = lds128(chunk_addr(vreg, u0, r, sh.row_bytes));
+              const uint4 w1 = lds128(chunk_addr(vreg, u1, r, sh.row_bytes));
+              const uint4 w2 = lds128(chunk_addr(vreg, u2, r, sh.row_bytes));
+              const uint4 w3 = lds128(chunk_addr(vreg, u3, r, sh.row_bytes));
+              const uint32_t A[4] = {w0.x, w0.y, w0.z, w0.w}, B[4] = {w1.x, w1.y, w1.z, w1.w};
+              const uint32_t C[4] = {w2.x, w2.y, w2.z, w2.w}, E[4] = {w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+              for (int wd = 0; wd < 4; ++wd) {
+                const uint32_t lo01 = __byte_perm(A[wd], B[wd], 0x5140);
+                const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
+                const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
+                const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
+                mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01),
+                               widen_e4m3x2<BF16>(lo89));
+                mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01 >> 16),
+                               widen_e4m3x2<BF16>(lo89 >> 16));
+                mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01),
+                               widen_e4m3x2<BF16>(hi89));
+                mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01 >> 16),
+                               widen_e4m3x2<BF16>(hi89 >> 16));
+              }
+            } else if constexpr (ELEM == 1) {   // D == 64: 8 bytes per token
+              const int c = r >> 1, half = (r & 1) * 8;
+              const uint2 w0 = lds64(chunk_addr(vreg, u0, c, sh.row_bytes) + half);
+              const uint2 w1 = lds64(chunk_addr(vreg, u1, c, sh.row_bytes) + half);
+              const uint2 w2 = lds64(chunk_addr(vreg, u2, c, sh.row_bytes) + half);
+              const uint2 w3 = lds64(chunk_addr(vreg, u3, c, sh.row_bytes) + half);
+              const uint32_t A[2] = {w0.x, w0.y}, B[2] = {w1.x, w1.y};
+              const uint32_t C[2] = {w2.x, w2.y}, E[2] = {w3.x, w3.y};
+#pragma unroll
+              for (int wd = 0; wd < 2; ++wd) {
+                const uint32_t lo01 = __byte_perm(A[wd], B[wd], 0x5140);
+                const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
+                const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
+                const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
+                mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01),
+                               widen_e4m3x2<BF16>(lo89));
+                mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01 >> 16),
+                               widen_e4m3x2<BF16>(lo89 >> 16));
+                mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01),
+                               widen_e4m3x2<BF16>(hi89));
+                mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01 >> 16),
+                               widen_e4m3x2<BF16>(hi89 >> 16));
+              }
+            } else {   // 16-bit: chunk r of each 128-byte region holds 8 dims
+#pragma unroll
+              for (int x2 = 0; x2 < D / 64; ++x2) {
+                const uint32_t reg = vreg + x2 * sh.region_bytes;
+                const uint4 w0 = lds128(chunk_addr(reg, u0, r, sh.row_bytes));
+                const uint4 w1 = lds128(chunk_addr(reg, u1, r, sh.row_bytes));
+                const uint4 w2 = lds128(chunk_addr(reg, u2, r, sh.row_bytes));
+                const uint4 w3 = lds128(chunk_addr(reg, u3, r, sh.row_bytes));
+                const uint32_t A[4] = {w0.x, w0.y, w0.z, w0.w}, B[4] = {w1.x, w1.y, w1.z, w1.w};
+                const uint32_t C[4] = {w2.x, w2.y, w2.z, w2.w}, E[4] = {w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+                for (int wd = 0; wd < 4; ++wd) {
+                  const int jt = x2 * 8 + 2 * wd;
+                  mma16816<BF16>(o[jt], pa0, pa1, pa2, pa3, __byte_perm(A[wd], B[wd], 0x5410),
+                                 __byte_perm(C[wd], E[wd], 0x5410));
+                  mma16816<BF16>(o[jt + 1], pa0, pa1, pa2, pa3, __byte_perm(A[wd], B[wd], 0x7632),
+                                 __byte_perm(C[wd], E[wd], 0x7632));
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[stg]);
+        if (issuer && !*(volatile int*)&sm.abort_flag) {
+          // every warp is done with this stage: refill it with tile n + S
+          if (mbar_wait(&sm.empty[stg], ph)) {
+            iss.issue(p, sh, sm, base, &tmk, &tmv);
+          } else {
+            raise_error(p.ws, kErrTimeout, 1);
+            *(volatile int*)&sm.abort_flag = 1;
+          }
+        }
+      }
+
+      // ---- end of segment: full row sums, merge the warps of a head tile
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      float* part = p.part_acc + (long long)seg.slot * p.hq * D;
+      float2* pml = p.part_ml + (long long)seg.slot * p.hq;
+      QT* outp = static_cast<QT*>(p.out) + qrow0 * D;
+      float* lsep = p.lse ? p.lse + qrow0 : nullptr;
+      if (sh.wph == 1) {
+        // this warp alone holds the head tile's state
+        const float r0 = l0 > 0.f ? p.v_scale / l0 : 0.f;
+        const float r1 = l1 > 0.f ? p.v_scale / l1 : 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int d = vdim<D, ELEM>(t, 2 * q + e);
+            if (seg.complete) {
+              if (v0) outp[(long long)li0 * D + d] = QType<QT>::from_f32(o[t][e] * r0);
+              if (v1) outp[(long long)li1 * D + d] = QType<QT>::from_f32(o[t][2 + e] * r1);
+            } else {
+              if (v0) part[(long long)li0 * D + d] = o[t][e];
+              if (v1) part[(long long)li1 * D + d] = o[t][2 + e];
+            }
+          }
+        }
+        if (q == 0) {
+          if (seg.complete) {
+            if (lsep && v0) lsep[li0] = l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY;
+            if (lsep && v1) lsep[li1] = l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY;
+          } else {
+            if (v0) pml[li0] = make_float2(m0, l0);
+            if (v1) pml[li1] = make_float2(m1, l1);
+          }
+        }
+      } else {
+        // stage every warp's state in shared memory, then the wph warps of a
+        // head tile merge its 16 x D outputs together
+        float* mine = merge + warp * 16 * (D + 2);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int d = vdim<D, ELEM>(t, 2 * q + e);
+            mine[r * D + d] = o[t][e];
+            mine[(r + 8) * D + d] = o[t][2 + e];
+          }
+        }
+        if (q == 0) {
+          mine[16 * D + r] = m0;
+          mine[16 * D + r + 8] = m1;
+          mine[16 * D + 16 + r] = l0;
+          mine[16 * D + 16 + r + 8] = l1;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
+        const float* grp = merge + (ht * sh.wph) * 16 * (D + 2);
+        for (int idx = ts * 32 + lane; idx < 16 * D; idx += sh.wph * 32) {
+          const int row = idx / D, d = idx - row * D;
+          const int lh = mtile * 16 + row;
+          if (lh >= G) continue;
+          float M = -INFINITY;
+          for (int w2 = 0; w2 < sh.wph; ++w2) M = fmaxf(M, grp[w2 * 16 * (D + 2) + 16 * D + row]);
+          float L = 0.f, A = 0.f;
+          for (int w2 = 0; w2 < sh.wph; ++w2) {
+            const float* g2 = grp + w2 * 16 * (D + 2);
+            const float mw = g2[16 * D + row];
+            const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+            L = fmaf(g2[16 * D + 16 + row], f, L);
+            A = fmaf(g2[row * D + d], f, A);
+          }
+          const int li = kvl * G + lh;
+          if (seg.complete) {
+            outp[(long long)li * D + d] = QType<QT>::from_f32(L > 0.f ? A * (p.v_scale / L) : 0.f);
+            if (d == 0 && lsep) lsep[li] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+          } else {
+            part[(long long)li * D + d] = A;
+            if (d == 0) pml[li] = make_float2(M, L);
+          }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
+      }
+  }
+  if (issuer && *(volatile int*)&sm.abort_flag) {
+    // drain: copies of the last S issued tiles must land before the CTA exits
+    for (long long i = iss.n - S < 0 ? 0 : iss.n - S; i < iss.n; ++i)
+      mbar_wait(&sm.full[i % S], (uint32_t)((i / S) & 1));
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps (cached), launch
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  long long rows;
+  int kvh, d, dtype, box_rows, row_bytes;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && kvh == o.kvh && d == o.d && dtype == o.dtype &&
+           box_rows == o.box_rows && row_bytes == o.row_bytes;
+  }
+};
+
+constexpr int kMapCache = 32;
+std::mutex g_map_mu;
+MapKey g_keys[kMapCache];
+CUtensorMap g_maps[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+
+// 3-D view of a cache: {head_dim, kv_heads, rows}; box {row_bytes/elem, 1, box_rows}.
+bool get_map(const void* ptr, long long rows, int kvh, int d, int dtype, int box_rows,
+             int row_bytes, CUtensorMap* out) {
+  MapKey key{ptr, rows, kvh, d, dtype, box_rows, row_bytes};
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  for (int i = 0; i < g_map_used; ++i)
+    if (g_keys[i] == key) {
+      *out = g_maps[i];
+      return true;
+    }
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int elem = dtype == FD_E4M3 ? 1 : 2;
+  CUtensorMapDataType dt = dtype == FD_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                            : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)kvh, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * elem, (cuuint64_t)d * elem * kvh};
+  cuuint32_t box[3] = {(cuuint32_t)(row_bytes / elem), 1u, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUtensorMap m;
+  CUresult res = fn(&m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) return false;
+  int slot = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
+  g_keys[slot] = key;
+  g_maps[slot] = m;
+  *out = m;
+  return true;
+}
+
+template <int KVT, typename QT, int D>
+cudaError_t launch_t(const Params& p, const Shape& sh, const CUtensorMap& mk, const CUtensorMap& mv,
+                     cudaStream_t stream) {
+  auto kern = mma_split_kernel<KVT, QT, D>;
+  static int configured = 0;
+  if (configured < sh.smem_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBudget);
+    if (e != cudaSuccess) return e;
+    configured = kSmemBudget;
+  }
+  kern<<<p.grid, kThreads, sh.smem_bytes, stream>>>(p, sh, mk, mv);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const Params& p, const Shape& sh, const CUtensorMap& mk,
+                     const CUtensorMap& mv, cudaStream_t st) {
+  if (p.kv_dtype == FD_F16) return launch_t<FD_F16, __half, D>(p, sh, mk, mv, st);
+  if (p.kv_dtype == FD_BF16) return launch_t<FD_BF16, __nv_bfloat16, D>(p, sh, mk, mv, st);
+  if (p.q_dtype == FD_F16) return launch_t<FD_E4M3, __half, D>(p, sh, mk, mv, st);
+  return launch_t<FD_E4M3, __nv_bfloat16, D>(p, sh, mk, mv, st);
+}
+
+}  // namespace
+
+bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv_dtype, int paged,
+                  int page_size) {
+  (void)q_dtype;
+  (void)kv_dtype;
+  if (head_dim != 64 && head_dim != 128) return false;
+  if (group < 1 || group > 128 || num_kv_heads < 1) return false;
+  if (paged && (page_size < 1 || page_size > 256)) return false;
+  if (paged) {
+    // every TMA box must start on a 1024-byte swizzle atom of shared memory
+    const Shape s = make_shape(group, num_kv_heads, head_dim, kv_dtype, page_size);
+    if ((s.box_rows * s.row_bytes) % 1024 != 0) return false;
+  }
+  if (!encode_fn()) return false;
+  return true;
+}
+
+void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms, int* hc,
+                int* tile, int* grid) {
+  const Shape s = make_shape(group, num_kv_heads, head_dim, kv_dtype, 0);
+  *hc = s.hc;
+  *tile = s.tile;
   *grid = sms;
 }
 
-cudaError_t launch_split_mma(const Params&, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {
+  if (p.kv_rows >= (1ll << 31)) return cudaErrorInvalidValue;
+  const Shape sh = make_shape(p.group, p.num_kv_heads, p.head_dim, p.kv_dtype,
+                              p.block_table ? p.page_size : 0);
+  if (sh.stages < 2 || sh.tile != p.tile || sh.hc != p.hc) return cudaErrorInvalidValue;
+  CUtensorMap mk, mv;
+  if (!get_map(p.k, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
+               &mk) ||
+      !get_map(p.v, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
+               &mv))
+    return cudaErrorInvalidValue;
+  if (p.head_dim == 128) return launch_d<128>(p, sh, mk, mv, stream);
+  return launch_d<64>(p, sh, mk, mv, stream);
+}
 
 }  // namespace fd
