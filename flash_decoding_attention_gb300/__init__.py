@@ -43,7 +43,7 @@ FD_KERNEL_MMA = 2
 EXPORTED = [
     "fd_workspace_bytes", "fd_decode_attention", "fd_check_device_error", "fd_status_string",
     "fd_set_kernel", "fd_selected_kernel", "fd_set_split_events", "fd_debug_read_plan",
-    "fd_debug_gather_kv",
+    "fd_debug_gather_kv", "fd_decode_attention_noalloc",
 ]
 
 
@@ -75,6 +75,10 @@ def load_library(path: Optional[str] = None):
         lib.fd_decode_attention.restype = i32
         lib.fd_decode_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, i32,
                                             i32, f32, f32, f32, i32, i32, vp, vp, vp, sz, vp]
+        lib.fd_decode_attention_noalloc.restype = i32
+        lib.fd_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32,
+                                                    i32, i32, i32, f32, f32, f32, i32, i32, vp,
+                                                    vp, vp]
         lib.fd_check_device_error.restype = i32
         lib.fd_check_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int64)]
         lib.fd_status_string.restype = ctypes.c_char_p
@@ -159,6 +163,30 @@ def fd_decode_attention(q, k_cache, v_cache, kv_start_idx, block_table, seq_len,
         _stream_handle(stream))
     if check and st != FD_OK:
         raise FdError(st, "fd_decode_attention")
+    return st
+
+
+def fd_decode_attention_noalloc(q, k_cache, v_cache, kv_start_idx, block_table, seq_len,
+                                kv_rows: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                page_size: int, softmax_scale: float, k_scale: float,
+                                v_scale: float, out, lse, stream=None,
+                                q_dtype: Optional[int] = None, kv_dtype: Optional[int] = None,
+                                check: bool = True) -> int:
+    """Like fd_decode_attention, but the library supplies the scratch memory
+    from a fixed array of its own, for callers that cannot allocate device
+    memory.  Calls that may overlap on the GPU must be serialised."""
+    lib = load_library()
+    batch = int(seq_len.shape[0])
+    stride = int(block_table.shape[1]) if block_table is not None else 0
+    st = lib.fd_decode_attention_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_start_idx), _ptr(block_table), stride,
+        _ptr(seq_len), int(kv_rows), batch, int(num_q_heads), int(num_kv_heads), int(head_dim),
+        int(page_size), float(softmax_scale), float(k_scale), float(v_scale),
+        _q_dtype(q) if q_dtype is None else int(q_dtype),
+        _kv_dtype(k_cache) if kv_dtype is None else int(kv_dtype),
+        _ptr(out), _ptr(lse), _stream_handle(stream))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_decode_attention_noalloc")
     return st
 
 

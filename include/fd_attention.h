@@ -136,6 +136,34 @@ fd_status fd_decode_attention(const void *q, const void *k_cache, const void *v_
                               void *workspace, size_t workspace_bytes, fd_stream_t stream);
 
 /*
+ * Same computation as fd_decode_attention, for callers that cannot allocate
+ * device memory (for example code running inside a framework that does not
+ * expose its allocator, or under a fixed memory budget).  The pages have no
+ * counterpart of this function; it exists only for those callers.
+ *
+ * Arguments are those of fd_decode_attention without the workspace: the
+ * scratch memory is a 16 MiB array compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  Sizes whose
+ * fd_workspace_bytes(...) exceeds 16 MiB return FD_ERR_WORKSPACE_TOO_SMALL
+ * before any launch.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Each call first clears the array's
+ * device-error word, so device-side bounds errors of this entry point are not
+ * reported; use fd_decode_attention when they must be.  All calls share the
+ * one array: calls that can overlap on the GPU (different streams, or
+ * different host threads) race on it and must be serialised by the caller.
+ * Nothing is allocated or freed.
+ */
+fd_status fd_decode_attention_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                      const int32_t *kv_start_idx, const int32_t *block_table,
+                                      int block_table_stride, const int32_t *seq_len,
+                                      int64_t kv_rows, int batch, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int page_size,
+                                      float softmax_scale, float k_scale, float v_scale,
+                                      fd_dtype q_dtype, fd_dtype kv_dtype, void *out, float *lse,
+                                      fd_stream_t stream);
+
+/*
  * Synchronises `stream`, reads and clears the workspace's sticky device-error
  * word.  Returns FD_OK, FD_ERR_DEVICE_BOUNDS, FD_ERR_DEVICE_TIMEOUT or
  * FD_ERR_CUDA.  If info is not NULL it receives the first offending value
