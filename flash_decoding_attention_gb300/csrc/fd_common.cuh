@@ -252,6 +252,12 @@ __device__ __forceinline__ long long cache_row(const Params& p, int b, int t) {
   return row;
 }
 
+// Lets the dependent (combine) grid be scheduled while this grid still runs;
+// the dependent grid waits for this grid's completion before it reads.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Small math helpers
 // ---------------------------------------------------------------------------

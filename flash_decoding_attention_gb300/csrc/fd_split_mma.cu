@@ -11,14 +11,18 @@
 // path ("From SGLang kernel source to GPU trace: DeepSeek V4.1
 // Flash-Decode", section 2.2).
 //
-// Work split inside a CTA (one persistent CTA per SM, 8 warps):
-//  - thread 0 also walks the CTA's tiles ahead of the others and, per stage,
-//    issues TMA tensor loads of the K and V rows of `tile` tokens for the
-//    stream's hc KV heads into shared memory (128-byte swizzle, or 64-byte
-//    for 64-byte rows), completing on the stage's "full" mbarrier; it refills
-//    a stage once all 8 warps have released it on its "empty" mbarrier;
-//  - warp w owns head tile w / wph (16 query heads of one KV head) and the
-//    w % wph-th run of 16 * r tokens of every stage.
+// Work split inside a CTA (one persistent CTA per SM, 9 warps):
+//  - warp 8 is the producer: it walks the CTA's tiles, stages the current
+//    sequence's block-table entries in shared memory (one parallel load per
+//    window of 256 pages), and its lane 0 issues, per stage, TMA tensor loads
+//    of the K and V rows of `tile` tokens for the stream's hc KV heads into
+//    shared memory (128-byte swizzle, or 64-byte for 64-byte rows),
+//    completing on the stage's "full" mbarrier, as soon as all consumer warps
+//    have released the stage on its "empty" mbarrier;
+//  - consumer warp w (0..7) owns head tile w / wph (16 query heads of one KV
+//    head) and the w % wph-th run of 16 * r tokens of every stage.  The head
+//    tile's Q fragments sit in shared memory for the whole segment (nine
+//    warps leave at most 168 registers per thread).
 //    Per 16-token sub-tile it computes S = Q K^T with m16n8k16 MMAs (query
 //    heads are the M rows, tokens the N columns, head dims the K depth),
 //    the online softmax update in registers, and O += P V with P taken
@@ -44,8 +48,9 @@
 namespace fd {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
+constexpr int kPageWindow = 256;   // block-table entries staged per window
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 225 * 1024;
 constexpr unsigned long long kWaitNs = 1000000000ull;
@@ -59,10 +64,13 @@ struct Shape {
   int box_rows;      // rows per TMA box
   int row_bytes;     // bytes of one swizzled row of a box (128 or 64)
   int nx;            // boxes across head_dim (head_dim * elem / row_bytes)
-  int region_bytes;  // tile * row_bytes
+  int region_bytes;  // tile * row_bytes; a stage holds K then V, each as
+                     // [nx][hc][tile][row_bytes] regions
   int kv_bytes;      // K (or V) bytes of one stage = hc * nx * region_bytes
+  int heads_box;     // 1: one TMA box covers all hc heads of a tile
   int stages;
   int merge_bytes;
+  int qfrag_bytes;
   int smem_bytes;
 };
 
@@ -76,10 +84,10 @@ Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int pa
   Shape s;
   const int elem = kv_dtype == FD_E4M3 ? 1 : 2;
   s.mt = next_pow2((group + 15) / 16);
-  int hc = kWarps / s.mt;
+  int hc = kConsumerWarps / s.mt;
   while (hc > 1 && num_kv_heads % hc != 0) hc >>= 1;
   s.hc = hc;
-  s.wph = kWarps / (s.mt * s.hc);
+  s.wph = kConsumerWarps / (s.mt * s.hc);
   const int row_elems_bytes = head_dim * elem;
   s.row_bytes = row_elems_bytes >= 128 ? 128 : 64;
   s.nx = row_elems_bytes / s.row_bytes;
@@ -92,12 +100,14 @@ Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int pa
   s.tile = 16 * s.wph * s.r;
   s.box_rows = page_size > 0 && page_size < s.tile ? page_size : s.tile;
   s.region_bytes = s.tile * s.row_bytes;
+  s.heads_box = 0;   // decided at launch (needs a tensor map over {dims, rows, heads})
   s.kv_bytes = s.hc * s.nx * s.region_bytes;
-  s.merge_bytes = s.wph > 1 ? kWarps * 16 * (head_dim + 2) * 4 : 0;
-  int st = (kSmemBudget - 1024 - s.merge_bytes) / (2 * s.kv_bytes);
+  s.merge_bytes = s.wph > 1 ? kConsumerWarps * (16 * (head_dim + head_dim / 8) + 32) * 4 : 0;
+  s.qfrag_bytes = s.mt * s.hc * (head_dim / 16) * 512;   // one Q fragment set per head tile
+  int st = (kSmemBudget - 1024 - s.merge_bytes - s.qfrag_bytes) / (2 * s.kv_bytes);
   if (st > kMaxStages) st = kMaxStages;
   s.stages = st;
-  s.smem_bytes = 1024 + st * 2 * s.kv_bytes + s.merge_bytes;
+  s.smem_bytes = 1024 + st * 2 * s.kv_bytes + s.merge_bytes + s.qfrag_bytes;
   return s;
 }
 
@@ -150,12 +160,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int h, int row,
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(h), "r"(row), "r"(smem_u32(bar))
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -244,32 +254,6 @@ __device__ __forceinline__ uint32_t chunk_addr(uint32_t region, int tt, int c, i
   return region + tt * row_bytes + ((c ^ swz) << 4);
 }
 
-// Cache row of TMA box i of the tile starting at token t0 of sequence b
-// (boxes of box_rows tokens; `valid` tokens of the tile belong to the
-// segment).  -1: the box holds no token of the segment; -2: its rows fall
-// outside the cache (recorded as a device error when `record`).
-__device__ __forceinline__ long long box_row(const Params& p, int box_rows, int b, int t0, int i,
-                                             int valid, bool record) {
-  const int t = t0 + i * box_rows;
-  if (t - t0 >= valid) return -1;
-  const int nval = min(box_rows, valid - (t - t0));
-  if (p.block_table) {
-    const int page = __ldg(p.block_table + (long long)b * p.bt_stride + (t >> p.page_shift));
-    const long long row = ((long long)page << p.page_shift) + (t & (p.page_size - 1));
-    if (page < 0 || row + nval > p.kv_rows) {
-      if (record) raise_error(p.ws, kErrBounds, page);
-      return -2;
-    }
-    return row;
-  }
-  const long long row = (long long)__ldg(p.kv_start + b) + t;
-  if (row < 0 || row + nval > p.kv_rows) {
-    if (record) raise_error(p.ws, kErrBounds, row < 0 ? row : row + nval - 1);
-    return -2;
-  }
-  return row;
-}
-
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -279,69 +263,7 @@ struct Shared {
   int bad[kMaxStages];
   int abort_flag;
   long long red[34];
-};
-
-// Walks the CTA's tiles in plan order and issues, per tile, the TMA loads of
-// its K and V rows into stage n % stages (the caller makes sure the stage is
-// free).  Used by one thread.
-template <int ELEM>
-struct Issuer {
-  SegmentIter it;
-  Segment seg;
-  bool live;
-  int t0;
-  long long n;
-
-  __device__ void init(const Params& p, const PlanResult& plan) {
-    it.init(p, plan);
-    live = it.next(p, seg);
-    t0 = live ? seg.t_begin : 0;
-    n = 0;
-  }
-
-  // Returns false when the CTA has no tile left.
-  __device__ bool issue(const Params& p, const Shape& sh, Shared& sm, uint8_t* base,
-                        const CUtensorMap* tmk, const CUtensorMap* tmv) {
-    while (live && t0 >= seg.t_end) {
-      live = it.next(p, seg);
-      if (live) t0 = seg.t_begin;
-    }
-    if (!live) return false;
-    const int stg = (int)(n % sh.stages);
-    const int b = seg.s / p.hg;
-    const int kvh0 = (seg.s - b * p.hg) * sh.hc;
-    const int valid = min(sh.tile, seg.t_end - t0);
-    const int nbox = sh.tile / sh.box_rows;
-    int bad = 0;
-    uint32_t bytes = 0;
-#pragma unroll 1
-    for (int i = 0; i < nbox; ++i) {
-      const long long row = box_row(p, sh.box_rows, b, t0, i, valid, true);
-      if (row == -2) bad = 1;
-      if (row >= 0) bytes += 2u * sh.hc * sh.nx * sh.box_rows * sh.row_bytes;
-    }
-    sm.bad[stg] = bad;
-    mbar_arrive_tx(&sm.full[stg], bytes);
-    uint8_t* kst = base + (size_t)stg * 2 * sh.kv_bytes;
-    uint8_t* vst = kst + sh.kv_bytes;
-#pragma unroll 1
-    for (int i = 0; i < nbox; ++i) {
-      const long long row = box_row(p, sh.box_rows, b, t0, i, valid, false);
-      if (row < 0) continue;
-      for (int h = 0; h < sh.hc; ++h) {
-        for (int x = 0; x < sh.nx; ++x) {
-          const size_t off = (size_t)(h * sh.nx + x) * sh.region_bytes +
-                             (size_t)i * sh.box_rows * sh.row_bytes;
-          const int xc = x * (sh.row_bytes / ELEM);
-          tma_load_3d(kst + off, tmk, xc, kvh0 + h, (int)row, &sm.full[stg]);
-          tma_load_3d(vst + off, tmv, xc, kvh0 + h, (int)row, &sm.full[stg]);
-        }
-      }
-    }
-    t0 += sh.tile;
-    ++n;
-    return true;
-  }
+  int pages[kPageWindow];   // producer's window of the current sequence's block table
 };
 
 template <int KVT, typename QT, int D>
@@ -359,62 +281,166 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const uint32_t stage0 = smem_u32(base);
   float* merge = reinterpret_cast<float*>(base + sh.stages * 2 * sh.kv_bytes);
+  const uint32_t qfrag0 = stage0 + sh.stages * 2 * sh.kv_bytes + sh.merge_bytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < sh.stages; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], kWarps);
+      mbar_init(&sm.empty[i], kConsumerWarps);
     }
     sm.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   const PlanResult plan = compute_plan(p, sm.red);   // contains __syncthreads
+  allow_dependent_launch();
 
   const int S = sh.stages;
-  // Thread 0 also issues the TMA copies: it fills all stages up front, then
-  // refills a stage as soon as every warp has released it.
-  const bool issuer = threadIdx.x == 0;
-  Issuer<ELEM> iss;
-  if (issuer) {
-    prefetch_map(&tmk);
-    prefetch_map(&tmv);
-    iss.init(p, plan);
-    for (int i = 0; i < S; ++i)
-      if (!iss.issue(p, sh, sm, base, &tmk, &tmv)) break;
-  }
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    // The whole warp walks the CTA's tiles; it stages block-table entries in
+    // shared memory with one parallel load per window, and lane 0 issues the
+    // TMA copies of each tile as soon as its stage is free.
+    if (lane == 0) {
+      prefetch_map(&tmk);
+      prefetch_map(&tmv);
+    }
+    SegmentIter it;
+    it.init(p, plan);
+    Segment seg;
+    long long n = 0;
+    bool stop = false;
+    while (!stop && it.next(p, seg)) {
+      const int b = seg.s / p.hg;
+      const int kvh0 = (seg.s - b * p.hg) * sh.hc;
+      const long long start = p.block_table ? 0 : (long long)__ldg(p.kv_start + b);
+      int win_lo = 0, win_hi = 0;   // logical pages [win_lo, win_hi) held in sm.pages
+      for (int t0 = seg.t_begin; t0 < seg.t_end; t0 += sh.tile, ++n) {
+        const int valid = min(sh.tile, seg.t_end - t0);
+        if (p.block_table) {
+          const int pg_lo = t0 >> p.page_shift;
+          const int pg_hi = ((t0 + valid - 1) >> p.page_shift) + 1;
+          if (pg_lo < win_lo || pg_hi > win_hi) {
+            const int last = ((seg.t_end - 1) >> p.page_shift) + 1;
+            win_lo = pg_lo;
+            win_hi = min(pg_lo + kPageWindow, last);
+            __syncwarp();
+            for (int k = lane; k < win_hi - win_lo; k += 32)
+              sm.pages[k] = __ldg(p.block_table + (long long)b * p.bt_stride + win_lo + k);
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          const int stg = (int)(n % S);
+          const uint32_t ph = (uint32_t)((n / S) & 1);
+          if (*(volatile int*)&sm.abort_flag || !mbar_wait(&sm.empty[stg], ph ^ 1u)) {
+            if (!*(volatile int*)&sm.abort_flag) {
+              raise_error(p.ws, kErrTimeout, 1);
+              *(volatile int*)&sm.abort_flag = 1;
+            }
+            stop = true;
+          } else {
+            const int nbox = sh.tile / sh.box_rows;
+            uint8_t* kst = base + (size_t)stg * 2 * sh.kv_bytes;
+            uint8_t* vst = kst + sh.kv_bytes;
+            int bad = 0;
+            uint32_t bytes = 0;
+            // pass 1: validate rows, count bytes; pass 2: issue
+            for (int pass = 0; pass < 2; ++pass) {
+              if (pass == 1) {
+                sm.bad[stg] = bad;
+                mbar_arrive_tx(&sm.full[stg], bytes);
+              }
+#pragma unroll 1
+              for (int i = 0; i < nbox; ++i) {
+                const int t = t0 + i * sh.box_rows;
+                if (t - t0 >= valid) break;
+                const int nval = min(sh.box_rows, valid - (t - t0));
+                long long row;
+                bool ok;
+                if (p.block_table) {
+                  const int page = sm.pages[(t >> p.page_shift) - win_lo];
+                  row = ((long long)page << p.page_shift) + (t & (p.page_size - 1));
+                  ok = page >= 0 && row + nval <= p.kv_rows;
+                  if (!ok && pass == 0) raise_error(p.ws, kErrBounds, page);
+                } else {
+                  row = start + t;
+                  ok = row >= 0 && row + nval <= p.kv_rows;
+                  if (!ok && pass == 0) raise_error(p.ws, kErrBounds, row < 0 ? row : row + nval - 1);
+                }
+                if (pass == 0) {
+                  if (ok) bytes += 2u * sh.hc * sh.nx * sh.box_rows * sh.row_bytes;
+                  else bad = 1;
+                  continue;
+                }
+                if (!ok) continue;
+                if (sh.heads_box) {
+                  // one box per head-dim slice: all hc heads of the tile's rows
+                  for (int x = 0; x < sh.nx; ++x) {
+                    const size_t off = (size_t)x * sh.hc * sh.region_bytes;
+                    const int xc = x * (sh.row_bytes / ELEM);
+                    tma_load_3d(kst + off, &tmk, xc, (int)row, kvh0, &sm.full[stg]);
+                    tma_load_3d(vst + off, &tmv, xc, (int)row, kvh0, &sm.full[stg]);
+                  }
+                  continue;
+                }
+                for (int h = 0; h < sh.hc; ++h) {
+                  for (int x = 0; x < sh.nx; ++x) {
+                    const size_t off = (size_t)(x * sh.hc + h) * sh.region_bytes +
+                                       (size_t)i * sh.box_rows * sh.row_bytes;
+                    const int xc = x * (sh.row_bytes / ELEM);
+                    tma_load_3d(kst + off, &tmk, xc, kvh0 + h, (int)row, &sm.full[stg]);
+                    tma_load_3d(vst + off, &tmv, xc, kvh0 + h, (int)row, &sm.full[stg]);
+                  }
+                }
+              }
+            }
+          }
+        }
+        stop = __shfl_sync(0xffffffffu, stop, 0);
+        if (stop) break;
+      }
+    }
+    if (lane == 0 && stop) {
+      // drain: copies of the last S issued tiles must land before the CTA exits
+      for (long long i = n - S < 0 ? 0 : n - S; i < n; ++i)
+        mbar_wait(&sm.full[i % S], (uint32_t)((i / S) & 1));
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int ht = warp / sh.wph, ts = warp - ht * sh.wph;
+    const int kvl = ht / sh.mt, mtile = ht - kvl * sh.mt;
+    const int r = lane >> 2, q = lane & 3;
+    const int G = p.group;
+    const QT* qg = static_cast<const QT*>(p.q);
+    // local query heads (within the stream) of rows r and r + 8
+    const int h0 = mtile * 16 + r, h1 = h0 + 8;
+    const bool v0 = h0 < G, v1 = h1 < G;
+    const int li0 = kvl * G + h0, li1 = kvl * G + h1;   // slot rows
+    // this head tile's Q fragments in shared memory: [kk][lane] x 16 bytes
+    const uint32_t qf = qfrag0 + (uint32_t)ht * KSTEPS * 512 + lane * 16;
 
-  const int ht = warp / sh.wph, ts = warp - ht * sh.wph;
-  const int kvl = ht / sh.mt, mtile = ht - kvl * sh.mt;
-  const int r = lane >> 2, q = lane & 3;
-  const int G = p.group;
-  const QT* qg = static_cast<const QT*>(p.q);
-  // local query heads (within the stream) of rows r and r + 8
-  const int h0 = mtile * 16 + r, h1 = h0 + 8;
-  const bool v0 = h0 < G, v1 = h1 < G;
-  const int li0 = kvl * G + h0, li1 = kvl * G + h1;   // slot rows
-
-  SegmentIter it;
-  it.init(p, plan);
-  Segment seg;
-  long long n = 0;
+    SegmentIter it;
+    it.init(p, plan);
+    Segment seg;
+    long long n = 0;
     while (it.next(p, seg)) {
       const int b = seg.s / p.hg;
       const int j = seg.s - b * p.hg;
       const long long qrow0 = (long long)b * p.num_q_heads + j * p.hq;   // first head of stream
-      // Q fragments (A operand), head dims permuted as kdim()
-      uint32_t qa[KSTEPS][4];
+      // Q fragments (A operand), head dims permuted as kdim(); every warp of
+      // the head tile writes the same values
 #pragma unroll
       for (int kk = 0; kk < KSTEPS; ++kk) {
         const int dd = kdim<D, ELEM>(kk, q);   // same dims as the K operand
         uint2 x0 = make_uint2(0, 0), x1 = make_uint2(0, 0);
         if (v0) x0 = __ldg(reinterpret_cast<const uint2*>(qg + (qrow0 + li0) * D + dd));
         if (v1) x1 = __ldg(reinterpret_cast<const uint2*>(qg + (qrow0 + li1) * D + dd));
-        qa[kk][0] = x0.x;
-        qa[kk][1] = x1.x;
-        qa[kk][2] = x0.y;
-        qa[kk][3] = x1.y;
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qf + kk * 512), "r"(x0.x),
+                     "r"(x1.x), "r"(x0.y), "r"(x1.y)
+                     : "memory");
       }
+      __syncwarp();
       float o[NT][4];
 #pragma unroll
       for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
@@ -430,57 +456,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         }
         if (ok && !sm.bad[stg]) {
-          const uint32_t kreg = stage0 + stg * 2 * sh.kv_bytes + kvl * sh.nx * sh.region_bytes;
+          const uint32_t kreg = stage0 + stg * 2 * sh.kv_bytes + kvl * sh.region_bytes;
+          const uint32_t xstride = sh.hc * sh.region_bytes;   // next head-dim slice
           const uint32_t vreg = kreg + sh.kv_bytes;
 #pragma unroll 1
           for (int rr = 0; rr < sh.r; ++rr) {
             const int sub = ts * 16 * sh.r + 16 * rr;     // first token of the sub-tile in the tile
             const int left = seg.t_end - (t0 + sub);      // valid tokens from the sub-tile start
             if (left <= 0) break;
-            // ---- S = Q K^T  (2 n-tiles of 8 tokens)
+            // ---- S = Q K^T  (2 n-tiles of 8 tokens).  Each Q fragment is read
+            //      from shared memory once and used for both n-tiles.
             float s[2][4];
 #pragma unroll
-            for (int jn = 0; jn < 2; ++jn) {
-              s[jn][0] = s[jn][1] = s[jn][2] = s[jn][3] = 0.f;
-              const int tt = sub + 8 * jn + r;
-              if constexpr (ELEM == 1 && D == 128) {
-                const uint4 c0 = lds128(chunk_addr(kreg, tt, 2 * q, sh.row_bytes));
-                const uint4 c1 = lds128(chunk_addr(kreg, tt, 2 * q + 1, sh.row_bytes));
-                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            for (int jn = 0; jn < 2; ++jn) s[jn][0] = s[jn][1] = s[jn][2] = s[jn][3] = 0.f;
+            const int tk0 = sub + r, tk1 = sub + 8 + r;   // this lane's K rows
+            if constexpr (ELEM == 1 && D == 128) {
+              const uint4 a0 = lds128(chunk_addr(kreg, tk0, 2 * q, sh.row_bytes));
+              const uint4 a1 = lds128(chunk_addr(kreg, tk0, 2 * q + 1, sh.row_bytes));
+              const uint4 b0 = lds128(chunk_addr(kreg, tk1, 2 * q, sh.row_bytes));
+              const uint4 b1 = lds128(chunk_addr(kreg, tk1, 2 * q + 1, sh.row_bytes));
+              const uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+              const uint32_t w1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                  mma16816<BF16>(s[jn], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
-                                 widen_e4m3x2<BF16>(w[kk]), widen_e4m3x2<BF16>(w[kk] >> 16));
-              } else if constexpr (ELEM == 1) {   // D == 64, 64-byte rows
-                const uint4 c0 = lds128(chunk_addr(kreg, tt, q, sh.row_bytes));
-                const uint32_t w[4] = {c0.x, c0.y, c0.z, c0.w};
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint4 a = lds128(qf + kk * 512);
+                mma16816<BF16>(s[0], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w0[kk]),
+                               widen_e4m3x2<BF16>(w0[kk] >> 16));
+                mma16816<BF16>(s[1], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w1[kk]),
+                               widen_e4m3x2<BF16>(w1[kk] >> 16));
+              }
+            } else if constexpr (ELEM == 1) {   // D == 64, 64-byte rows
+              const uint4 a0 = lds128(chunk_addr(kreg, tk0, q, sh.row_bytes));
+              const uint4 b0 = lds128(chunk_addr(kreg, tk1, q, sh.row_bytes));
+              const uint32_t w0[4] = {a0.x, a0.y, a0.z, a0.w};
+              const uint32_t w1[4] = {b0.x, b0.y, b0.z, b0.w};
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  mma16816<BF16>(s[jn], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
-                                 widen_e4m3x2<BF16>(w[kk]), widen_e4m3x2<BF16>(w[kk] >> 16));
-              } else if constexpr (D == 128) {    // 16-bit, two 128-byte regions
-                uint4 c[4];
-                c[0] = lds128(chunk_addr(kreg, tt, 2 * q, sh.row_bytes));
-                c[1] = lds128(chunk_addr(kreg, tt, 2 * q + 1, sh.row_bytes));
-                c[2] = lds128(chunk_addr(kreg + sh.region_bytes, tt, 2 * q, sh.row_bytes));
-                c[3] = lds128(chunk_addr(kreg + sh.region_bytes, tt, 2 * q + 1, sh.row_bytes));
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint4 a = lds128(qf + kk * 512);
+                mma16816<BF16>(s[0], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w0[kk]),
+                               widen_e4m3x2<BF16>(w0[kk] >> 16));
+                mma16816<BF16>(s[1], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w1[kk]),
+                               widen_e4m3x2<BF16>(w1[kk] >> 16));
+              }
+            } else {   // 16-bit: chunk pairs (2q, 2q+1) of each 128-byte region
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                  const uint4 cc = c[kk >> 1];
-                  const uint32_t b0 = (kk & 1) ? cc.z : cc.x;
-                  const uint32_t b1 = (kk & 1) ? cc.w : cc.y;
-                  mma16816<BF16>(s[jn], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                }
-              } else {                            // 16-bit, D == 64, one region
-                uint4 c[2];
-                c[0] = lds128(chunk_addr(kreg, tt, 2 * q, sh.row_bytes));
-                c[1] = lds128(chunk_addr(kreg, tt, 2 * q + 1, sh.row_bytes));
+              for (int x2 = 0; x2 < D / 64; ++x2) {
+                const uint32_t reg = kreg + x2 * xstride;
+                uint4 c0[2], c1[2];
+                c0[0] = lds128(chunk_addr(reg, tk0, 2 * q, sh.row_bytes));
+                c0[1] = lds128(chunk_addr(reg, tk0, 2 * q + 1, sh.row_bytes));
+                c1[0] = lds128(chunk_addr(reg, tk1, 2 * q, sh.row_bytes));
+                c1[1] = lds128(chunk_addr(reg, tk1, 2 * q + 1, sh.row_bytes));
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint4 cc = c[kk >> 1];
-                  const uint32_t b0 = (kk & 1) ? cc.z : cc.x;
-                  const uint32_t b1 = (kk & 1) ? cc.w : cc.y;
-                  mma16816<BF16>(s[jn], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                for (int k4 = 0; k4 < 4; ++k4) {
+                  const int kk = x2 * 4 + k4;
+                  const uint4 a = lds128(qf + kk * 512);
+                  const uint4 p0 = c0[k4 >> 1], p1 = c1[k4 >> 1];
+                  mma16816<BF16>(s[0], a.x, a.y, a.z, a.w, (k4 & 1) ? p0.z : p0.x,
+                                 (k4 & 1) ? p0.w : p0.y);
+                  mma16816<BF16>(s[1], a.x, a.y, a.z, a.w, (k4 & 1) ? p1.z : p1.x,
+                                 (k4 & 1) ? p1.w : p1.y);
                 }
               }
             }
@@ -587,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {   // 16-bit: chunk r of each 128-byte region holds 8 dims
 #pragma unroll
               for (int x2 = 0; x2 < D / 64; ++x2) {
-                const uint32_t reg = vreg + x2 * sh.region_bytes;
+                const uint32_t reg = vreg + x2 * xstride;
                 const uint4 w0 = lds128(chunk_addr(reg, u0, r, sh.row_bytes));
                 const uint4 w1 = lds128(chunk_addr(reg, u1, r, sh.row_bytes));
                 const uint4 w2 = lds128(chunk_addr(reg, u2, r, sh.row_bytes));
@@ -608,15 +643,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stg]);
-        if (issuer && !*(volatile int*)&sm.abort_flag) {
-          // every warp is done with this stage: refill it with tile n + S
-          if (mbar_wait(&sm.empty[stg], ph)) {
-            iss.issue(p, sh, sm, base, &tmk, &tmv);
-          } else {
-            raise_error(p.ws, kErrTimeout, 1);
-            *(volatile int*)&sm.abort_flag = 1;
-          }
-        }
       }
 
       // ---- end of segment: full row sums, merge the warps of a head tile
@@ -629,20 +655,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       QT* outp = static_cast<QT*>(p.out) + qrow0 * D;
       float* lsep = p.lse ? p.lse + qrow0 : nullptr;
       if (sh.wph == 1) {
-        // this warp alone holds the head tile's state
+        // This warp alone holds the head tile's state.  Its head dims form
+        // runs of consecutive dims (vdim), written 4 at a time.
         const float r0 = l0 > 0.f ? p.v_scale / l0 : 0.f;
         const float r1 = l1 > 0.f ? p.v_scale / l1 : 0.f;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
+        for (int hh = 0; hh < 2; ++hh) {
+          const bool vh = hh ? v1 : v0;
+          const long long li = hh ? li1 : li0;
+          const float rs = hh ? r1 : r0;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int d = vdim<D, ELEM>(t, 2 * q + e);
-            if (seg.complete) {
-              if (v0) outp[(long long)li0 * D + d] = QType<QT>::from_f32(o[t][e] * r0);
-              if (v1) outp[(long long)li1 * D + d] = QType<QT>::from_f32(o[t][2 + e] * r1);
-            } else {
-              if (v0) part[(long long)li0 * D + d] = o[t][e];
-              if (v1) part[(long long)li1 * D + d] = o[t][2 + e];
+#pragma unroll
+            for (int t4 = 0; t4 < NT / 4; ++t4) {
+              const int d = vdim<D, ELEM>(4 * t4, 2 * q + e);
+              const float a0 = o[4 * t4][2 * hh + e], a1 = o[4 * t4 + 1][2 * hh + e];
+              const float a2 = o[4 * t4 + 2][2 * hh + e], a3 = o[4 * t4 + 3][2 * hh + e];
+              if (!vh) continue;
+              if (seg.complete) {
+                uint2 w;
+                w.x = pack_f32x2(a0 * rs, a1 * rs, BF16);
+                w.y = pack_f32x2(a2 * rs, a3 * rs, BF16);
+                *reinterpret_cast<uint2*>(outp + li * D + d) = w;
+              } else {
+                *reinterpret_cast<float4*>(part + li * D + d) = make_float4(a0, a1, a2, a3);
+              }
             }
           }
         }
@@ -656,39 +693,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // stage every warp's state in shared memory, then the wph warps of a
-        // head tile merge its 16 x D outputs together
-        float* mine = merge + warp * 16 * (D + 2);
+        // Stage every warp's state in shared memory, then the wph warps of a
+        // head tile merge its 16 x D outputs together.  A staged row has 4
+        // floats of padding after every 32 dims, which spreads the float4
+        // stores of the 4 lanes of a row over different banks.
+        constexpr int RS = D + D / 8;                 // padded row stride (floats)
+        constexpr int WS = 16 * RS + 32;              // one warp's area (+ m, l)
+        float* mine = merge + warp * WS;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
+        for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int d = vdim<D, ELEM>(t, 2 * q + e);
-            mine[r * D + d] = o[t][e];
-            mine[(r + 8) * D + d] = o[t][2 + e];
+#pragma unroll
+            for (int t4 = 0; t4 < NT / 4; ++t4) {
+              const int d = vdim<D, ELEM>(4 * t4, 2 * q + e);
+              *reinterpret_cast<float4*>(mine + (r + 8 * hh) * RS + d + 4 * (d >> 5)) =
+                  make_float4(o[4 * t4][2 * hh + e], o[4 * t4 + 1][2 * hh + e],
+                              o[4 * t4 + 2][2 * hh + e], o[4 * t4 + 3][2 * hh + e]);
+            }
           }
         }
         if (q == 0) {
-          mine[16 * D + r] = m0;
-          mine[16 * D + r + 8] = m1;
-          mine[16 * D + 16 + r] = l0;
-          mine[16 * D + 16 + r + 8] = l1;
+          mine[16 * RS + r] = m0;
+          mine[16 * RS + r + 8] = m1;
+          mine[16 * RS + 16 + r] = l0;
+          mine[16 * RS + 16 + r + 8] = l1;
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
-        const float* grp = merge + (ht * sh.wph) * 16 * (D + 2);
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        const float* grp = merge + (ht * sh.wph) * WS;
         for (int idx = ts * 32 + lane; idx < 16 * D; idx += sh.wph * 32) {
           const int row = idx / D, d = idx - row * D;
           const int lh = mtile * 16 + row;
           if (lh >= G) continue;
           float M = -INFINITY;
-          for (int w2 = 0; w2 < sh.wph; ++w2) M = fmaxf(M, grp[w2 * 16 * (D + 2) + 16 * D + row]);
+          for (int w2 = 0; w2 < sh.wph; ++w2) M = fmaxf(M, grp[w2 * WS + 16 * RS + row]);
           float L = 0.f, A = 0.f;
           for (int w2 = 0; w2 < sh.wph; ++w2) {
-            const float* g2 = grp + w2 * 16 * (D + 2);
-            const float mw = g2[16 * D + row];
+            const float* g2 = grp + w2 * WS;
+            const float mw = g2[16 * RS + row];
             const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-            L = fmaf(g2[16 * D + 16 + row], f, L);
-            A = fmaf(g2[row * D + d], f, A);
+            L = fmaf(g2[16 * RS + 16 + row], f, L);
+            A = fmaf(g2[row * RS + d + 4 * (d >> 5)], f, A);
           }
           const int li = kvl * G + lh;
           if (seg.complete) {
@@ -699,16 +744,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (d == 0) pml[li] = make_float2(M, L);
           }
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
       }
-  }
-  if (issuer && *(volatile int*)&sm.abort_flag) {
-    // drain: copies of the last S issued tiles must land before the CTA exits
-    for (long long i = iss.n - S < 0 ? 0 : iss.n - S; i < iss.n; ++i)
-      mbar_wait(&sm.full[i % S], (uint32_t)((i / S) & 1));
+    }
   }
   __syncthreads();
 }
+
 
 // ---------------------------------------------------------------------------
 // Host side: tensor maps (cached), launch
@@ -730,10 +772,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct MapKey {
   const void* ptr;
   long long rows;
-  int kvh, d, dtype, box_rows, row_bytes;
+  int kvh, d, dtype, box_rows, row_bytes, heads;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && rows == o.rows && kvh == o.kvh && d == o.d && dtype == o.dtype &&
-           box_rows == o.box_rows && row_bytes == o.row_bytes;
+           box_rows == o.box_rows && row_bytes == o.row_bytes && heads == o.heads;
   }
 };
 
@@ -743,10 +785,13 @@ MapKey g_keys[kMapCache];
 CUtensorMap g_maps[kMapCache];
 int g_map_used = 0, g_map_next = 0;
 
-// 3-D view of a cache: {head_dim, kv_heads, rows}; box {row_bytes/elem, 1, box_rows}.
+// 3-D view of a cache.  heads == 0: dims {head_dim, kv_heads, rows}, box
+// {row_bytes/elem, 1, box_rows} (one head per box).  heads > 0: dims
+// {head_dim, rows, kv_heads}, box {row_bytes/elem, box_rows, heads}, so that
+// one box lands in shared memory as [heads][box_rows][row_bytes].
 bool get_map(const void* ptr, long long rows, int kvh, int d, int dtype, int box_rows,
-             int row_bytes, CUtensorMap* out) {
-  MapKey key{ptr, rows, kvh, d, dtype, box_rows, row_bytes};
+             int row_bytes, int heads, CUtensorMap* out) {
+  MapKey key{ptr, rows, kvh, d, dtype, box_rows, row_bytes, heads};
   std::lock_guard<std::mutex> lk(g_map_mu);
   for (int i = 0; i < g_map_used; ++i)
     if (g_keys[i] == key) {
@@ -761,6 +806,14 @@ bool get_map(const void* ptr, long long rows, int kvh, int d, int dtype, int box
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)kvh, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)d * elem, (cuuint64_t)d * elem * kvh};
   cuuint32_t box[3] = {(cuuint32_t)(row_bytes / elem), 1u, (cuuint32_t)box_rows};
+  if (heads > 0) {
+    dims[1] = (cuuint64_t)rows;
+    dims[2] = (cuuint64_t)kvh;
+    strides[0] = (cuuint64_t)d * elem * kvh;
+    strides[1] = (cuuint64_t)d * elem;
+    box[1] = (cuuint32_t)box_rows;
+    box[2] = (cuuint32_t)heads;
+  }
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUtensorMap m;
   CUresult res = fn(&m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -827,15 +880,25 @@ void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms
 
 cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {
   if (p.kv_rows >= (1ll << 31)) return cudaErrorInvalidValue;
-  const Shape sh = make_shape(p.group, p.num_kv_heads, p.head_dim, p.kv_dtype,
-                              p.block_table ? p.page_size : 0);
+  Shape sh = make_shape(p.group, p.num_kv_heads, p.head_dim, p.kv_dtype,
+                        p.block_table ? p.page_size : 0);
   if (sh.stages < 2 || sh.tile != p.tile || sh.hc != p.hc) return cudaErrorInvalidValue;
   CUtensorMap mk, mv;
-  if (!get_map(p.k, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
-               &mk) ||
-      !get_map(p.v, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
-               &mv))
+  // Prefer one box per tile covering all hc heads (fewer, larger TMA copies);
+  // fall back to one box per head when the tile spans several pages or the
+  // driver refuses the head-minor view.
+  if (sh.hc > 1 && sh.box_rows == sh.tile &&
+      get_map(p.k, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
+              sh.hc, &mk) &&
+      get_map(p.v, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
+              sh.hc, &mv)) {
+    sh.heads_box = 1;
+  } else if (!get_map(p.k, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows,
+                      sh.row_bytes, 0, &mk) ||
+             !get_map(p.v, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows,
+                      sh.row_bytes, 0, &mv)) {
     return cudaErrorInvalidValue;
+  }
   if (p.head_dim == 128) return launch_d<128>(p, sh, mk, mv, stream);
   return launch_d<64>(p, sh, mk, mv, stream);
 }

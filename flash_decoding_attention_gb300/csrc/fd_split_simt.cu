@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p
   __shared__ long long red[34];
 
   const PlanResult plan = compute_plan(p, red);
+  allow_dependent_launch();
   SegmentIter it;
   it.init(p, plan);
 
