@@ -11,42 +11,45 @@
 // Streams held by a single CTA were finalised by the split kernel; streams
 // with no token get out = 0 and lse = -inf here.
 //
-// One warp merges one (stream, query head): its lanes first read the
-// segments' (m, l) in parallel, then sweep the accumulators with several
-// segment loads in flight per lane.
 #include "fd_common.cuh"
 
 namespace fd {
 namespace {
 
 constexpr int kCombineWarps = 4;
-constexpr int kMaxSegments = 1024;   // per stream; more are merged in chunks
 
 // Segment k of a stream whose first tile is in CTA c0 -> its partial slot:
 // the first CTA's "last" slot, then each later CTA's "first" slot.
 __device__ __forceinline__ int seg_slot(int c0, int k) { return k == 0 ? 2 * c0 + 1 : 2 * (c0 + k); }
 
+// One CTA merges one (stream, query head).  Its threads first take the max
+// of the segments' m together; then warp w accumulates segments w, w + 4, ...
+// (lanes over head dims, several segment loads in flight), and warp 0 adds
+// the four warps' sums.
 template <typename QT, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Params p) {
   constexpr int DPL = D / 32;
-  __shared__ float wts[kCombineWarps][kMaxSegments];
+  __shared__ float red_m[kCombineWarps];
+  __shared__ float red_l[kCombineWarps];
+  __shared__ float red_a[kCombineWarps][D];
   // wait for the split kernel (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.batch * p.hg;
-  const long long gw = (long long)blockIdx.x * kCombineWarps + warp;
-  if (gw >= (long long)S * p.hq) return;
-  const int s = (int)(gw / p.hq), i = (int)(gw - (long long)s * p.hq);
+  const int s = blockIdx.x / p.hq, i = blockIdx.x - (blockIdx.x / p.hq) * p.hq;
+  if (s >= S) return;
   const int b = s / p.hg, j = s - b * p.hg;
   const int qh = j * p.hq + i;
-  QT* out = static_cast<QT*>(p.out) + ((long long)b * p.num_q_heads + qh) * D + lane * DPL;
+  QT* out = static_cast<QT*>(p.out) + ((long long)b * p.num_q_heads + qh) * D;
   float* lse = p.lse ? p.lse + (long long)b * p.num_q_heads + qh : nullptr;
 
   const long long P0 = p.prefix[s], P1 = p.prefix[s + 1], total = p.prefix[S];
   if (P1 == P0) {
+    if (warp == 0) {
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) out[k] = QType<QT>::from_f32(0.f);
-    if (lse && lane == 0) *lse = -INFINITY;
+      for (int k = 0; k < DPL; ++k) out[lane * DPL + k] = QType<QT>::from_f32(0.f);
+      if (lse && lane == 0) *lse = -INFINITY;
+    }
     return;
   }
   const long long per_cta = (total + p.grid - 1) / p.grid;
@@ -55,45 +58,54 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
   const int nseg = c1 - c0 + 1;
 
   float M = -INFINITY;
-  for (int k = lane; k < nseg; k += 32) M = fmaxf(M, p.part_ml[(long long)seg_slot(c0, k) * p.hq + i].x);
+  for (int k = threadIdx.x; k < nseg; k += blockDim.x)
+    M = fmaxf(M, p.part_ml[(long long)seg_slot(c0, k) * p.hq + i].x);
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red_m[warp] = M;
+  __syncthreads();
+  M = red_m[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, red_m[w]);
 
   float L = 0.f, acc[DPL];
 #pragma unroll
   for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
-  for (int k0 = 0; k0 < nseg; k0 += kMaxSegments) {
-    const int kn = min(kMaxSegments, nseg - k0);
-    for (int k = lane; k < kn; k += 32) {
-      const float2 ml = p.part_ml[(long long)seg_slot(c0, k0 + k) * p.hq + i];
-      const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-      wts[warp][k] = f;
-      L = fmaf(ml.y, f, L);
-    }
-    __syncwarp();
 #pragma unroll 8
-    for (int k = 0; k < kn; ++k) {
-      const float f = wts[warp][k];
-      const float* a = p.part_acc + ((long long)seg_slot(c0, k0 + k) * p.hq + i) * D + lane * DPL;
-      if constexpr (DPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(a);
-        acc[0] = fmaf(v.x, f, acc[0]);
-        acc[1] = fmaf(v.y, f, acc[1]);
-        acc[2] = fmaf(v.z, f, acc[2]);
-        acc[3] = fmaf(v.w, f, acc[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(a);
-        acc[0] = fmaf(v.x, f, acc[0]);
-        acc[1] = fmaf(v.y, f, acc[1]);
-      }
+  for (int k = warp; k < nseg; k += kCombineWarps) {
+    const long long slot = seg_slot(c0, k);
+    const float2 ml = p.part_ml[slot * p.hq + i];
+    const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+    L = fmaf(ml.y, f, L);
+    const float* a = p.part_acc + (slot * p.hq + i) * D + lane * DPL;
+    if constexpr (DPL == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(a);
+      acc[0] = fmaf(v.x, f, acc[0]);
+      acc[1] = fmaf(v.y, f, acc[1]);
+      acc[2] = fmaf(v.z, f, acc[2]);
+      acc[3] = fmaf(v.w, f, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(a);
+      acc[0] = fmaf(v.x, f, acc[0]);
+      acc[1] = fmaf(v.y, f, acc[1]);
     }
-    __syncwarp();
   }
+  if (lane == 0) red_l[warp] = L;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  for (int k = 0; k < DPL; ++k) red_a[warp][lane * DPL + k] = acc[k];
+  __syncthreads();
+  if (warp != 0) return;
+  L = red_l[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) L += red_l[w];
   const float r = L > 0.f ? p.v_scale / L : 0.f;
 #pragma unroll
-  for (int k = 0; k < DPL; ++k) out[k] = QType<QT>::from_f32(acc[k] * r);
+  for (int k = 0; k < DPL; ++k) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) v += red_a[w][lane * DPL + k];
+    out[lane * DPL + k] = QType<QT>::from_f32(v * r);
+  }
   if (lse && lane == 0) *lse = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
@@ -102,8 +114,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
 // until the split kernel has completed and its writes are visible.
 template <typename QT, int D>
 cudaError_t launch_t(const Params& p, cudaStream_t stream) {
-  const long long warps = (long long)p.batch * p.hg * p.hq;
-  const long long blocks = (warps + kCombineWarps - 1) / kCombineWarps;
+  const long long blocks = (long long)p.batch * p.hg * p.hq;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kCombineWarps * 32);

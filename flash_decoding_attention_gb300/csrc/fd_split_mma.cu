@@ -59,8 +59,8 @@ struct Shape {
   int mt;            // 16-row head tiles per KV head (power of two)
   int hc;            // KV heads per stream
   int wph;           // consumer warps per head tile
-  int r;             // 16-token sub-tiles per warp per stage
-  int tile;          // tokens per stage = 16 * wph * r
+  int r;             // consumer sub-tiles (32 tokens for FP8, 16 for 16-bit KV) per warp per stage
+  int tile;          // tokens per stage = sub-tile tokens * wph * r
   int box_rows;      // rows per TMA box
   int row_bytes;     // bytes of one swizzled row of a box (128 or 64)
   int nx;            // boxes across head_dim (head_dim * elem / row_bytes)
@@ -91,13 +91,13 @@ Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int pa
   const int row_elems_bytes = head_dim * elem;
   s.row_bytes = row_elems_bytes >= 128 ? 128 : 64;
   s.nx = row_elems_bytes / s.row_bytes;
-  const int per_subtile = 16 * s.wph * s.hc * row_elems_bytes * 2;   // K+V bytes per r step
-  const int target = elem == 1 ? 32768 : 65536;
-  s.r = target / per_subtile;
+  const int sub = elem == 1 ? 32 : 16;   // tokens per consumer sub-tile (matches the kernel)
+  const int per_subtile = sub * s.wph * s.hc * row_elems_bytes * 2;   // K+V bytes per r step
+  s.r = 65536 / per_subtile;
   if (s.r < 1) s.r = 1;
   if (s.r > 4) s.r = 4;
-  while (16 * s.wph * s.r > 256) s.r >>= 1;   // TMA box height <= 256
-  s.tile = 16 * s.wph * s.r;
+  while (s.r > 1 && sub * s.wph * s.r > 256) s.r >>= 1;   // TMA box height <= 256
+  s.tile = sub * s.wph * s.r;
   s.box_rows = page_size > 0 && page_size < s.tile ? page_size : s.tile;
   s.region_bytes = s.tile * s.row_bytes;
   s.heads_box = 0;   // decided at launch (needs a tensor map over {dims, rows, heads})
@@ -274,6 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool BF16 = std::is_same<QT, __nv_bfloat16>::value;
   constexpr int KSTEPS = D / 16;
   constexpr int NT = D / 8;     // n-tiles of the PV product
+  constexpr int SUB = ELEM == 1 ? 32 : 16;   // tokens per sub-tile (one softmax step)
+  constexpr int NJ = SUB / 8;                // n-tiles of the QK product
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Shared sm;
 
@@ -461,83 +463,88 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vreg = kreg + sh.kv_bytes;
 #pragma unroll 1
           for (int rr = 0; rr < sh.r; ++rr) {
-            const int sub = ts * 16 * sh.r + 16 * rr;     // first token of the sub-tile in the tile
+            const int sub = ts * SUB * sh.r + SUB * rr;   // first token of the sub-tile in the tile
             const int left = seg.t_end - (t0 + sub);      // valid tokens from the sub-tile start
             if (left <= 0) break;
-            // ---- S = Q K^T  (2 n-tiles of 8 tokens).  Each Q fragment is read
-            //      from shared memory once and used for both n-tiles.
-            float s[2][4];
+            // ---- S = Q K^T over NJ n-tiles of 8 tokens.  Each Q fragment is
+            //      read from shared memory once and used for every n-tile.
+            float s[NJ][4];
 #pragma unroll
-            for (int jn = 0; jn < 2; ++jn) s[jn][0] = s[jn][1] = s[jn][2] = s[jn][3] = 0.f;
-            const int tk0 = sub + r, tk1 = sub + 8 + r;   // this lane's K rows
+            for (int jn = 0; jn < NJ; ++jn) s[jn][0] = s[jn][1] = s[jn][2] = s[jn][3] = 0.f;
             if constexpr (ELEM == 1 && D == 128) {
-              const uint4 a0 = lds128(chunk_addr(kreg, tk0, 2 * q, sh.row_bytes));
-              const uint4 a1 = lds128(chunk_addr(kreg, tk0, 2 * q + 1, sh.row_bytes));
-              const uint4 b0 = lds128(chunk_addr(kreg, tk1, 2 * q, sh.row_bytes));
-              const uint4 b1 = lds128(chunk_addr(kreg, tk1, 2 * q + 1, sh.row_bytes));
-              const uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-              const uint32_t w1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+              uint32_t w[NJ][8];
+#pragma unroll
+              for (int jn = 0; jn < NJ; ++jn) {
+                const int tk = sub + 8 * jn + r;
+                const uint4 a0 = lds128(chunk_addr(kreg, tk, 2 * q, sh.row_bytes));
+                const uint4 a1 = lds128(chunk_addr(kreg, tk, 2 * q + 1, sh.row_bytes));
+                w[jn][0] = a0.x; w[jn][1] = a0.y; w[jn][2] = a0.z; w[jn][3] = a0.w;
+                w[jn][4] = a1.x; w[jn][5] = a1.y; w[jn][6] = a1.z; w[jn][7] = a1.w;
+              }
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint4 a = lds128(qf + kk * 512);
-                mma16816<BF16>(s[0], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w0[kk]),
-                               widen_e4m3x2<BF16>(w0[kk] >> 16));
-                mma16816<BF16>(s[1], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w1[kk]),
-                               widen_e4m3x2<BF16>(w1[kk] >> 16));
+#pragma unroll
+                for (int jn = 0; jn < NJ; ++jn)
+                  mma16816<BF16>(s[jn], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w[jn][kk]),
+                                 widen_e4m3x2<BF16>(w[jn][kk] >> 16));
               }
             } else if constexpr (ELEM == 1) {   // D == 64, 64-byte rows
-              const uint4 a0 = lds128(chunk_addr(kreg, tk0, q, sh.row_bytes));
-              const uint4 b0 = lds128(chunk_addr(kreg, tk1, q, sh.row_bytes));
-              const uint32_t w0[4] = {a0.x, a0.y, a0.z, a0.w};
-              const uint32_t w1[4] = {b0.x, b0.y, b0.z, b0.w};
+              uint32_t w[NJ][4];
+#pragma unroll
+              for (int jn = 0; jn < NJ; ++jn) {
+                const uint4 a0 = lds128(chunk_addr(kreg, sub + 8 * jn + r, q, sh.row_bytes));
+                w[jn][0] = a0.x; w[jn][1] = a0.y; w[jn][2] = a0.z; w[jn][3] = a0.w;
+              }
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint4 a = lds128(qf + kk * 512);
-                mma16816<BF16>(s[0], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w0[kk]),
-                               widen_e4m3x2<BF16>(w0[kk] >> 16));
-                mma16816<BF16>(s[1], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w1[kk]),
-                               widen_e4m3x2<BF16>(w1[kk] >> 16));
+#pragma unroll
+                for (int jn = 0; jn < NJ; ++jn)
+                  mma16816<BF16>(s[jn], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w[jn][kk]),
+                                 widen_e4m3x2<BF16>(w[jn][kk] >> 16));
               }
             } else {   // 16-bit: chunk pairs (2q, 2q+1) of each 128-byte region
 #pragma unroll
               for (int x2 = 0; x2 < D / 64; ++x2) {
                 const uint32_t reg = kreg + x2 * xstride;
-                uint4 c0[2], c1[2];
-                c0[0] = lds128(chunk_addr(reg, tk0, 2 * q, sh.row_bytes));
-                c0[1] = lds128(chunk_addr(reg, tk0, 2 * q + 1, sh.row_bytes));
-                c1[0] = lds128(chunk_addr(reg, tk1, 2 * q, sh.row_bytes));
-                c1[1] = lds128(chunk_addr(reg, tk1, 2 * q + 1, sh.row_bytes));
+                uint4 c[NJ][2];
+#pragma unroll
+                for (int jn = 0; jn < NJ; ++jn) {
+                  c[jn][0] = lds128(chunk_addr(reg, sub + 8 * jn + r, 2 * q, sh.row_bytes));
+                  c[jn][1] = lds128(chunk_addr(reg, sub + 8 * jn + r, 2 * q + 1, sh.row_bytes));
+                }
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
-                  const int kk = x2 * 4 + k4;
-                  const uint4 a = lds128(qf + kk * 512);
-                  const uint4 p0 = c0[k4 >> 1], p1 = c1[k4 >> 1];
-                  mma16816<BF16>(s[0], a.x, a.y, a.z, a.w, (k4 & 1) ? p0.z : p0.x,
-                                 (k4 & 1) ? p0.w : p0.y);
-                  mma16816<BF16>(s[1], a.x, a.y, a.z, a.w, (k4 & 1) ? p1.z : p1.x,
-                                 (k4 & 1) ? p1.w : p1.y);
+                  const uint4 a = lds128(qf + (x2 * 4 + k4) * 512);
+#pragma unroll
+                  for (int jn = 0; jn < NJ; ++jn) {
+                    const uint4 pp = c[jn][k4 >> 1];
+                    mma16816<BF16>(s[jn], a.x, a.y, a.z, a.w, (k4 & 1) ? pp.z : pp.x,
+                                   (k4 & 1) ? pp.w : pp.y);
+                  }
                 }
               }
             }
             // ---- online softmax (rows r and r + 8; this lane holds tokens
-            //      8*jn + 2q + {0,1})
-            float x[2][4];
+            //      8*jn + 2q + {0,1} of the sub-tile)
+            float pr[NJ][4];
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int jn = 0; jn < 2; ++jn) {
+            for (int jn = 0; jn < NJ; ++jn) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int tok = 8 * jn + 2 * q + (e & 1);
                 float v = s[jn][e] * p.score_scale;
-                if (tok >= left) v = -INFINITY;
-                x[jn][e] = v;
+                if (left < SUB && tok >= left) v = -INFINITY;   // ragged end of the segment
+                pr[jn][e] = v;
               }
-              mx0 = fmaxf(mx0, fmaxf(x[jn][0], x[jn][1]));
-              mx1 = fmaxf(mx1, fmaxf(x[jn][2], x[jn][3]));
+              mx0 = fmaxf(mx0, fmaxf(pr[jn][0], pr[jn][1]));
+              mx1 = fmaxf(mx1, fmaxf(pr[jn][2], pr[jn][3]));
             }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
             const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
             const float base0 = mn0 == -INFINITY ? 0.f : mn0;
@@ -545,14 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float a0 = fast_exp2(m0 - base0), a1 = fast_exp2(m1 - base1);
             m0 = mn0;
             m1 = mn1;
-            float pr[2][4];
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-            for (int jn = 0; jn < 2; ++jn) {
-              pr[jn][0] = fast_exp2(x[jn][0] - base0);
-              pr[jn][1] = fast_exp2(x[jn][1] - base0);
-              pr[jn][2] = fast_exp2(x[jn][2] - base1);
-              pr[jn][3] = fast_exp2(x[jn][3] - base1);
+            for (int jn = 0; jn < NJ; ++jn) {
+              pr[jn][0] = fast_exp2(pr[jn][0] - base0);
+              pr[jn][1] = fast_exp2(pr[jn][1] - base0);
+              pr[jn][2] = fast_exp2(pr[jn][2] - base1);
+              pr[jn][3] = fast_exp2(pr[jn][3] - base1);
               ps0 += pr[jn][0] + pr[jn][1];
               ps1 += pr[jn][2] + pr[jn][3];
             }
@@ -567,75 +573,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o[t][3] *= a1;
               }
             }
-            const uint32_t pa0 = pack_f32x2(pr[0][0], pr[0][1], BF16);
-            const uint32_t pa1 = pack_f32x2(pr[0][2], pr[0][3], BF16);
-            const uint32_t pa2 = pack_f32x2(pr[1][0], pr[1][1], BF16);
-            const uint32_t pa3 = pack_f32x2(pr[1][2], pr[1][3], BF16);
-            // ---- O += P V ; this lane's B fragments: tokens 2q, 2q+1 (b0)
-            //      and 2q+8, 2q+9 (b1), head dims vdim(j, r)
-            const int u0 = sub + 2 * q, u1 = u0 + 1, u2 = u0 + 8, u3 = u0 + 9;
-            if constexpr (ELEM == 1 && D == 128) {
-              const uint4 w0 = lds128(chunk_addr(vreg, u0, r, sh.row_bytes));
-              const uint4 w1 = lds128(chunk_addr(vreg, u1, r, sh.row_bytes));
-              const uint4 w2 = lds128(chunk_addr(vreg, u2, r, sh.row_bytes));
-              const uint4 w3 = lds128(chunk_addr(vreg, u3, r, sh.row_bytes));
-              const uint32_t A[4] = {w0.x, w0.y, w0.z, w0.w}, B[4] = {w1.x, w1.y, w1.z, w1.w};
-              const uint32_t C[4] = {w2.x, w2.y, w2.z, w2.w}, E[4] = {w3.x, w3.y, w3.z, w3.w};
+            // ---- O += P V, one k-step of 16 tokens at a time.  This lane's B
+            //      fragments: tokens 2q, 2q+1 (b0) and 2q+8, 2q+9 (b1) of the
+            //      k-step, head dims vdim(j, r).
 #pragma unroll
-              for (int wd = 0; wd < 4; ++wd) {
-                const uint32_t lo01 = __byte_perm(A[wd], B[wd], 0x5140);
-                const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
-                const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
-                const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
-                mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01),
-                               widen_e4m3x2<BF16>(lo89));
-                mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01 >> 16),
-                               widen_e4m3x2<BF16>(lo89 >> 16));
-                mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01),
-                               widen_e4m3x2<BF16>(hi89));
-                mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01 >> 16),
-                               widen_e4m3x2<BF16>(hi89 >> 16));
-              }
-            } else if constexpr (ELEM == 1) {   // D == 64: 8 bytes per token
-              const int c = r >> 1, half = (r & 1) * 8;
-              const uint2 w0 = lds64(chunk_addr(vreg, u0, c, sh.row_bytes) + half);
-              const uint2 w1 = lds64(chunk_addr(vreg, u1, c, sh.row_bytes) + half);
-              const uint2 w2 = lds64(chunk_addr(vreg, u2, c, sh.row_bytes) + half);
-              const uint2 w3 = lds64(chunk_addr(vreg, u3, c, sh.row_bytes) + half);
-              const uint32_t A[2] = {w0.x, w0.y}, B[2] = {w1.x, w1.y};
-              const uint32_t C[2] = {w2.x, w2.y}, E[2] = {w3.x, w3.y};
-#pragma unroll
-              for (int wd = 0; wd < 2; ++wd) {
-                const uint32_t lo01 = __byte_perm(A[wd], B[wd], 0x5140);
-                const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
-                const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
-                const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
-                mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01),
-                               widen_e4m3x2<BF16>(lo89));
-                mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01 >> 16),
-                               widen_e4m3x2<BF16>(lo89 >> 16));
-                mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01),
-                               widen_e4m3x2<BF16>(hi89));
-                mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01 >> 16),
-                               widen_e4m3x2<BF16>(hi89 >> 16));
-              }
-            } else {   // 16-bit: chunk r of each 128-byte region holds 8 dims
-#pragma unroll
-              for (int x2 = 0; x2 < D / 64; ++x2) {
-                const uint32_t reg = vreg + x2 * xstride;
-                const uint4 w0 = lds128(chunk_addr(reg, u0, r, sh.row_bytes));
-                const uint4 w1 = lds128(chunk_addr(reg, u1, r, sh.row_bytes));
-                const uint4 w2 = lds128(chunk_addr(reg, u2, r, sh.row_bytes));
-                const uint4 w3 = lds128(chunk_addr(reg, u3, r, sh.row_bytes));
+            for (int kt = 0; kt < SUB / 16; ++kt) {
+              const uint32_t pa0 = pack_f32x2(pr[2 * kt][0], pr[2 * kt][1], BF16);
+              const uint32_t pa1 = pack_f32x2(pr[2 * kt][2], pr[2 * kt][3], BF16);
+              const uint32_t pa2 = pack_f32x2(pr[2 * kt + 1][0], pr[2 * kt + 1][1], BF16);
+              const uint32_t pa3 = pack_f32x2(pr[2 * kt + 1][2], pr[2 * kt + 1][3], BF16);
+              const int u0 = sub + 16 * kt + 2 * q, u1 = u0 + 1, u2 = u0 + 8, u3 = u0 + 9;
+              if constexpr (ELEM == 1 && D == 128) {
+                const uint4 w0 = lds128(chunk_addr(vreg, u0, r, sh.row_bytes));
+                const uint4 w1 = lds128(chunk_addr(vreg, u1, r, sh.row_bytes));
+                const uint4 w2 = lds128(chunk_addr(vreg, u2, r, sh.row_bytes));
+                const uint4 w3 = lds128(chunk_addr(vreg, u3, r, sh.row_bytes));
                 const uint32_t A[4] = {w0.x, w0.y, w0.z, w0.w}, B[4] = {w1.x, w1.y, w1.z, w1.w};
                 const uint32_t C[4] = {w2.x, w2.y, w2.z, w2.w}, E[4] = {w3.x, w3.y, w3.z, w3.w};
 #pragma unroll
                 for (int wd = 0; wd < 4; ++wd) {
-                  const int jt = x2 * 8 + 2 * wd;
-                  mma16816<BF16>(o[jt], pa0, pa1, pa2, pa3, __byte_perm(A[wd], B[wd], 0x5410),
-                                 __byte_perm(C[wd], E[wd], 0x5410));
-                  mma16816<BF16>(o[jt + 1], pa0, pa1, pa2, pa3, __byte_perm(A[wd], B[wd], 0x7632),
-                                 __byte_perm(C[wd], E[wd], 0x7632));
+                  const uint32_t lo01 = __byte_perm(A[wd], B[wd], 0x5140);
+                  const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
+                  const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
+                  const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
+                  mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01),
+                                 widen_e4m3x2<BF16>(lo89));
+                  mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01 >> 16),
+                                 widen_e4m3x2<BF16>(lo89 >> 16));
+                  mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01),
+                                 widen_e4m3x2<BF16>(hi89));
+                  mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01 >> 16),
+                                 widen_e4m3x2<BF16>(hi89 >> 16));
+                }
+              } else if constexpr (ELEM == 1) {   // D == 64: 8 bytes per token
+                const int c = r >> 1, half = (r & 1) * 8;
+                const uint2 w0 = lds64(chunk_addr(vreg, u0, c, sh.row_bytes) + half);
+                const uint2 w1 = lds64(chunk_addr(vreg, u1, c, sh.row_bytes) + half);
+                const uint2 w2 = lds64(chunk_addr(vreg, u2, c, sh.row_bytes) + half);
+                const uint2 w3 = lds64(chunk_addr(vreg, u3, c, sh.row_bytes) + half);
+                const uint32_t A[2] = {w0.x, w0.y}, B[2] = {w1.x, w1.y};
+                const uint32_t C[2] = {w2.x, w2.y}, E[2] = {w3.x, w3.y};
+#pragma unroll
+                for (int wd = 0; wd < 2; ++wd) {
+                  const uint32_t lo01 = __byte_perm(A[wd], B[wd], 0x5140);
+                  const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
+                  const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
+                  const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
+                  mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01),
+                                 widen_e4m3x2<BF16>(lo89));
+                  mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01 >> 16),
+                                 widen_e4m3x2<BF16>(lo89 >> 16));
+                  mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01),
+                                 widen_e4m3x2<BF16>(hi89));
+                  mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01 >> 16),
+                                 widen_e4m3x2<BF16>(hi89 >> 16));
+                }
+              } else {   // 16-bit: chunk r of each 128-byte region holds 8 dims
+#pragma unroll
+                for (int x2 = 0; x2 < D / 64; ++x2) {
+                  const uint32_t reg = vreg + x2 * xstride;
+                  const uint4 w0 = lds128(chunk_addr(reg, u0, r, sh.row_bytes));
+                  const uint4 w1 = lds128(chunk_addr(reg, u1, r, sh.row_bytes));
+                  const uint4 w2 = lds128(chunk_addr(reg, u2, r, sh.row_bytes));
+                  const uint4 w3 = lds128(chunk_addr(reg, u3, r, sh.row_bytes));
+                  const uint32_t A[4] = {w0.x, w0.y, w0.z, w0.w}, B[4] = {w1.x, w1.y, w1.z, w1.w};
+                  const uint32_t C[4] = {w2.x, w2.y, w2.z, w2.w}, E[4] = {w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+                  for (int wd = 0; wd < 4; ++wd) {
+                    const int jt = x2 * 8 + 2 * wd;
+                    mma16816<BF16>(o[jt], pa0, pa1, pa2, pa3, __byte_perm(A[wd], B[wd], 0x5410),
+                                   __byte_perm(C[wd], E[wd], 0x5410));
+                    mma16816<BF16>(o[jt + 1], pa0, pa1, pa2, pa3, __byte_perm(A[wd], B[wd], 0x7632),
+                                   __byte_perm(C[wd], E[wd], 0x7632));
+                  }
                 }
               }
             }
@@ -720,27 +730,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           mine[16 * RS + 16 + r + 8] = l1;
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        // each warp of the head tile merges whole rows, a lane 4 dims of one
+        // row; the row's weights come from broadcast reads of m and l
         const float* grp = merge + (ht * sh.wph) * WS;
-        for (int idx = ts * 32 + lane; idx < 16 * D; idx += sh.wph * 32) {
-          const int row = idx / D, d = idx - row * D;
+        for (int idx = ts * 32 + lane; idx < 16 * (D / 4); idx += sh.wph * 32) {
+          const int row = idx / (D / 4), d = 4 * (idx - row * (D / 4));
           const int lh = mtile * 16 + row;
           if (lh >= G) continue;
           float M = -INFINITY;
           for (int w2 = 0; w2 < sh.wph; ++w2) M = fmaxf(M, grp[w2 * WS + 16 * RS + row]);
-          float L = 0.f, A = 0.f;
+          float L = 0.f;
+          float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
           for (int w2 = 0; w2 < sh.wph; ++w2) {
             const float* g2 = grp + w2 * WS;
             const float mw = g2[16 * RS + row];
             const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
             L = fmaf(g2[16 * RS + 16 + row], f, L);
-            A = fmaf(g2[row * RS + d + 4 * (d >> 5)], f, A);
+            const float4 v = *reinterpret_cast<const float4*>(g2 + row * RS + d + 4 * (d >> 5));
+            A.x = fmaf(v.x, f, A.x);
+            A.y = fmaf(v.y, f, A.y);
+            A.z = fmaf(v.z, f, A.z);
+            A.w = fmaf(v.w, f, A.w);
           }
           const int li = kvl * G + lh;
           if (seg.complete) {
-            outp[(long long)li * D + d] = QType<QT>::from_f32(L > 0.f ? A * (p.v_scale / L) : 0.f);
+            const float rs = L > 0.f ? p.v_scale / L : 0.f;
+            uint2 w;
+            w.x = pack_f32x2(A.x * rs, A.y * rs, BF16);
+            w.y = pack_f32x2(A.z * rs, A.w * rs, BF16);
+            *reinterpret_cast<uint2*>(outp + (long long)li * D + d) = w;
             if (d == 0 && lsep) lsep[li] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
           } else {
-            part[(long long)li * D + d] = A;
+            *reinterpret_cast<float4*>(part + (long long)li * D + d) = A;
             if (d == 0) pml[li] = make_float2(M, L);
           }
         }
