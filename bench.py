@@ -52,6 +52,22 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Largest value over the ranks of the default process group (the
+    slowest replica sets the whole job's time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Units processed by all replicas (each does the same work) per second
+    of the slowest one."""
+    return units_per_rank * world / max_seconds
+
+
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, on the host cores
 # ---------------------------------------------------------------------------
@@ -288,12 +304,10 @@ def run_gpu(args):
     split_ms = [a.elapsed_time(b) for a, b in sev]
     total_ms = sum(step_ms)
     if pg:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / K
     alg = w.algorithmic_bytes()
-    value = alg * world / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_throughput(alg, world, ms_per_step * 1e-3) / 1e9
 
     # end to end through the public API: pinned host inputs in, result out
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(K, 50))
@@ -330,10 +344,8 @@ def run_gpu(args):
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
         if pg:
-            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
-        e2e_val = alg * world / (e2e_ms * 1e-3) / 1e9
+            e2e_ms = max_over_ranks(e2e_ms, dev)
+        e2e_val = whole_job_throughput(alg, world, e2e_ms * 1e-3) / 1e9
         e2e = {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 

@@ -10,69 +10,79 @@
 //   out = v_scale * A / L,  lse = (M + log2 L) * ln 2.
 // Streams held by a single CTA were finalised by the split kernel; streams
 // with no token get out = 0 and lse = -inf here.
-//
+#include <type_traits>
+
 #include "fd_common.cuh"
 
 namespace fd {
 namespace {
 
-constexpr int kCombineWarps = 4;
+constexpr int kCombineWarps = 8;
 
 // Segment k of a stream whose first tile is in CTA c0 -> its partial slot:
 // the first CTA's "last" slot, then each later CTA's "first" slot.
 __device__ __forceinline__ int seg_slot(int c0, int k) { return k == 0 ? 2 * c0 + 1 : 2 * (c0 + k); }
 
-// One CTA merges one (stream, query head).  Its threads first take the max
-// of the segments' m together; then warp w accumulates segments w, w + 4, ...
-// (lanes over head dims, several segment loads in flight), and warp 0 adds
-// the four warps' sums.
-template <typename QT, int D>
+// One item = one (stream, query head).  A CTA of 8 warps takes 8 / WPI items;
+// the WPI warps of an item split its segments (segment k goes to part
+// k mod WPI), so that few long streams still spread their loads over many
+// warps, while many short ones run one warp per item in a single wave.
+template <typename QT, int D, int WPI>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Params p) {
   constexpr int DPL = D / 32;
+  constexpr int IPC = kCombineWarps / WPI;          // items per CTA
   __shared__ float red_m[kCombineWarps];
   __shared__ float red_l[kCombineWarps];
   __shared__ float red_a[kCombineWarps][D];
   // wait for the split kernel (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int part = warp % WPI, slot_in_cta = warp / WPI;
   const int S = p.batch * p.hg;
-  const int s = blockIdx.x / p.hq, i = blockIdx.x - (blockIdx.x / p.hq) * p.hq;
-  if (s >= S) return;
-  const int b = s / p.hg, j = s - b * p.hg;
-  const int qh = j * p.hq + i;
-  QT* out = static_cast<QT*>(p.out) + ((long long)b * p.num_q_heads + qh) * D;
-  float* lse = p.lse ? p.lse + (long long)b * p.num_q_heads + qh : nullptr;
-
-  const long long P0 = p.prefix[s], P1 = p.prefix[s + 1], total = p.prefix[S];
-  if (P1 == P0) {
-    if (warp == 0) {
+  const long long item = (long long)blockIdx.x * IPC + slot_in_cta;
+  const bool live = item < (long long)S * p.hq;
+  int s = 0, i = 0, nseg = 0, c0 = 0;
+  QT* out = nullptr;
+  float* lse = nullptr;
+  if (live) {
+    s = (int)(item / p.hq);
+    i = (int)(item - (long long)s * p.hq);
+    const int b = s / p.hg, j = s - b * p.hg;
+    const int qh = j * p.hq + i;
+    out = static_cast<QT*>(p.out) + ((long long)b * p.num_q_heads + qh) * D;
+    lse = p.lse ? p.lse + (long long)b * p.num_q_heads + qh : nullptr;
+    const long long P0 = p.prefix[s], P1 = p.prefix[s + 1], total = p.prefix[S];
+    if (P1 == P0) {
+      if (part == 0) {
 #pragma unroll
-      for (int k = 0; k < DPL; ++k) out[lane * DPL + k] = QType<QT>::from_f32(0.f);
-      if (lse && lane == 0) *lse = -INFINITY;
+        for (int k = 0; k < DPL; ++k) out[lane * DPL + k] = QType<QT>::from_f32(0.f);
+        if (lse && lane == 0) *lse = -INFINITY;
+      }
+    } else {
+      const long long per_cta = (total + p.grid - 1) / p.grid;
+      c0 = (int)(P0 / per_cta);
+      const int c1 = (int)((P1 - 1) / per_cta);
+      nseg = c0 == c1 ? 0 : c1 - c0 + 1;   // 0: the split kernel wrote the output
     }
-    return;
   }
-  const long long per_cta = (total + p.grid - 1) / p.grid;
-  const int c0 = (int)(P0 / per_cta), c1 = (int)((P1 - 1) / per_cta);
-  if (c0 == c1) return;
-  const int nseg = c1 - c0 + 1;
-
+  // max of m over this part's segments (lanes over segments)
   float M = -INFINITY;
-  for (int k = threadIdx.x; k < nseg; k += blockDim.x)
+  for (int k = part + WPI * lane; k < nseg; k += WPI * 32)
     M = fmaxf(M, p.part_ml[(long long)seg_slot(c0, k) * p.hq + i].x);
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) red_m[warp] = M;
-  __syncthreads();
-  M = red_m[0];
+  if constexpr (WPI > 1) {
+    if (lane == 0) red_m[warp] = M;
+    __syncthreads();
 #pragma unroll
-  for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, red_m[w]);
-
+    for (int w = 0; w < WPI; ++w) M = fmaxf(M, red_m[slot_in_cta * WPI + w]);
+  }
+  // weighted sums over this part's segments, several loads in flight
   float L = 0.f, acc[DPL];
 #pragma unroll
   for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
 #pragma unroll 8
-  for (int k = warp; k < nseg; k += kCombineWarps) {
+  for (int k = part; k < nseg; k += WPI) {
     const long long slot = seg_slot(c0, k);
     const float2 ml = p.part_ml[slot * p.hq + i];
     const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
@@ -90,21 +100,43 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
       acc[1] = fmaf(v.y, f, acc[1]);
     }
   }
-  if (lane == 0) red_l[warp] = L;
+  if constexpr (WPI > 1) {
+    if (lane == 0) red_l[warp] = L;
 #pragma unroll
-  for (int k = 0; k < DPL; ++k) red_a[warp][lane * DPL + k] = acc[k];
-  __syncthreads();
-  if (warp != 0) return;
-  L = red_l[0];
+    for (int k = 0; k < DPL; ++k) red_a[warp][lane * DPL + k] = acc[k];
+    __syncthreads();
+    if (part != 0) return;
+    L = 0.f;
 #pragma unroll
-  for (int w = 1; w < kCombineWarps; ++w) L += red_l[w];
+    for (int w = 0; w < WPI; ++w) L += red_l[slot_in_cta * WPI + w];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < WPI; ++w) v += red_a[slot_in_cta * WPI + w][lane * DPL + k];
+      acc[k] = v;
+    }
+  }
+  if (nseg == 0) return;
   const float r = L > 0.f ? p.v_scale / L : 0.f;
+  if constexpr (DPL == 4) {
+    uint2 w;
+    __half2 h0, h1;
+    if constexpr (std::is_same<QT, __half>::value) {
+      h0 = __floats2half2_rn(acc[0] * r, acc[1] * r);
+      h1 = __floats2half2_rn(acc[2] * r, acc[3] * r);
+      w.x = *reinterpret_cast<uint32_t*>(&h0);
+      w.y = *reinterpret_cast<uint32_t*>(&h1);
+    } else {
+      __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0] * r, acc[1] * r);
+      __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[2] * r, acc[3] * r);
+      w.x = *reinterpret_cast<uint32_t*>(&b0);
+      w.y = *reinterpret_cast<uint32_t*>(&b1);
+    }
+    *reinterpret_cast<uint2*>(out + lane * DPL) = w;
+  } else {
 #pragma unroll
-  for (int k = 0; k < DPL; ++k) {
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) v += red_a[w][lane * DPL + k];
-    out[lane * DPL + k] = QType<QT>::from_f32(v * r);
+    for (int k = 0; k < DPL; ++k) out[lane * DPL + k] = QType<QT>::from_f32(acc[k] * r);
   }
   if (lse && lane == 0) *lse = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
@@ -112,9 +144,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
 // Launched as a programmatic dependent of the split kernel: its CTAs may be
 // scheduled while the split kernel drains, and wait (griddepcontrol.wait)
 // until the split kernel has completed and its writes are visible.
-template <typename QT, int D>
-cudaError_t launch_t(const Params& p, cudaStream_t stream) {
-  const long long blocks = (long long)p.batch * p.hg * p.hq;
+template <typename QT, int D, int WPI>
+cudaError_t launch_w(const Params& p, cudaStream_t stream) {
+  const long long items = (long long)p.batch * p.hg * p.hq;
+  const long long blocks = (items + kCombineWarps / WPI - 1) / (kCombineWarps / WPI);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kCombineWarps * 32);
@@ -125,7 +158,18 @@ cudaError_t launch_t(const Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<QT, D>, p);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<QT, D, WPI>, p);
+}
+
+// Warps per item: enough to give every SM about 8 warps of merging work.
+template <typename QT, int D>
+cudaError_t launch_t(const Params& p, cudaStream_t stream) {
+  const long long items = (long long)p.batch * p.hg * p.hq;
+  const long long target = (long long)p.grid * kCombineWarps;
+  if (items * 4 <= target) return launch_w<QT, D, 8>(p, stream);
+  if (items * 2 <= target) return launch_w<QT, D, 4>(p, stream);
+  if (items <= target) return launch_w<QT, D, 2>(p, stream);
+  return launch_w<QT, D, 1>(p, stream);
 }
 
 }  // namespace
