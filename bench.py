@@ -158,6 +158,18 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        # nvidia-smi's start-up (NVML initialisation) can stall the GPU for a
+        # while: wait for its first two samples before anything is timed
+        t_end = time.time() + 10.0
+        while time.time() < t_end and self.proc.poll() is None:
+            try:
+                with open(self.path) as f:
+                    if sum(1 for _ in f) >= 2:
+                        break
+            except OSError:
+                pass
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -222,6 +234,9 @@ def recorded_traffic(kernel_name: str, config: int):
     return e.get("dram_bytes_per_launch")
 
 
+SYNC_EVERY = 64   # timed steps between host waits (keeps the launch queue short)
+
+
 def run_gpu(args):
     import torch
     import flash_decoding_attention_gb300 as fda
@@ -263,6 +278,7 @@ def run_gpu(args):
         flush_r.max()
 
     for _ in range(args.warmup):
+        flush()   # also loads the flush kernels before anything is timed
         step()
     torch.cuda.synchronize()
     st, info = fda.fd_check_device_error(ws)
@@ -282,12 +298,17 @@ def run_gpu(args):
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    # headline: whole decode steps (split + combine, launched back to back)
+    # headline: whole decode steps (split + combine, launched back to back).
+    # The host waits for the GPU every SYNC_EVERY steps, between two timed
+    # steps, so the launch queue never fills: a host thread blocked on a full
+    # queue can wake up late and leave the GPU idle inside a timed step.
     for i in range(K):
         flush()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
+        if (i + 1) % SYNC_EVERY == 0:
+            torch.cuda.synchronize()
     # roofline: the same steps again with events around the split kernel alone
     # (an event between the two launches stops the combine from overlapping
     # the split kernel's tail, so these steps are not used for the headline)
@@ -296,6 +317,8 @@ def run_gpu(args):
         fda.fd_set_split_events(*sev[i])
         step()
         fda.fd_set_split_events(None, None)
+        if (i + 1) % SYNC_EVERY == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
@@ -366,6 +389,8 @@ def run_gpu(args):
         "us_per_step": round(ms_per_step * 1e3, 2),
         "us_per_step_p10_p50_p90": [round(float(np.percentile(step_ms, q)) * 1e3, 2)
                                     for q in (10, 50, 90)],
+        "us_per_step_max": round(max(step_ms) * 1e3, 2),
+        "slow_steps": int(sum(1 for x in step_ms if x > 1.5 * float(np.median(step_ms)))),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3->f16 mma, f32 acc" if w.kv_dtype == "e4m3" else f"{w.kv_dtype} mma, f32 acc",
         "data": "synthetic",

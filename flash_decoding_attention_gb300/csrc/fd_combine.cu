@@ -27,10 +27,16 @@ __device__ __forceinline__ int seg_slot(int c0, int k) { return k == 0 ? 2 * c0 
 // the WPI warps of an item split its segments (segment k goes to part
 // k mod WPI), so that few long streams still spread their loads over many
 // warps, while many short ones run one warp per item in a single wave.
+// Every load that does not depend on another is issued before the first use:
+// after the plan words, the m/l pairs (one segment per lane) and the first
+// batch of accumulator rows travel together, so a stream with up to 8 * WPI
+// segments costs two dependent round trips to memory.
 template <typename QT, int D, int WPI>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Params p) {
   constexpr int DPL = D / 32;
   constexpr int IPC = kCombineWarps / WPI;          // items per CTA
+  constexpr int BATCH = 8;                          // accumulator rows in flight per lane
+  using VecT = typename std::conditional<DPL == 4, float4, float2>::type;
   __shared__ float red_m[kCombineWarps];
   __shared__ float red_l[kCombineWarps];
   __shared__ float red_a[kCombineWarps][D];
@@ -65,10 +71,26 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
       nseg = c0 == c1 ? 0 : c1 - c0 + 1;   // 0: the split kernel wrote the output
     }
   }
-  // max of m over this part's segments (lanes over segments)
-  float M = -INFINITY;
-  for (int k = part + WPI * lane; k < nseg; k += WPI * 32)
-    M = fmaxf(M, p.part_ml[(long long)seg_slot(c0, k) * p.hq + i].x);
+  // this part's segments: k_u = part + WPI * u, u < nu
+  const int nu = nseg > part ? (nseg - part + WPI - 1) / WPI : 0;
+  auto acc_row = [&](int u) -> const VecT* {
+    const long long slot = seg_slot(c0, part + WPI * u);
+    return reinterpret_cast<const VecT*>(p.part_acc + (slot * p.hq + i) * D + lane * DPL);
+  };
+  auto ml_of = [&](int u) -> float2 {
+    return p.part_ml[(long long)seg_slot(c0, part + WPI * u) * p.hq + i];
+  };
+  // round trip 1: m/l of the first 32 segments (lane u) + first accumulator batch
+  const float2 ml0 = lane < nu ? ml_of(lane) : make_float2(-INFINITY, 0.f);
+  VecT v[BATCH];
+#pragma unroll
+  for (int u = 0; u < BATCH; ++u) {
+    if (u < nu) v[u] = *acc_row(u);
+    else v[u] = VecT{};
+  }
+  // max over this part's segments (beyond 32 segments: extra passes)
+  float M = ml0.x;
+  for (int u = 32 + lane; u < nu; u += 32) M = fmaxf(M, ml_of(u).x);
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   if constexpr (WPI > 1) {
@@ -77,29 +99,44 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
 #pragma unroll
     for (int w = 0; w < WPI; ++w) M = fmaxf(M, red_m[slot_in_cta * WPI + w]);
   }
-  // weighted sums over this part's segments, several loads in flight
-  float L = 0.f, acc[DPL];
+  // weighted sums; lane u holds the weight of segment u of the current chunk
+  float f = ml0.x == -INFINITY ? 0.f : fast_exp2(ml0.x - M);
+  float L = ml0.y * f;
+  float acc[DPL];
 #pragma unroll
   for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
-#pragma unroll 8
-  for (int k = part; k < nseg; k += WPI) {
-    const long long slot = seg_slot(c0, k);
-    const float2 ml = p.part_ml[slot * p.hq + i];
-    const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-    L = fmaf(ml.y, f, L);
-    const float* a = p.part_acc + (slot * p.hq + i) * D + lane * DPL;
+  auto accumulate = [&](const VecT& x, float w) {
     if constexpr (DPL == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(a);
-      acc[0] = fmaf(v.x, f, acc[0]);
-      acc[1] = fmaf(v.y, f, acc[1]);
-      acc[2] = fmaf(v.z, f, acc[2]);
-      acc[3] = fmaf(v.w, f, acc[3]);
+      acc[0] = fmaf(x.x, w, acc[0]);
+      acc[1] = fmaf(x.y, w, acc[1]);
+      acc[2] = fmaf(x.z, w, acc[2]);
+      acc[3] = fmaf(x.w, w, acc[3]);
     } else {
-      const float2 v = *reinterpret_cast<const float2*>(a);
-      acc[0] = fmaf(v.x, f, acc[0]);
-      acc[1] = fmaf(v.y, f, acc[1]);
+      acc[0] = fmaf(x.x, w, acc[0]);
+      acc[1] = fmaf(x.y, w, acc[1]);
+    }
+  };
+#pragma unroll
+  for (int u = 0; u < BATCH; ++u) accumulate(v[u], __shfl_sync(0xffffffffu, f, u));
+  for (int c = 0; c < nu; c += 32) {
+    if (c > 0) {   // next chunk of 32 segments: its m/l and weights
+      const float2 ml = c + lane < nu ? ml_of(c + lane) : make_float2(-INFINITY, 0.f);
+      f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+      L = fmaf(ml.y, f, L);
+    }
+    const int cnt = min(32, nu - c);
+    for (int u0 = c == 0 ? BATCH : 0; u0 < cnt; u0 += BATCH) {
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        if (u0 + u < cnt) v[u] = *acc_row(c + u0 + u);
+        else v[u] = VecT{};
+      }
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) accumulate(v[u], __shfl_sync(0xffffffffu, f, (u0 + u) & 31));
     }
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   if constexpr (WPI > 1) {
     if (lane == 0) red_l[warp] = L;
 #pragma unroll
@@ -111,10 +148,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
     for (int w = 0; w < WPI; ++w) L += red_l[slot_in_cta * WPI + w];
 #pragma unroll
     for (int k = 0; k < DPL; ++k) {
-      float v = 0.f;
+      float x = 0.f;
 #pragma unroll
-      for (int w = 0; w < WPI; ++w) v += red_a[slot_in_cta * WPI + w][lane * DPL + k];
-      acc[k] = v;
+      for (int w = 0; w < WPI; ++w) x += red_a[slot_in_cta * WPI + w][lane * DPL + k];
+      acc[k] = x;
     }
   }
   if (nseg == 0) return;
