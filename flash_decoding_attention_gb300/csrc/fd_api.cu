@@ -13,7 +13,7 @@ namespace fd {
 bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv_dtype,
                   int paged, int page_size);
 void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms, int* hc,
-                int* tile, int* grid);
+                int* tile, int* grid, int* seg_units);
 
 namespace {
 
@@ -40,6 +40,7 @@ int current_sms() {
 struct Config {
   int kernel;   // FD_KERNEL_SIMT or FD_KERNEL_MMA
   int hc, hg, hq, tile, grid;
+  int seg_units;   // plan cost of a segment start, in tiles
 };
 
 constexpr int kSimtTile = 32;
@@ -60,7 +61,8 @@ bool choose(int pref, int num_q_heads, int num_kv_heads, int head_dim, int q_dty
   if (pref == FD_KERNEL_MMA || (pref == FD_KERNEL_AUTO && mma_ok)) {
     if (!mma_ok) return false;
     c->kernel = FD_KERNEL_MMA;
-    mma_config(group, num_kv_heads, head_dim, kv_dtype, sms, &c->hc, &c->tile, &c->grid);
+    mma_config(group, num_kv_heads, head_dim, kv_dtype, sms, &c->hc, &c->tile, &c->grid,
+               &c->seg_units);
     c->hg = num_kv_heads / c->hc;
     c->hq = c->hc * group;
     return true;
@@ -72,6 +74,7 @@ bool choose(int pref, int num_q_heads, int num_kv_heads, int head_dim, int q_dty
   c->hg = num_q_heads / c->hq;
   c->tile = kSimtTile;
   c->grid = sms * simt_ctas_per_sm();
+  c->seg_units = 0;
   return true;
 }
 
@@ -240,6 +243,7 @@ fd_status fd_decode_attention(const void* q, const void* k_cache, const void* v_
   p.hg = c.hg;
   p.hq = c.hq;
   p.tile = c.tile;
+  p.seg_units = c.seg_units;
   p.grid = c.grid;
   p.kernel = c.kernel;
   p.q_dtype = q_dtype;

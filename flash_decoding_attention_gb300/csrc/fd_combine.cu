@@ -1,8 +1,9 @@
 // fd_combine.cu -- log-sum-exp merge of the partial states of split streams.
 //
-// A stream that the split plan cut across CTAs c0 .. c1 left one partial
-// state (m_i in log2 units, l_i, acc_i[D]) per CTA: slot 2*c0+1 for the CTA
-// that holds its first tile, slot 2*c for every later CTA.  Merging is the
+// A stream that the split plan cut across CTAs c0 .. c1 (the CTAs holding its
+// first and last tile units) left one partial state (m_i in log2 units, l_i,
+// acc_i[D]) per CTA: slot 2*c0+1 for the CTA that holds its first tile, slot
+// 2*c for every later CTA.  Merging is the
 // rescale step of the online softmax ("SGLang Prefill optimisation:
 // dissecting FlashAttention kernel bottlenecks with GPU Trace", section 2.2)
 // applied to whole partial states:
@@ -66,8 +67,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
       }
     } else {
       const long long per_cta = (total + p.grid - 1) / p.grid;
-      c0 = (int)(P0 / per_cta);
-      const int c1 = (int)((P1 - 1) / per_cta);
+      c0 = (int)((P0 + p.seg_units) / per_cta);   // CTA holding tile 0
+      const int c1 = (int)((P1 - 1) / per_cta);     // CTA holding the last tile
       nseg = c0 == c1 ? 0 : c1 - c0 + 1;   // 0: the split kernel wrote the output
     }
   }

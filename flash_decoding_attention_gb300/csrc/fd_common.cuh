@@ -80,6 +80,7 @@ struct Params {
   int hq;           // query heads per work stream; stream j of a sequence
                     // serves query heads [j * hq, (j + 1) * hq)
   int tile;         // tokens per plan tile
+  int seg_units;    // plan cost of starting a segment, in tiles (see compute_plan)
   int grid;         // CTAs of the split kernel
   int kernel;       // fd_kernel of the split kernel
   int q_dtype, kv_dtype;   // fd_dtype
@@ -88,11 +89,16 @@ struct Params {
 };
 
 // ---------------------------------------------------------------------------
-// Split plan ("stream-K" over tiles).  A work stream is (sequence b, a run of
-// hq consecutive query heads and the KV heads they read); stream s = b * hg + j.  Stream s has n_s = ceil(T_b / tile)
-// tiles; the streams' tiles are concatenated in stream order and CTA c takes
-// global tiles [c * L, min(N, (c + 1) * L)) with N = sum n_s and
-// L = ceil(N / grid).  The piece of a stream inside one CTA is a segment.
+// Split plan ("stream-K", balanced on cost).  A work stream is (sequence b,
+// a run of hq consecutive query heads and the KV heads they read); stream
+// s = b * hg + j.  Stream s has n_s = ceil(T_b / tile) tiles and, when
+// n_s > 0, costs u_s = A + n_s plan units: A units for starting a segment
+// (reloading Q and the row data; A = seg_units) followed by one unit per
+// tile.  The streams' units are concatenated in stream order and CTA c takes
+// units [c * L, min(U, (c + 1) * L)) with U = sum u_s and L = ceil(U / grid),
+// so a CTA that starts more segments gets fewer tiles.  The tiles of stream
+// s inside one CTA's range form a segment; a range that holds only some of
+// a stream's A leading units holds no segment of it.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int stream_tokens(const Params& p, int s) {
   int t = __ldg(p.seq_len + s / p.hg);
@@ -103,11 +109,16 @@ __device__ __forceinline__ int stream_tiles(const Params& p, int s) {
   return (stream_tokens(p, s) + p.tile - 1) / p.tile;
 }
 
+__device__ __forceinline__ int stream_units(const Params& p, int s) {
+  const int n = stream_tiles(p, s);
+  return n > 0 ? n + p.seg_units : 0;
+}
+
 struct PlanResult {
-  long long total;      // N
+  long long total;      // U
   long long per_cta;    // L
-  int s_first;          // first stream with a tile in this CTA (or num_streams)
-  long long p_first;    // prefix of s_first
+  int s_first;          // stream holding this CTA's first unit (or num_streams)
+  long long p_first;    // prefix (in units) of s_first
 };
 
 // Block-wide; every thread gets the same result.  CTA 0 also writes the
@@ -117,9 +128,9 @@ __device__ inline PlanResult compute_plan(const Params& p, long long* red) {
   const int S = p.batch * p.hg;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
-  // pass 1: total tiles
+  // pass 1: total units
   long long acc = 0;
-  for (int s = tid; s < S; s += blockDim.x) acc += stream_tiles(p, s);
+  for (int s = tid; s < S; s += blockDim.x) acc += stream_units(p, s);
   for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) red[warp] = acc;
   __syncthreads();
@@ -136,7 +147,7 @@ __device__ inline PlanResult compute_plan(const Params& p, long long* red) {
   long long carry = 0;
   for (int base = 0; base < S; base += blockDim.x) {
     int s = base + tid;
-    long long v = s < S ? stream_tiles(p, s) : 0;
+    long long v = s < S ? stream_units(p, s) : 0;
     long long x = v;
     for (int o = 1; o < 32; o <<= 1) {
       long long y = __shfl_up_sync(0xffffffffu, x, o);
@@ -169,7 +180,7 @@ __device__ inline PlanResult compute_plan(const Params& p, long long* red) {
     p.ws->plan[4] = (int32_t)total;
     p.ws->plan[5] = (int32_t)r.per_cta;
     p.ws->plan[6] = p.kernel;
-    p.ws->plan[7] = 0;
+    p.ws->plan[7] = p.seg_units;
     if (total > 0x7fffffffLL) raise_error(p.ws, kErrPlan, total);
   }
   r.s_first = has_work ? (int)red[32] : S;
@@ -178,7 +189,7 @@ __device__ inline PlanResult compute_plan(const Params& p, long long* red) {
   return r;
 }
 
-// One segment: stream s, tokens [t_begin, t_end), global tiles [g_begin, g_end).
+// One segment: stream s, tokens [t_begin, t_end).
 struct Segment {
   int s;
   int t_begin, t_end;
@@ -190,9 +201,9 @@ struct Segment {
 // Iterates the segments of one CTA; every thread of a warp (or block) that
 // uses it sees the same sequence.
 struct SegmentIter {
-  long long g, g_end;   // next global tile, end of this CTA's range
-  int s;                // stream holding tile g
-  long long ps;         // prefix of s
+  long long g, g_end;   // next unit, end of this CTA's range
+  int s;                // stream holding unit g
+  long long ps;         // prefix (units) of s
   int S;
 
   __device__ void init(const Params& p, const PlanResult& r) {
@@ -205,26 +216,31 @@ struct SegmentIter {
   }
   // Returns false when the CTA has no more segments.
   __device__ bool next(const Params& p, Segment& seg) {
-    if (g >= g_end || s >= S) return false;
-    int ns = stream_tiles(p, s);
-    while (g >= ps + ns) {   // skip empty / finished streams
-      ps += ns;
-      ++s;
-      if (s >= S) return false;
-      ns = stream_tiles(p, s);
+    for (;;) {
+      if (g >= g_end || s >= S) return false;
+      int nu = stream_units(p, s);
+      while (g >= ps + nu) {   // skip empty / finished streams
+        ps += nu;
+        ++s;
+        if (s >= S) return false;
+        nu = stream_units(p, s);
+      }
+      const long long a = g, e = ps + nu < g_end ? ps + nu : g_end;
+      const long long tb = ps + p.seg_units;   // unit of tile 0
+      g = e;
+      if (e <= tb) continue;                   // only leading units of s: no segment
+      seg.s = s;
+      seg.T = stream_tokens(p, s);
+      const long long first = a > tb ? a - tb : 0;
+      seg.t_begin = (int)(first * p.tile);
+      const long long te = (e - tb) * p.tile;
+      seg.t_end = te < seg.T ? (int)te : seg.T;
+      const bool starts_mid = a > tb;
+      const bool ends_mid = e < ps + nu;
+      seg.complete = !starts_mid && !ends_mid;
+      seg.slot = 2 * (int)blockIdx.x + (starts_mid ? 0 : 1);
+      return true;
     }
-    long long a = g, e = ps + ns < g_end ? ps + ns : g_end;
-    seg.s = s;
-    seg.T = stream_tokens(p, s);
-    seg.t_begin = (int)((a - ps) * p.tile);
-    long long te = (e - ps) * p.tile;
-    seg.t_end = te < seg.T ? (int)te : seg.T;
-    bool starts_mid = a > ps;
-    bool ends_mid = e < ps + ns;
-    seg.complete = !starts_mid && !ends_mid;
-    seg.slot = 2 * (int)blockIdx.x + (starts_mid ? 0 : 1);
-    g = e;
-    return true;
   }
 };
 

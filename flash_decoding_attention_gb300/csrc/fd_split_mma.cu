@@ -891,12 +891,17 @@ bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv
   return true;
 }
 
+// A segment start costs the consumers a Q reload and the producer a row-data
+// load, each a DRAM round trip under full load: about what streaming
+// 128 KB takes per SM.  The plan charges it in tiles of this shape.
 void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms, int* hc,
-                int* tile, int* grid) {
+                int* tile, int* grid, int* seg_units) {
   const Shape s = make_shape(group, num_kv_heads, head_dim, kv_dtype, 0);
   *hc = s.hc;
   *tile = s.tile;
   *grid = sms;
+  const int stage = 2 * s.kv_bytes;
+  *seg_units = (131072 + stage - 1) / stage;
 }
 
 cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {

@@ -197,9 +197,12 @@ fd_status fd_set_split_events(fd_event_t before, fd_event_t after);
  * Test hook: copies the split plan of the last fd_decode_attention call that
  * used this workspace into host memory (synchronises `stream`).
  * plan[0..7] = {num_streams, streams_per_sequence, tile_tokens, grid,
- * total_tiles, tiles_per_cta, kernel, 0}; stream j of sequence b serves
- * query heads [j * h, (j + 1) * h) with h = num_q_heads / streams_per_sequence;
- * plan[8 .. 8 + num_streams] = exclusive prefix of tiles per stream
+ * total_units, units_per_cta, kernel, start_units}; stream j of sequence b
+ * serves query heads [j * h, (j + 1) * h) with h = num_q_heads /
+ * streams_per_sequence.  A stream with n > 0 tiles costs start_units + n
+ * plan units (the start cost first), an empty stream none; CTA c takes units
+ * [c * units_per_cta, (c + 1) * units_per_cta).
+ * plan[8 .. 8 + num_streams] = exclusive prefix of units per stream
  * (num_streams + 1 values).  capacity = number of int32 that fit in plan.
  */
 fd_status fd_debug_read_plan(const void *workspace, fd_stream_t stream, int32_t *plan,

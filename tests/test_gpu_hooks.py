@@ -39,14 +39,15 @@ def test_device_plan_matches_restatement(kernel, case):
     ws = fda.alloc_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim)
     run(w, kernel, workspace=ws)
     head, prefix = fda.fd_debug_read_plan(ws)
-    S, hg, tile, grid, total, per_cta, k, _ = head
+    S, hg, tile, grid, total, per_cta, k, seg_units = head
     assert k == kernel
     assert hg >= 1 and w.num_q_heads % hg == 0
     hq = w.num_q_heads // hg
     group = w.num_q_heads // w.num_kv_heads
     assert hq % group == 0 or group % hq == 0      # a stream never splits a KV head's reads
     assert S == w.batch * hg
-    p_prefix, p_total, p_per_cta, _ = plan_ref.plan(w.seq_len, hg, tile, grid)
+    assert seg_units >= 0 and (kernel == 2 or seg_units == 0)
+    p_prefix, p_total, p_per_cta, _ = plan_ref.plan(w.seq_len, hg, tile, grid, seg_units)
     assert prefix == p_prefix
     assert (total, per_cta) == (p_total, p_per_cta)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
