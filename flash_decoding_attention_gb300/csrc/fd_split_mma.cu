@@ -160,13 +160,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint64_t* bar) {
+// TMA 3-D tile load into shared memory, completing on an mbarrier, with an
+// L2 cache policy (createpolicy) for the copied lines.
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int c0, int c1,
+                                                 int c2, uint64_t* bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+      "l"(policy)
       : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
+__device__ __forceinline__ void prefetch_l2_keep(const void* a) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(a));
+}
+
+// Start-up, before the plan: pulls the index array the producer reads right
+// after the plan (the block table, or kv_start) into L2, a slice per CTA.
+// Tables above 4 MB are left to the producer's own loads.
+__device__ __forceinline__ void prefetch_index_arrays(const Params& p) {
+  const char* a = p.block_table ? reinterpret_cast<const char*>(p.block_table)
+                                : reinterpret_cast<const char*>(p.kv_start);
+  const size_t bytes = p.block_table ? (size_t)p.batch * (size_t)p.bt_stride * 4u
+                                     : (size_t)p.batch * 4u;
+  if (bytes > ((size_t)4 << 20)) return;
+  const size_t lines = (bytes + 127) / 128;
+  for (size_t l = (size_t)blockIdx.x * blockDim.x + threadIdx.x; l < lines;
+       l += (size_t)gridDim.x * blockDim.x)
+    prefetch_l2(a + l * 128);
 }
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
@@ -294,6 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // work that does not need the plan: the tensor-map descriptors and the
+  // index array the producer reads first
+  if (threadIdx.x == kConsumerWarps * 32) {
+    prefetch_map(&tmk);
+    prefetch_map(&tmv);
+  }
+  prefetch_index_arrays(p);
   const PlanResult plan = compute_plan(p, sm.red);   // contains __syncthreads
   allow_dependent_launch();
 
@@ -303,10 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp walks the CTA's tiles; it stages block-table entries in
     // shared memory with one parallel load per window, and lane 0 issues the
     // TMA copies of each tile as soon as its stage is free.
-    if (lane == 0) {
-      prefetch_map(&tmk);
-      prefetch_map(&tmv);
-    }
+    // K/V lines are read once: they leave L2 first, before Q rows, index
+    // data and partial states
+    uint64_t kv_policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(kv_policy));
     SegmentIter it;
     it.init(p, plan);
     Segment seg;
@@ -381,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   for (int x = 0; x < sh.nx; ++x) {
                     const size_t off = (size_t)x * sh.hc * sh.region_bytes;
                     const int xc = x * (sh.row_bytes / ELEM);
-                    tma_load_3d(kst + off, &tmk, xc, (int)row, kvh0, &sm.full[stg]);
-                    tma_load_3d(vst + off, &tmv, xc, (int)row, kvh0, &sm.full[stg]);
+                    tma_load_3d_hint(kst + off, &tmk, xc, (int)row, kvh0, &sm.full[stg], kv_policy);
+                    tma_load_3d_hint(vst + off, &tmv, xc, (int)row, kvh0, &sm.full[stg], kv_policy);
                   }
                   continue;
                 }
@@ -391,8 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const size_t off = (size_t)(x * sh.hc + h) * sh.region_bytes +
                                        (size_t)i * sh.box_rows * sh.row_bytes;
                     const int xc = x * (sh.row_bytes / ELEM);
-                    tma_load_3d(kst + off, &tmk, xc, kvh0 + h, (int)row, &sm.full[stg]);
-                    tma_load_3d(vst + off, &tmv, xc, kvh0 + h, (int)row, &sm.full[stg]);
+                    tma_load_3d_hint(kst + off, &tmk, xc, kvh0 + h, (int)row, &sm.full[stg],
+                                     kv_policy);
+                    tma_load_3d_hint(vst + off, &tmv, xc, kvh0 + h, (int)row, &sm.full[stg],
+                                     kv_policy);
                   }
                 }
               }
@@ -424,6 +459,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     SegmentIter it;
     it.init(p, plan);
+    {
+      // the Q rows of this head tile for the CTA's later segments, into L2
+      // (kept there): a segment start then waits for L2, not for DRAM
+      SegmentIter ahead = it;
+      Segment sa;
+      const int row = lane >> 1, lh = mtile * 16 + row;
+      for (int k = 0; k < 8 && ahead.next(p, sa); ++k) {
+        if (k == 0 || lh >= G) continue;   // the first segment's Q is loaded next
+        const int bs = sa.s / p.hg;
+        const long long qr = (long long)bs * p.num_q_heads + (long long)(sa.s - bs * p.hg) * p.hq +
+                             kvl * G + lh;
+        prefetch_l2_keep(qg + qr * D + (lane & 1) * (D / 2));
+      }
+    }
     Segment seg;
     long long n = 0;
     while (it.next(p, seg)) {
