@@ -280,6 +280,19 @@ __device__ __forceinline__ uint32_t chunk_addr(uint32_t region, int tt, int c, i
   return region + tt * row_bytes + ((c ^ swz) << 4);
 }
 
+// V rows of tokens past a segment's end are whatever the stage held (a
+// skipped box, a page tail, a gap between sequences): they may hold NaN or
+// Inf bit patterns, and 0 * NaN would poison the accumulator, so their words
+// are zeroed before the P V product.  w0..w3 are the rows of sub-tile tokens
+// tk, tk + 1, tk + 8, tk + 9; `left` tokens of the sub-tile are valid.
+template <typename W>
+__device__ __forceinline__ void zero_rows_past_end(W& w0, W& w1, W& w2, W& w3, int tk, int left) {
+  if (tk >= left) w0 = W{};
+  if (tk + 1 >= left) w1 = W{};
+  if (tk + 8 >= left) w2 = W{};
+  if (tk + 9 >= left) w3 = W{};
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -633,10 +646,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t pa3 = pack_f32x2(pr[2 * kt + 1][2], pr[2 * kt + 1][3], BF16);
               const int u0 = sub + 16 * kt + 2 * q, u1 = u0 + 1, u2 = u0 + 8, u3 = u0 + 9;
               if constexpr (ELEM == 1 && D == 128) {
-                const uint4 w0 = lds128(chunk_addr(vreg, u0, r, sh.row_bytes));
-                const uint4 w1 = lds128(chunk_addr(vreg, u1, r, sh.row_bytes));
-                const uint4 w2 = lds128(chunk_addr(vreg, u2, r, sh.row_bytes));
-                const uint4 w3 = lds128(chunk_addr(vreg, u3, r, sh.row_bytes));
+                uint4 w0 = lds128(chunk_addr(vreg, u0, r, sh.row_bytes));
+                uint4 w1 = lds128(chunk_addr(vreg, u1, r, sh.row_bytes));
+                uint4 w2 = lds128(chunk_addr(vreg, u2, r, sh.row_bytes));
+                uint4 w3 = lds128(chunk_addr(vreg, u3, r, sh.row_bytes));
+                if (left < SUB) zero_rows_past_end(w0, w1, w2, w3, 16 * kt + 2 * q, left);
                 const uint32_t A[4] = {w0.x, w0.y, w0.z, w0.w}, B[4] = {w1.x, w1.y, w1.z, w1.w};
                 const uint32_t C[4] = {w2.x, w2.y, w2.z, w2.w}, E[4] = {w3.x, w3.y, w3.z, w3.w};
 #pragma unroll
@@ -656,10 +670,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               } else if constexpr (ELEM == 1) {   // D == 64: 8 bytes per token
                 const int c = r >> 1, half = (r & 1) * 8;
-                const uint2 w0 = lds64(chunk_addr(vreg, u0, c, sh.row_bytes) + half);
-                const uint2 w1 = lds64(chunk_addr(vreg, u1, c, sh.row_bytes) + half);
-                const uint2 w2 = lds64(chunk_addr(vreg, u2, c, sh.row_bytes) + half);
-                const uint2 w3 = lds64(chunk_addr(vreg, u3, c, sh.row_bytes) + half);
+                uint2 w0 = lds64(chunk_addr(vreg, u0, c, sh.row_bytes) + half);
+                uint2 w1 = lds64(chunk_addr(vreg, u1, c, sh.row_bytes) + half);
+                uint2 w2 = lds64(chunk_addr(vreg, u2, c, sh.row_bytes) + half);
+                uint2 w3 = lds64(chunk_addr(vreg, u3, c, sh.row_bytes) + half);
+                if (left < SUB) zero_rows_past_end(w0, w1, w2, w3, 16 * kt + 2 * q, left);
                 const uint32_t A[2] = {w0.x, w0.y}, B[2] = {w1.x, w1.y};
                 const uint32_t C[2] = {w2.x, w2.y}, E[2] = {w3.x, w3.y};
 #pragma unroll
@@ -681,10 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int x2 = 0; x2 < D / 64; ++x2) {
                   const uint32_t reg = vreg + x2 * xstride;
-                  const uint4 w0 = lds128(chunk_addr(reg, u0, r, sh.row_bytes));
-                  const uint4 w1 = lds128(chunk_addr(reg, u1, r, sh.row_bytes));
-                  const uint4 w2 = lds128(chunk_addr(reg, u2, r, sh.row_bytes));
-                  const uint4 w3 = lds128(chunk_addr(reg, u3, r, sh.row_bytes));
+                  uint4 w0 = lds128(chunk_addr(reg, u0, r, sh.row_bytes));
+                  uint4 w1 = lds128(chunk_addr(reg, u1, r, sh.row_bytes));
+                  uint4 w2 = lds128(chunk_addr(reg, u2, r, sh.row_bytes));
+                  uint4 w3 = lds128(chunk_addr(reg, u3, r, sh.row_bytes));
+                  if (left < SUB) zero_rows_past_end(w0, w1, w2, w3, 16 * kt + 2 * q, left);
                   const uint32_t A[4] = {w0.x, w0.y, w0.z, w0.w}, B[4] = {w1.x, w1.y, w1.z, w1.w};
                   const uint32_t C[4] = {w2.x, w2.y, w2.z, w2.w}, E[4] = {w3.x, w3.y, w3.z, w3.w};
 #pragma unroll

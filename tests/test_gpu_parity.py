@@ -70,6 +70,46 @@ def test_edge_lengths_with_poisoned_gaps(q_dtype, kv_dtype, D):
     check_workload(w)
 
 
+NAN_BITS = {"e4m3": 0x7F, "f16": 0x7E00, "bf16": 0x7FC0}
+
+
+def _fill_unowned_rows_with_nan(w):
+    """Every cache row no sequence owns (gaps between sequences, page tails,
+    unused pages) gets a NaN bit pattern; the oracle never reads them."""
+    nan = NAN_BITS[w.kv_dtype]
+    k, v = w.k_cache.copy(), w.v_cache.copy()
+    if w.paged:
+        owned = np.zeros(k.shape[:2], dtype=bool)       # [pages, page_size]
+        for b in range(w.batch):
+            T = int(w.seq_len[b])
+            for j in range(-(-T // w.page_size)):
+                owned[w.block_table[b, j], : min(w.page_size, T - j * w.page_size)] = True
+    else:
+        owned = np.zeros(k.shape[0], dtype=bool)
+        for b in range(w.batch):
+            s = int(w.kv_start_idx[b])
+            owned[s:s + int(w.seq_len[b])] = True
+    k[~owned] = nan
+    v[~owned] = nan
+    import dataclasses
+    return dataclasses.replace(w, k_cache=k, v_cache=v)
+
+
+@pytest.mark.parametrize("kv_dtype,P", [("e4m3", 0), ("e4m3", 16), ("e4m3", 64), ("f16", 0),
+                                        ("f16", 16), ("bf16", 32)])
+@pytest.mark.parametrize("qh,kvh", [(16, 2), (8, 8), (16, 1)])
+def test_nan_in_rows_outside_sequences_never_leaks(kv_dtype, P, qh, kvh):
+    """Rows past a sequence's end are loaded with its last tile (box rows,
+    page tails): whatever bytes they hold must not reach the outputs."""
+    q_dtype = "bf16" if kv_dtype == "bf16" else "f16"
+    w = fw.make_contiguous(f"nan-{kv_dtype}-{P}-{qh}-{kvh}", 41, [100, 37, 300, 1, 0, 129], qh, kvh,
+                           128, q_dtype, kv_dtype, gap=5, lead=3, tail=9)
+    if P:
+        w = fw.to_paged(w, P, 42)
+    w = _fill_unowned_rows_with_nan(w)
+    check_workload(w)
+
+
 @pytest.mark.parametrize("qh,kvh", [(8, 8), (8, 4), (16, 4), (32, 4), (64, 8), (16, 1), (32, 1),
                                     (64, 1), (128, 1), (12, 3), (40, 5)])
 def test_head_groupings(qh, kvh):
