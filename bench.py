@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--shared-prefix", type=int, default=0,
+                    help="paged workloads: every sequence's first pages alias those of "
+                         "sequence 0 up to this many tokens (prefix-cache hits)")
     return ap.parse_args()
 
 
@@ -105,11 +108,27 @@ def oracle_sample(w: fw.Workload, budget_s: float):
     return gbs, threads, desc, elapsed
 
 
+def make_workload(args) -> fw.Workload:
+    w = fw.CONFIGS[args.config]()
+    if args.shared_prefix:
+        if not w.paged:
+            raise SystemExit("--shared-prefix needs a paged workload")
+        w = fw.share_prefix(w, args.shared_prefix)
+    return w
+
+
+def workload_config(args) -> dict:
+    c = {"workload": fw.CONFIG_NAMES[args.config]}
+    if args.shared_prefix:
+        c["shared_prefix_tokens"] = args.shared_prefix
+    return c
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = fw.CONFIGS[args.config]()
+    w = make_workload(args)
     per_step = []
     gbs_all = []
     threads = 0
@@ -125,7 +144,7 @@ def run_reference(args):
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * statistics.median(per_step), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": fw.CONFIG_NAMES[args.config]},
+        "data": "synthetic", "config": workload_config(args),
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": "per step: " + desc},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -251,7 +270,7 @@ def run_gpu(args):
     fda.load_library()
     fda.fd_set_kernel({"auto": 0, "simt": 1, "mma": 2}[args.kernel])
 
-    w = fw.CONFIGS[args.config]()
+    w = make_workload(args)
     t = fw.to_torch(w, dev)
     B, QH, KVH, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
     out = torch.empty_like(t["q"])
@@ -394,7 +413,7 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3->f16 mma, f32 acc" if w.kv_dtype == "e4m3" else f"{w.kv_dtype} mma, f32 acc",
         "data": "synthetic",
-        "config": {"workload": fw.CONFIG_NAMES[args.config], "kernel": kname,
+        "config": {**workload_config(args), "kernel": kname,
                    "algorithmic_bytes_per_step": alg, "sum_seq_len": int(w.seq_len.sum()),
                    "l2": "flushed between steps (write then read of 2x L2 buffers, outside the "
                          "timed events)",
@@ -402,7 +421,7 @@ def run_gpu(args):
         "gpu_launches": 4 * K,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(kname, args.config),
+                     "traffic": None if args.shared_prefix else recorded_traffic(kname, args.config),
                      "kernel": f"split ({kname})", "split_us": round(split_avg * 1e3, 2)},
         "e2e": e2e,
         "clocks": clk,

@@ -232,6 +232,23 @@ def to_paged(w: Workload, page_size: int, seed: int, oversize: float = 1.2,
                                page_size=P, kv_start_idx=None, block_table=table)
 
 
+def share_prefix(w: Workload, shared_tokens: int) -> Workload:
+    """Prefix-cache hit pattern on a paged workload: every sequence's first
+    pages alias the physical pages of sequence 0 (the block tables point at
+    the same pool pages; nothing is copied), as a serving system does when
+    requests share a system prompt or a long context.  Only whole pages that
+    both sequences fill are aliased, up to ``shared_tokens`` tokens; the
+    pages a sequence gives up stay in the pool unused."""
+    assert w.paged
+    P = w.page_size
+    table = w.block_table.copy()
+    T0 = int(w.seq_len[0])
+    for b in range(1, w.batch):
+        k = min(int(shared_tokens) // P, T0 // P, int(w.seq_len[b]) // P)
+        table[b, :k] = table[0, :k]
+    return dataclasses.replace(w, name=w.name + f"-shared{int(shared_tokens)}", block_table=table)
+
+
 # ----------------------------------------------------------------------------
 # the five decode workloads
 # ----------------------------------------------------------------------------

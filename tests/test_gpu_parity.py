@@ -110,6 +110,17 @@ def test_nan_in_rows_outside_sequences_never_leaks(kv_dtype, P, qh, kvh):
     check_workload(w)
 
 
+@pytest.mark.parametrize("P,shared", [(16, 256), (64, 1024), (64, 5000)])
+def test_shared_prefix_pages(P, shared):
+    """Block tables whose first entries alias the same physical pages
+    (prefix-cache hits): read through the table like any other page."""
+    base = fw.make_contiguous(f"prefix-{P}-{shared}", 51, [3000, 2048, 1500, 900, 64, 4500, 17, 0],
+                              64, 8, 128, "f16", "e4m3", gap=2)
+    w = fw.share_prefix(fw.to_paged(base, P, 52), shared)
+    assert (w.block_table[1, :4] == w.block_table[0, :4]).all()
+    check_workload(w)
+
+
 @pytest.mark.parametrize("qh,kvh", [(8, 8), (8, 4), (16, 4), (32, 4), (64, 8), (16, 1), (32, 1),
                                     (64, 1), (128, 1), (12, 3), (40, 5)])
 def test_head_groupings(qh, kvh):
