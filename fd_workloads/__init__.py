@@ -34,6 +34,8 @@ E4M3_MAX = 448.0
 # sequences, unused pages, page tails).  A kernel that reads such a row
 # produces a grossly wrong score or output, so parity fails loudly.
 POISON_E4M3 = 0x7E          # +448
+
+SCALE_TENSOR, SCALE_HEAD, SCALE_TOKEN = 0, 1, 2
 POISON_F16 = 30000.0
 
 
@@ -56,6 +58,11 @@ class Workload:
     page_size: int = 0        # 0 = contiguous layout
     kv_start_idx: Optional[np.ndarray] = None   # int32 [B] (contiguous)
     block_table: Optional[np.ndarray] = None    # int32 [B, stride] (paged)
+    # finer K/V scales on top of k_scale / v_scale: 0 none, 1 per KV head
+    # (float32 [KVH]), 2 per token and KV head (float32 [kv_rows, KVH], by cache row)
+    scale_kind: int = 0
+    k_scales: Optional[np.ndarray] = None
+    v_scales: Optional[np.ndarray] = None
 
     @property
     def paged(self) -> bool:
@@ -88,6 +95,10 @@ class Workload:
             idx = 4 * B + 4 * pages
         else:
             idx = 8 * B
+        if self.scale_kind == SCALE_HEAD:
+            idx += 2 * 4 * KVH
+        elif self.scale_kind == SCALE_TOKEN:
+            idx += 2 * 4 * total * KVH
         return kv + qo + idx
 
 
@@ -232,6 +243,26 @@ def to_paged(w: Workload, page_size: int, seed: int, oversize: float = 1.2,
                                page_size=P, kv_start_idx=None, block_table=table)
 
 
+def with_scales(w: Workload, kind: int, seed: int, powers_of_two: bool = False) -> Workload:
+    """Adds per-KV-head (kind 1) or per-token (kind 2) K/V scales to an e4m3
+    workload.  They multiply k_scale / v_scale; seeded draws from [0.5, 2),
+    or from {1/4, 1/2, 1, 2, 4} with ``powers_of_two`` (products stay exact)."""
+    assert w.kv_dtype == "e4m3" and kind in (SCALE_HEAD, SCALE_TOKEN)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shape = (w.num_kv_heads,) if kind == SCALE_HEAD else (w.kv_rows, w.num_kv_heads)
+
+    def draw():
+        if powers_of_two:
+            return np.exp2(rng.integers(-2, 3, size=shape)).astype(np.float32)
+        return rng.uniform(0.5, 2.0, size=shape).astype(np.float32)
+
+    ks = draw()
+    vs = draw()
+    tag = "head" if kind == SCALE_HEAD else "token"
+    return dataclasses.replace(w, name=w.name + f"-{tag}scales", scale_kind=kind, k_scales=ks,
+                               v_scales=vs)
+
+
 def share_prefix(w: Workload, shared_tokens: int) -> Workload:
     """Prefix-cache hit pattern on a paged workload: every sequence's first
     pages alias the physical pages of sequence 0 (the block tables point at
@@ -349,4 +380,6 @@ def to_torch(w: Workload, device="cuda", pin: bool = False) -> dict:
     else:
         out["kv_start_idx"] = mk(w.kv_start_idx)
         out["block_table"] = None
+    out["k_scales"] = mk(w.k_scales) if w.scale_kind else None
+    out["v_scales"] = mk(w.v_scales) if w.scale_kind else None
     return out

@@ -72,6 +72,7 @@ class Oracle:
             vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_double, ctypes.c_double, ctypes.c_double,
+            ctypes.c_int, vp, vp,
             vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp]
         self.lib = lib
         self.path = lib_path
@@ -89,10 +90,14 @@ class Oracle:
                              num_q_heads, num_kv_heads, head_dim, softmax_scale, k_scale,
                              v_scale, kv_start_idx=None, block_table=None, page_size=0,
                              kv_rows=None, pairs: Optional[Sequence[Tuple[int, int]]] = None,
-                             nthreads: int = 0, want_weights: bool = False):
+                             nthreads: int = 0, want_weights: bool = False, scale_kind: int = 0,
+                             k_scales=None, v_scales=None):
         """Oracle on raw arrays.  Returns (out [B,QH,D] f64, lse [B,QH] f64,
         weights [B,QH,maxT] or None, threads used).  With ``pairs`` only those
-        (b, qh) rows are computed; the rest of ``out``/``lse`` stays NaN."""
+        (b, qh) rows are computed; the rest of ``out``/``lse`` stays NaN.
+        ``scale_kind`` 1 (per KV head, arrays [KVH]) or 2 (per token, arrays
+        [kv_rows, KVH]) multiplies K and V elements by ``k_scales`` and
+        ``v_scales`` on top of ``k_scale`` and ``v_scale``."""
         q = np.ascontiguousarray(q)
         k_cache = np.ascontiguousarray(k_cache)
         v_cache = np.ascontiguousarray(v_cache)
@@ -119,12 +124,18 @@ class Oracle:
         if pairs is not None:
             pairs_arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
             n_pairs = int(pairs_arr.shape[0])
+        if scale_kind:
+            k_scales = np.ascontiguousarray(k_scales, dtype=np.float32)
+            v_scales = np.ascontiguousarray(v_scales, dtype=np.float32)
+        else:
+            k_scales = v_scales = None
         used = ctypes.c_int(0)
         rc = self.lib.fdo_decode_attention(
             _ptr(q), _DTYPES[q_dtype], _ptr(k_cache), _ptr(v_cache), _DTYPES[kv_dtype],
             _ptr(kv_start_idx), _ptr(block_table), bt_stride, _ptr(seq_len), int(kv_rows),
             B, int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size),
             float(softmax_scale), float(k_scale), float(v_scale),
+            int(scale_kind), _ptr(k_scales), _ptr(v_scales),
             _ptr(pairs_arr), n_pairs, int(nthreads), _ptr(out), _ptr(lse), _ptr(weights),
             wstride, ctypes.addressof(used))
         if rc != 0:
@@ -138,7 +149,9 @@ class Oracle:
             w.q, w.q_dtype, w.k_cache, w.v_cache, w.kv_dtype, w.seq_len, w.num_q_heads,
             w.num_kv_heads, w.head_dim, w.softmax_scale, w.k_scale, w.v_scale,
             kv_start_idx=w.kv_start_idx, block_table=w.block_table, page_size=w.page_size,
-            kv_rows=w.kv_rows, pairs=pairs, nthreads=nthreads, want_weights=want_weights)
+            kv_rows=w.kv_rows, pairs=pairs, nthreads=nthreads, want_weights=want_weights,
+            scale_kind=getattr(w, "scale_kind", 0), k_scales=getattr(w, "k_scales", None),
+            v_scales=getattr(w, "v_scales", None))
         if want_weights:
             return out, lse, weights
         return out, lse

@@ -15,8 +15,11 @@
  *                                                        heads share a KV head)
  *   row(t)   = kv_start_idx[b] + t                       (contiguous cache)
  *            = block_table[b][t / P] * P + t % P         (paged cache)
- *   k_t[d]   = k_scale * dec(K[row(t)][kvh][d])
- *   v_t[d]   = v_scale * dec(V[row(t)][kvh][d])
+ *   k_t[d]   = k_scale * ks(t) * dec(K[row(t)][kvh][d])
+ *   v_t[d]   = v_scale * vs(t) * dec(V[row(t)][kvh][d])
+ *   ks(t), vs(t) = 1                                     (per-tensor scales only)
+ *            = k_scales[kvh], v_scales[kvh]              (per KV head)
+ *            = k_scales[row(t) * KVH + kvh], v_scales[..] (per token and KV head)
  *   s_t      = softmax_scale * sum_d q[b][qh][d] * k_t[d]
  *   M        = max_t s_t,  w_t = exp(s_t - M),  Z = sum_t w_t
  *   out[d]   = sum_t (w_t / Z) * v_t[d]
@@ -36,9 +39,9 @@
  *    (page * page_size + offset) rows into a [page, offset, head, dim] pool);
  *  - GQA grouping (group = QH / KVH query heads per KV head): same chapter,
  *    section 15.12;
- *  - per-tensor FP8 scales: the decoded code times a fp32 scale, the KV
- *    quantisation of section 15.11 of the same chapter with one scale per
- *    tensor.
+ *  - FP8 scales: the decoded code times a fp32 scale, the KV quantisation of
+ *    section 15.11 of the same chapter, which names the scale granularity
+ *    (one per tensor, per head or per token) as part of the method.
  *
  * Readings where the pages are silent: the contiguous cache is token-major
  * [rows, KVH, D] with kv_start_idx in rows; LSE is in natural log of the
@@ -57,6 +60,7 @@
 #endif
 
 enum { FDO_F16 = 0, FDO_BF16 = 1, FDO_E4M3 = 2 };
+enum { FDO_SCALE_TENSOR = 0, FDO_SCALE_HEAD = 1, FDO_SCALE_TOKEN = 2 };
 
 enum {
   FDO_OK = 0,
@@ -128,6 +132,13 @@ static int64_t cache_row(const int32_t *kv_start_idx, const int32_t *block_table
   return row;
 }
 
+/* The finer scale of a K or V element: 1, per KV head, or per (row, KV head). */
+static double scale_at(int kind, const float *arr, int64_t row, int num_kv_heads, int kvh) {
+  if (kind == FDO_SCALE_HEAD) return (double)arr[kvh];
+  if (kind == FDO_SCALE_TOKEN) return (double)arr[(size_t)row * num_kv_heads + kvh];
+  return 1.0;
+}
+
 /*
  * Computes out[B][QH][D] and lse[B][QH] in fp64.
  *
@@ -135,6 +146,9 @@ static int64_t cache_row(const int32_t *kv_start_idx, const int32_t *block_table
  * k_cache, v_cache: [rows][KVH][D] (contiguous) or [pages][P][KVH][D] (paged)
  *   elements of kv_dtype; kv_rows = number of token rows they hold.
  * Exactly one of kv_start_idx / block_table is non-NULL.
+ * scale_kind: FDO_SCALE_TENSOR (k_scales, v_scales unused), FDO_SCALE_HEAD
+ *   (k_scales, v_scales: [KVH]) or FDO_SCALE_TOKEN ([kv_rows][KVH], indexed by
+ *   cache row like the caches); they multiply k_scale, v_scale.
  * pairs: NULL for every (b, qh), else n_pairs entries of (b, qh) to compute;
  *   the other outputs are left untouched.
  * weights: NULL, or [B][QH][weights_stride] receiving w_t / Z.
@@ -145,6 +159,7 @@ int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const 
                          int block_table_stride, const int32_t *seq_len, int64_t kv_rows,
                          int batch, int num_q_heads, int num_kv_heads, int head_dim,
                          int page_size, double softmax_scale, double k_scale, double v_scale,
+                         int scale_kind, const float *k_scales, const float *v_scales,
                          const int32_t *pairs, int n_pairs, int nthreads, double *out,
                          double *lse, double *weights, int weights_stride, int *threads_used) {
   if (!q || !k_cache || !v_cache || !seq_len || !out || !lse) return FDO_BAD_ARG;
@@ -154,6 +169,8 @@ int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const 
   if (block_table && page_size <= 0) return FDO_BAD_ARG;
   if (q_dtype != FDO_F16 && q_dtype != FDO_BF16) return FDO_BAD_ARG;
   if (kv_dtype != FDO_F16 && kv_dtype != FDO_BF16 && kv_dtype != FDO_E4M3) return FDO_BAD_ARG;
+  if (scale_kind < FDO_SCALE_TENSOR || scale_kind > FDO_SCALE_TOKEN) return FDO_BAD_ARG;
+  if (scale_kind != FDO_SCALE_TENSOR && (!k_scales || !v_scales)) return FDO_BAD_ARG;
 
   const int group = num_q_heads / num_kv_heads;
   const int n_work = pairs ? n_pairs : batch * num_q_heads;
@@ -200,16 +217,17 @@ int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const 
     for (int d = 0; d < head_dim; ++d)
       qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + d);
 
-    /* scores s_t = softmax_scale * q . (k_scale * dec(k_t)) */
+    /* scores s_t = softmax_scale * q . (k_scale * ks(t) * dec(k_t)) */
     for (int t = 0; t < T && !bad; ++t) {
       rows[t] = cache_row(kv_start_idx, block_table, block_table_stride, page_size, b, t, kv_rows);
       if (rows[t] < 0) { bad = FDO_ROW_OUT_OF_RANGE; break; }
       size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;
+      const double ks = k_scale * scale_at(scale_kind, k_scales, rows[t], num_kv_heads, kvh);
       double dot = 0.0;
       for (int d = 0; d < head_dim; ++d) {
         double kd = decode_elem(k_cache, kv_dtype, base + d);
         if (isnan(kd)) { bad = FDO_NAN_CODE; break; }
-        dot += qv[d] * (k_scale * kd);
+        dot += qv[d] * (ks * kd);
       }
       s[t] = softmax_scale * dot;
     }
@@ -224,10 +242,11 @@ int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const 
         double wt = s[t] / Z;
         if (weights) weights[((size_t)b * num_q_heads + qh) * weights_stride + t] = wt;
         size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;
+        const double vs = v_scale * scale_at(scale_kind, v_scales, rows[t], num_kv_heads, kvh);
         for (int d = 0; d < head_dim; ++d) {
           double vd = decode_elem(v_cache, kv_dtype, base + d);
           if (isnan(vd)) { bad = FDO_NAN_CODE; break; }
-          o[d] += wt * (v_scale * vd);
+          o[d] += wt * (vs * vd);
         }
       }
       *l = M + log(Z);

@@ -392,9 +392,81 @@ def pin_online_recurrence(orc):
         _close(lse[fin], ref_lse[fin], 1e-12, 1e-13, f"online lse {w.name}")
 
 
+def materialize_scales(w: fw.Workload) -> fw.Workload:
+    """The same attention with the finer scales multiplied into an f16 cache
+    (per-tensor scales only).  Exact when the scales are powers of two: an
+    e4m3 value times 2^-2 .. 2^2 is an f16 value."""
+    KVH, D = w.num_kv_heads, w.head_dim
+    kd = lib_decode(w.k_cache, "e4m3").reshape(-1, KVH, D)
+    vd = lib_decode(w.v_cache, "e4m3").reshape(-1, KVH, D)
+    if w.scale_kind == fw.SCALE_HEAD:
+        ks = w.k_scales.astype(np.float64)[None, :, None]
+        vs = w.v_scales.astype(np.float64)[None, :, None]
+    else:
+        ks = w.k_scales.astype(np.float64).reshape(-1, KVH)[:, :, None]
+        vs = w.v_scales.astype(np.float64).reshape(-1, KVH)[:, :, None]
+    kf, vf = kd * ks, vd * vs
+    k16 = fw.f32_to_f16_bits(kf.astype(np.float32)).reshape(w.k_cache.shape)
+    v16 = fw.f32_to_f16_bits(vf.astype(np.float32)).reshape(w.v_cache.shape)
+    assert np.array_equal(lib_decode(k16, "f16").reshape(kf.shape), kf)
+    assert np.array_equal(lib_decode(v16, "f16").reshape(vf.shape), vf)
+    return dataclasses.replace(w, kv_dtype="f16", k_cache=k16, v_cache=v16, scale_kind=0,
+                               k_scales=None, v_scales=None)
+
+
+def pin_head_scales_materialized(orc):
+    """Per-KV-head scales equal an f16 cache holding scale * decoded code
+    (GQA, two dtypes of q, different K and V scales per head)."""
+    for seed, qdt in ((31, "f16"), (32, "bf16")):
+        base = fw.make_contiguous("hs", seed, [1, 40, 129], 16, 4, 64, qdt, "e4m3", gap=3)
+        w = fw.with_scales(base, fw.SCALE_HEAD, seed + 100, powers_of_two=True)
+        assert len(set(w.k_scales.tolist())) > 1 and not np.array_equal(w.k_scales, w.v_scales)
+        a = orc.decode_attention(w)
+        b = orc.decode_attention(materialize_scales(w))
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def pin_token_scales_materialized(orc):
+    """Per-token scales, indexed by cache row and KV head, equal an f16
+    cache holding scale * decoded code: with gaps between sequences (row !=
+    position) and through a shuffled page pool."""
+    base = fw.make_contiguous("ts", 33, [1, 17, 64, 200], 8, 2, 64, "f16", "e4m3", gap=5, lead=2)
+    cases = [base, fw.to_paged(base, 16, 34)]
+    for i, c in enumerate(cases):
+        w = fw.with_scales(c, fw.SCALE_TOKEN, 35 + i, powers_of_two=True)
+        a = orc.decode_attention(w)
+        b = orc.decode_attention(materialize_scales(w))
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), c.name
+
+
+def pin_token_scales_single_key(orc):
+    """One key: out = v_scale * vs(row) * v, lse = softmax_scale * k_scale *
+    ks(row) * q.k (closed form, per head)."""
+    rng = np.random.default_rng(36)
+    D, KVH, QH = 64, 2, 4
+    q = rng.standard_normal((1, QH, D))
+    k = rng.standard_normal((1, KVH, D))
+    v = rng.standard_normal((1, KVH, D))
+    w = custom(q, k, v, [1], kv_dtype="e4m3", softmax_scale=0.25, k_scale=0.5, v_scale=2.0,
+               kv_start_idx=[3])
+    w = dataclasses.replace(w, k_cache=np.concatenate([np.full((3, KVH, D), 0x7E, np.uint8), w.k_cache]),
+                            v_cache=np.concatenate([np.full((3, KVH, D), 0x7E, np.uint8), w.v_cache]))
+    w = fw.with_scales(w, fw.SCALE_TOKEN, 37)
+    out, lse = orc.decode_attention(w)
+    qf = lib_decode(w.q, "f16").reshape(QH, D)
+    kf = lib_decode(w.k_cache, "e4m3")[3]
+    vf = lib_decode(w.v_cache, "e4m3")[3]
+    for qh in range(QH):
+        h = qh // (QH // KVH)
+        ks, vs = float(w.k_scales[3, h]), float(w.v_scales[3, h])
+        _close(out[0, qh], 2.0 * vs * vf[h], 1e-15, 0, "single key out")
+        _close(lse[0, qh], 0.25 * 0.5 * ks * float(qf[qh] @ kf[h]), 1e-12, 1e-14, "single key lse")
+
+
 ALL_PINS = [
     pin_e4m3_codes, pin_f16_codes, pin_bf16_codes, pin_identical_v_rows, pin_single_key,
     pin_zero_query, pin_identical_k_rows, pin_two_keys, pin_dominant_key, pin_empty_sequence,
     pin_weights_sum_to_one, pin_key_permutation, pin_gqa_equals_replicated_mha,
     pin_paged_equals_contiguous, pin_scale_factors, pin_score_shift, pin_online_recurrence,
+    pin_head_scales_materialized, pin_token_scales_materialized, pin_token_scales_single_key,
 ]

@@ -16,10 +16,10 @@ def test_oracle_pin(orc, pin):
 
 # (text in fd_oracle.c, replacement, what the mistake is)
 MUTATIONS = [
-    ("dot += qv[d] * (k_scale * kd);", "dot += qv[d] * kd;", "k_scale dropped"),
+    ("const double ks = k_scale * scale_at(", "const double ks = 1.0 * scale_at(", "k_scale dropped"),
     ("s[t] = softmax_scale * dot;", "s[t] = dot;", "softmax_scale dropped"),
-    ("o[d] += wt * (v_scale * vd);", "o[d] += wt * vd;", "v_scale dropped"),
-    ("o[d] += wt * (v_scale * vd);", "o[d] += s[t] * (v_scale * vd);", "weights not normalised"),
+    ("const double vs = v_scale * scale_at(", "const double vs = 1.0 * scale_at(", "v_scale dropped"),
+    ("o[d] += wt * (vs * vd);", "o[d] += s[t] * (vs * vd);", "weights not normalised"),
     ("*l = M + log(Z);", "*l = log(Z);", "lse misses the max"),
     ("*l = M + log(Z);", "*l = M + log(Z) / 2;", "lse wrong log"),
     ("int kvh = qh / group;", "int kvh = qh % num_kv_heads;", "GQA head map interleaved"),
@@ -36,9 +36,18 @@ MUTATIONS = [
      "else mag = ldexp(1.0 + (double)m / 256.0, e - 127);", "bf16 mantissa"),
     ("for (int t = 0; t < T; ++t) { s[t] = exp(s[t] - M); Z += s[t]; }",
      "for (int t = 0; t < T; ++t) { s[t] = exp(s[t] - M); Z += s[t] * s[t]; }", "wrong sum"),
-    ("size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;\n        for (int d = 0; d < head_dim; ++d) {\n          double vd",
-     "size_t base = ((size_t)rows[t] * num_kv_heads + 0) * head_dim;\n        for (int d = 0; d < head_dim; ++d) {\n          double vd",
+    ("size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;\n        const double vs",
+     "size_t base = ((size_t)rows[t] * num_kv_heads + 0) * head_dim;\n        const double vs",
      "V read from head 0"),
+    ("if (kind == FDO_SCALE_HEAD) return (double)arr[kvh];",
+     "if (kind == FDO_SCALE_HEAD) return (double)arr[0];", "head scale of head 0"),
+    ("if (kind == FDO_SCALE_TOKEN) return (double)arr[(size_t)row * num_kv_heads + kvh];",
+     "if (kind == FDO_SCALE_TOKEN) return (double)arr[(size_t)kvh * num_kv_heads + row % num_kv_heads];",
+     "token scale transposed"),
+    ("scale_at(scale_kind, k_scales, rows[t], num_kv_heads, kvh)",
+     "scale_at(scale_kind, k_scales, t, num_kv_heads, kvh)", "token scale by position"),
+    ("scale_at(scale_kind, v_scales, rows[t], num_kv_heads, kvh)",
+     "scale_at(scale_kind, k_scales, rows[t], num_kv_heads, kvh)", "V scaled by K scales"),
     ("qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + d);",
      "qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + (head_dim - 1 - d));",
      "q transposed"),
