@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--scales", default="tensor", choices=["tensor", "head", "token"],
+                    help="FP8 workloads: finer K/V scales per KV head or per token")
     ap.add_argument("--shared-prefix", type=int, default=0,
                     help="paged workloads: every sequence's first pages alias those of "
                          "sequence 0 up to this many tokens (prefix-cache hits)")
@@ -114,6 +116,11 @@ def make_workload(args) -> fw.Workload:
         if not w.paged:
             raise SystemExit("--shared-prefix needs a paged workload")
         w = fw.share_prefix(w, args.shared_prefix)
+    if args.scales != "tensor":
+        if w.kv_dtype != "e4m3":
+            raise SystemExit("--scales needs an FP8 workload")
+        kind = fw.SCALE_HEAD if args.scales == "head" else fw.SCALE_TOKEN
+        w = fw.with_scales(w, kind, 90 + args.config)
     return w
 
 
@@ -121,6 +128,8 @@ def workload_config(args) -> dict:
     c = {"workload": fw.CONFIG_NAMES[args.config]}
     if args.shared_prefix:
         c["shared_prefix_tokens"] = args.shared_prefix
+    if args.scales != "tensor":
+        c["kv_scales"] = f"per {args.scales} (fp32, on top of the per-tensor scales)"
     return c
 
 
@@ -283,6 +292,12 @@ def run_gpu(args):
     kname = {1: "simt", 2: "mma"}.get(sel, "none")
 
     def step():
+        if w.scale_kind:
+            fda.fd_decode_attention_scaled(
+                t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
+                w.kv_rows, QH, KVH, D, w.page_size, float(w.softmax_scale), float(w.k_scale),
+                float(w.v_scale), w.scale_kind, t["k_scales"], t["v_scales"], out, lse, ws, stream)
+            return
         fda.fd_decode_attention(t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"],
                                 t["seq_len"], w.kv_rows, QH, KVH, D, w.page_size,
                                 float(w.softmax_scale), float(w.k_scale), float(w.v_scale), out,
@@ -369,7 +384,8 @@ def run_gpu(args):
             fda.decode_attention(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["seq_len"],
                                  kv_start_idx=dev_in["kv_start_idx"], block_table=dev_in["block_table"],
                                  softmax_scale=float(w.softmax_scale), k_scale=float(w.k_scale),
-                                 v_scale=float(w.v_scale), workspace=ws, out=out, lse=lse)
+                                 v_scale=float(w.v_scale), workspace=ws, out=out, lse=lse,
+                                 k_scales=dev_in.get("k_scales"), v_scales=dev_in.get("v_scales"))
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 
@@ -421,7 +437,8 @@ def run_gpu(args):
         "gpu_launches": 4 * K,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None if args.shared_prefix else recorded_traffic(kname, args.config),
+                     "traffic": None if (args.shared_prefix or args.scales != "tensor")
+                     else recorded_traffic(kname, args.config),
                      "kernel": f"split ({kname})", "split_us": round(split_avg * 1e3, 2)},
         "e2e": e2e,
         "clocks": clk,

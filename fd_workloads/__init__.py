@@ -243,9 +243,10 @@ def to_paged(w: Workload, page_size: int, seed: int, oversize: float = 1.2,
                                page_size=P, kv_start_idx=None, block_table=table)
 
 
-def with_scales(w: Workload, kind: int, seed: int, powers_of_two: bool = False) -> Workload:
+def with_scales(w: Workload, kind: int, seed: int, powers_of_two: bool = False,
+                span=(0.5, 2.0)) -> Workload:
     """Adds per-KV-head (kind 1) or per-token (kind 2) K/V scales to an e4m3
-    workload.  They multiply k_scale / v_scale; seeded draws from [0.5, 2),
+    workload.  They multiply k_scale / v_scale; seeded draws from ``span``,
     or from {1/4, 1/2, 1, 2, 4} with ``powers_of_two`` (products stay exact)."""
     assert w.kv_dtype == "e4m3" and kind in (SCALE_HEAD, SCALE_TOKEN)
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -254,7 +255,7 @@ def with_scales(w: Workload, kind: int, seed: int, powers_of_two: bool = False) 
     def draw():
         if powers_of_two:
             return np.exp2(rng.integers(-2, 3, size=shape)).astype(np.float32)
-        return rng.uniform(0.5, 2.0, size=shape).astype(np.float32)
+        return rng.uniform(span[0], span[1], size=shape).astype(np.float32)
 
     ks = draw()
     vs = draw()

@@ -40,10 +40,14 @@ FD_KERNEL_AUTO = 0
 FD_KERNEL_SIMT = 1
 FD_KERNEL_MMA = 2
 
+FD_SCALE_TENSOR = 0
+FD_SCALE_HEAD = 1
+FD_SCALE_TOKEN = 2
+
 EXPORTED = [
     "fd_workspace_bytes", "fd_decode_attention", "fd_check_device_error", "fd_status_string",
     "fd_set_kernel", "fd_selected_kernel", "fd_set_split_events", "fd_debug_read_plan",
-    "fd_debug_gather_kv", "fd_decode_attention_noalloc",
+    "fd_debug_gather_kv", "fd_decode_attention_noalloc", "fd_decode_attention_scaled",
 ]
 
 
@@ -75,6 +79,10 @@ def load_library(path: Optional[str] = None):
         lib.fd_decode_attention.restype = i32
         lib.fd_decode_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, i32,
                                             i32, f32, f32, f32, i32, i32, vp, vp, vp, sz, vp]
+        lib.fd_decode_attention_scaled.restype = i32
+        lib.fd_decode_attention_scaled.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32,
+                                                   i32, i32, f32, f32, f32, i32, vp, vp, i32, i32,
+                                                   vp, vp, vp, sz, vp]
         lib.fd_decode_attention_noalloc.restype = i32
         lib.fd_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32,
                                                     i32, i32, i32, f32, f32, f32, i32, i32, vp,
@@ -163,6 +171,32 @@ def fd_decode_attention(q, k_cache, v_cache, kv_start_idx, block_table, seq_len,
         _stream_handle(stream))
     if check and st != FD_OK:
         raise FdError(st, "fd_decode_attention")
+    return st
+
+
+def fd_decode_attention_scaled(q, k_cache, v_cache, kv_start_idx, block_table, seq_len,
+                               kv_rows: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                               page_size: int, softmax_scale: float, k_scale: float,
+                               v_scale: float, scale_kind: int, k_scales, v_scales, out, lse,
+                               workspace, stream=None, q_dtype: Optional[int] = None,
+                               kv_dtype: Optional[int] = None, check: bool = True) -> int:
+    """fd_decode_attention with per-KV-head (FD_SCALE_HEAD, fp32 [KVH]) or
+    per-token (FD_SCALE_TOKEN, fp32 [kv_rows, KVH]) K/V scales on top of
+    k_scale / v_scale."""
+    lib = load_library()
+    batch = int(seq_len.shape[0])
+    stride = int(block_table.shape[1]) if block_table is not None else 0
+    st = lib.fd_decode_attention_scaled(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_start_idx), _ptr(block_table), stride,
+        _ptr(seq_len), int(kv_rows), batch, int(num_q_heads), int(num_kv_heads), int(head_dim),
+        int(page_size), float(softmax_scale), float(k_scale), float(v_scale), int(scale_kind),
+        _ptr(k_scales), _ptr(v_scales),
+        _q_dtype(q) if q_dtype is None else int(q_dtype),
+        _kv_dtype(k_cache) if kv_dtype is None else int(kv_dtype),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_decode_attention_scaled")
     return st
 
 
@@ -256,9 +290,13 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                      block_table: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
                      k_scale: float = 1.0, v_scale: float = 1.0,
                      workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-                     lse: Optional[torch.Tensor] = None, stream=None):
+                     lse: Optional[torch.Tensor] = None, stream=None,
+                     k_scales: Optional[torch.Tensor] = None,
+                     v_scales: Optional[torch.Tensor] = None):
     """Decode attention over a contiguous ([rows, KVH, D]) or paged
-    ([pages, page_size, KVH, D]) cache; returns (out, lse)."""
+    ([pages, page_size, KVH, D]) cache; returns (out, lse).  Optional FP8
+    ``k_scales`` / ``v_scales``: fp32 [KVH] (per KV head) or [kv_rows, KVH]
+    (per token, by cache row), multiplying ``k_scale`` / ``v_scale``."""
     B, QH, D = q.shape
     if block_table is not None:
         pages, P, KVH, D2 = k_cache.shape
@@ -275,6 +313,13 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         lse = torch.empty((B, QH), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = alloc_workspace(B, QH, KVH, D, q.device)
-    fd_decode_attention(q, k_cache, v_cache, kv_start_idx, block_table, seq_len, kv_rows, QH, KVH,
-                        D, P, softmax_scale, k_scale, v_scale, out, lse, workspace, stream)
+    if k_scales is None:
+        fd_decode_attention(q, k_cache, v_cache, kv_start_idx, block_table, seq_len, kv_rows, QH,
+                            KVH, D, P, softmax_scale, k_scale, v_scale, out, lse, workspace,
+                            stream)
+    else:
+        kind = FD_SCALE_HEAD if k_scales.dim() == 1 else FD_SCALE_TOKEN
+        fd_decode_attention_scaled(q, k_cache, v_cache, kv_start_idx, block_table, seq_len,
+                                   kv_rows, QH, KVH, D, P, softmax_scale, k_scale, v_scale, kind,
+                                   k_scales, v_scales, out, lse, workspace, stream)
     return out, lse

@@ -184,6 +184,31 @@ fd_status fd_decode_attention(const void* q, const void* k_cache, const void* v_
                               int page_size, float softmax_scale, float k_scale, float v_scale,
                               fd_dtype q_dtype, fd_dtype kv_dtype, void* out, float* lse,
                               void* workspace, size_t workspace_bytes, fd_stream_t stream) {
+  return fd_decode_attention_scaled(q, k_cache, v_cache, kv_start_idx, block_table,
+                                    block_table_stride, seq_len, kv_rows, batch, num_q_heads,
+                                    num_kv_heads, head_dim, page_size, softmax_scale, k_scale,
+                                    v_scale, FD_SCALE_TENSOR, nullptr, nullptr, q_dtype, kv_dtype,
+                                    out, lse, workspace, workspace_bytes, stream);
+}
+
+fd_status fd_decode_attention_scaled(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* kv_start_idx, const int32_t* block_table,
+                                     int block_table_stride, const int32_t* seq_len,
+                                     int64_t kv_rows, int batch, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int page_size,
+                                     float softmax_scale, float k_scale, float v_scale,
+                                     fd_scale_kind scale_kind, const float* k_scales,
+                                     const float* v_scales, fd_dtype q_dtype, fd_dtype kv_dtype,
+                                     void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, fd_stream_t stream) {
+  if (scale_kind != FD_SCALE_TENSOR && scale_kind != FD_SCALE_HEAD &&
+      scale_kind != FD_SCALE_TOKEN)
+    return FD_ERR_INVALID_ARG;
+  if (scale_kind != FD_SCALE_TENSOR) {
+    if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4))
+      return FD_ERR_INVALID_ARG;
+    if (kv_dtype != FD_E4M3) return FD_ERR_UNSUPPORTED;
+  }
   if (!q || !k_cache || !v_cache || !seq_len || !out || !workspace) return FD_ERR_INVALID_ARG;
   if ((kv_start_idx == nullptr) == (block_table == nullptr)) return FD_ERR_INVALID_ARG;
   if (batch <= 0 || batch > (1 << 24)) return FD_ERR_INVALID_ARG;
@@ -250,6 +275,9 @@ fd_status fd_decode_attention(const void* q, const void* k_cache, const void* v_
   p.kv_dtype = kv_dtype;
   p.score_scale = softmax_scale * k_scale * kLog2e;
   p.v_scale = v_scale;
+  p.scale_kind = scale_kind;
+  p.k_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : k_scales;
+  p.v_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : v_scales;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool timed = t_ev_before != nullptr;

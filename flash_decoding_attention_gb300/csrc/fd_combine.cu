@@ -156,7 +156,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
     }
   }
   if (nseg == 0) return;
-  const float r = L > 0.f ? p.v_scale / L : 0.f;
+  // per-KV-head V scales apply here; per-token ones are inside the partials
+  float vsc = p.v_scale;
+  if (p.scale_kind == FD_SCALE_HEAD) {
+    const int qh = (s - (s / p.hg) * p.hg) * p.hq + i;   // query head of the item
+    vsc *= __ldg(p.v_scales + qh / p.group);
+  }
+  const float r = L > 0.f ? vsc / L : 0.f;
   if constexpr (DPL == 4) {
     uint2 w;
     __half2 h0, h1;

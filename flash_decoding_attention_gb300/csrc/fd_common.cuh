@@ -86,6 +86,9 @@ struct Params {
   int q_dtype, kv_dtype;   // fd_dtype
   float score_scale;   // softmax_scale * k_scale * log2(e)  (scores in log2 units)
   float v_scale;
+  int scale_kind;            // fd_scale_kind: finer K/V scales on top of the two above
+  const float* k_scales;     // FD_SCALE_HEAD: [KVH]; FD_SCALE_TOKEN: [kv_rows][KVH]
+  const float* v_scales;
 };
 
 // ---------------------------------------------------------------------------

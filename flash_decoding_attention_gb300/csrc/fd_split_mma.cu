@@ -71,6 +71,7 @@ struct Shape {
   int stages;
   int merge_bytes;
   int qfrag_bytes;
+  int scale_bytes;   // per stage with per-token scales: K and V scales, [2][hc][tile] fp32
   int smem_bytes;
 };
 
@@ -80,7 +81,8 @@ __host__ __device__ inline int next_pow2(int x) {
   return p;
 }
 
-Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int page_size) {
+Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int page_size,
+                 bool token_scales) {
   Shape s;
   const int elem = kv_dtype == FD_E4M3 ? 1 : 2;
   s.mt = next_pow2((group + 15) / 16);
@@ -104,10 +106,11 @@ Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int pa
   s.kv_bytes = s.hc * s.nx * s.region_bytes;
   s.merge_bytes = s.wph > 1 ? kConsumerWarps * (16 * (head_dim + head_dim / 8) + 32) * 4 : 0;
   s.qfrag_bytes = s.mt * s.hc * (head_dim / 16) * 512;   // one Q fragment set per head tile
-  int st = (kSmemBudget - 1024 - s.merge_bytes - s.qfrag_bytes) / (2 * s.kv_bytes);
+  s.scale_bytes = token_scales ? 2 * s.hc * s.tile * 4 : 0;
+  int st = (kSmemBudget - 1024 - s.merge_bytes - s.qfrag_bytes) / (2 * s.kv_bytes + s.scale_bytes);
   if (st > kMaxStages) st = kMaxStages;
   s.stages = st;
-  s.smem_bytes = 1024 + st * 2 * s.kv_bytes + s.merge_bytes + s.qfrag_bytes;
+  s.smem_bytes = 1024 + st * (2 * s.kv_bytes + s.scale_bytes) + s.merge_bytes + s.qfrag_bytes;
   return s;
 }
 
@@ -170,6 +173,13 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
       "l"(policy)
       : "memory");
+}
+
+// 4-byte asynchronous global -> shared copy; src_bytes 0 writes zero.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* a) {
@@ -305,7 +315,13 @@ struct Shared {
   int pages[kPageWindow];   // producer's window of the current sequence's block table
 };
 
-template <int KVT, typename QT, int D>
+// TOK: per-token K/V scales (fd_scale_kind FD_SCALE_TOKEN).  The producer
+// copies each tile's scales into the stage's scale area with 4-byte cp.async
+// completing on the stage's "full" barrier (one arrival per producer lane);
+// a consumer multiplies each score by its token's K scale and each
+// probability by its token's V scale before the P V product (the softmax sum
+// keeps the unscaled probabilities).
+template <int KVT, typename QT, int D, bool TOK>
 __global__ void __launch_bounds__(kThreads, 1)
     mma_split_kernel(const Params p, const Shape sh, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
@@ -323,11 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t stage0 = smem_u32(base);
   float* merge = reinterpret_cast<float*>(base + sh.stages * 2 * sh.kv_bytes);
   const uint32_t qfrag0 = stage0 + sh.stages * 2 * sh.kv_bytes + sh.merge_bytes;
+  float* scl = reinterpret_cast<float*>(base + sh.stages * 2 * sh.kv_bytes + sh.merge_bytes +
+                                        sh.qfrag_bytes);   // per-token scales (TOK)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < sh.stages; ++i) {
-      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.full[i], TOK ? 1 + 32 : 1);
       mbar_init(&sm.empty[i], kConsumerWarps);
     }
     sm.abort_flag = 0;
@@ -449,8 +467,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         stop = __shfl_sync(0xffffffffu, stop, 0);
         if (stop) break;
+        if constexpr (TOK) {
+          // the tile's per-token scales of its hc heads (rows past the end,
+          // or outside the cache, read as zero)
+          const int stg = (int)(n % S);
+          float* dk = scl + (size_t)stg * (sh.scale_bytes / 4);
+          float* dv = dk + sh.hc * sh.tile;
+          for (int idx = lane; idx < sh.hc * sh.tile; idx += 32) {
+            const int h = idx / sh.tile, tt = idx - h * sh.tile;
+            const int t = t0 + tt;
+            long long row = -1;
+            if (tt < valid) {
+              row = p.block_table
+                        ? ((long long)sm.pages[(t >> p.page_shift) - win_lo] << p.page_shift) +
+                              (t & (p.page_size - 1))
+                        : start + t;
+              if (row < 0 || row >= p.kv_rows) row = -1;
+            }
+            const long long e = row >= 0 ? row * p.num_kv_heads + kvh0 + h : 0;
+            cp_async4(dk + idx, p.k_scales + e, row >= 0 ? 4 : 0);
+            cp_async4(dv + idx, p.v_scales + e, row >= 0 ? 4 : 0);
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                           smem_u32(&sm.full[stg]))
+                       : "memory");
+        }
       }
     }
+    if constexpr (TOK) asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0 && stop) {
       // drain: copies of the last S issued tiles must land before the CTA exits
       for (long long i = n - S < 0 ? 0 : n - S; i < n; ++i)
@@ -492,6 +536,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = seg.s / p.hg;
       const int j = seg.s - b * p.hg;
       const long long qrow0 = (long long)b * p.num_q_heads + j * p.hq;   // first head of stream
+      // score and output factors of this warp's KV head (per-KV-head scales)
+      float sc = p.score_scale, vsc = p.v_scale;
+      if (ELEM == 1 && p.scale_kind == FD_SCALE_HEAD) {   // finer scales: FP8 caches only
+        const int kvh = j * sh.hc + kvl;
+        sc *= __ldg(p.k_scales + kvh);
+        vsc *= __ldg(p.v_scales + kvh);
+      }
       // Q fragments (A operand), head dims permuted as kdim(); every warp of
       // the head tile writes the same values
 #pragma unroll
@@ -592,12 +643,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             //      8*jn + 2q + {0,1} of the sub-tile)
             float pr[NJ][4];
             float mx0 = -INFINITY, mx1 = -INFINITY;
+            // per-token scales of this warp's KV head in the stage (TOK)
+            const float* tsk = scl + (size_t)stg * (sh.scale_bytes / 4) + kvl * sh.tile + sub;
+            const float* tsv = tsk + sh.hc * sh.tile;
 #pragma unroll
             for (int jn = 0; jn < NJ; ++jn) {
+              float2 kk2 = make_float2(1.f, 1.f);
+              if constexpr (TOK) kk2 = *reinterpret_cast<const float2*>(tsk + 8 * jn + 2 * q);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int tok = 8 * jn + 2 * q + (e & 1);
-                float v = s[jn][e] * p.score_scale;
+                float v = s[jn][e] * sc;
+                if constexpr (TOK) v *= (e & 1) ? kk2.y : kk2.x;
                 if (left < SUB && tok >= left) v = -INFINITY;   // ragged end of the segment
                 pr[jn][e] = v;
               }
@@ -626,6 +683,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             l0 = fmaf(l0, a0, ps0);
             l1 = fmaf(l1, a1, ps1);
+            if constexpr (TOK) {   // V scales weight the probabilities, not their sum
+#pragma unroll
+              for (int jn = 0; jn < NJ; ++jn) {
+                const float2 vv = *reinterpret_cast<const float2*>(tsv + 8 * jn + 2 * q);
+                pr[jn][0] *= vv.x;
+                pr[jn][1] *= vv.y;
+                pr[jn][2] *= vv.x;
+                pr[jn][3] *= vv.y;
+              }
+            }
             if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {
 #pragma unroll
               for (int t = 0; t < NT; ++t) {
@@ -732,8 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (sh.wph == 1) {
         // This warp alone holds the head tile's state.  Its head dims form
         // runs of consecutive dims (vdim), written 4 at a time.
-        const float r0 = l0 > 0.f ? p.v_scale / l0 : 0.f;
-        const float r1 = l1 > 0.f ? p.v_scale / l1 : 0.f;
+        const float r0 = l0 > 0.f ? vsc / l0 : 0.f;
+        const float r1 = l1 > 0.f ? vsc / l1 : 0.f;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const bool vh = hh ? v1 : v0;
@@ -819,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int li = kvl * G + lh;
           if (seg.complete) {
-            const float rs = L > 0.f ? p.v_scale / L : 0.f;
+            const float rs = L > 0.f ? vsc / L : 0.f;
             uint2 w;
             w.x = pack_f32x2(A.x * rs, A.y * rs, BF16);
             w.y = pack_f32x2(A.z * rs, A.w * rs, BF16);
@@ -914,10 +981,10 @@ bool get_map(const void* ptr, long long rows, int kvh, int d, int dtype, int box
   return true;
 }
 
-template <int KVT, typename QT, int D>
+template <int KVT, typename QT, int D, bool TOK>
 cudaError_t launch_t(const Params& p, const Shape& sh, const CUtensorMap& mk, const CUtensorMap& mv,
                      cudaStream_t stream) {
-  auto kern = mma_split_kernel<KVT, QT, D>;
+  auto kern = mma_split_kernel<KVT, QT, D, TOK>;
   static int configured = 0;
   if (configured < sh.smem_bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -932,10 +999,14 @@ cudaError_t launch_t(const Params& p, const Shape& sh, const CUtensorMap& mk, co
 template <int D>
 cudaError_t launch_d(const Params& p, const Shape& sh, const CUtensorMap& mk,
                      const CUtensorMap& mv, cudaStream_t st) {
-  if (p.kv_dtype == FD_F16) return launch_t<FD_F16, __half, D>(p, sh, mk, mv, st);
-  if (p.kv_dtype == FD_BF16) return launch_t<FD_BF16, __nv_bfloat16, D>(p, sh, mk, mv, st);
-  if (p.q_dtype == FD_F16) return launch_t<FD_E4M3, __half, D>(p, sh, mk, mv, st);
-  return launch_t<FD_E4M3, __nv_bfloat16, D>(p, sh, mk, mv, st);
+  if (p.kv_dtype == FD_F16) return launch_t<FD_F16, __half, D, false>(p, sh, mk, mv, st);
+  if (p.kv_dtype == FD_BF16) return launch_t<FD_BF16, __nv_bfloat16, D, false>(p, sh, mk, mv, st);
+  const bool tok = p.scale_kind == FD_SCALE_TOKEN;
+  if (p.q_dtype == FD_F16)
+    return tok ? launch_t<FD_E4M3, __half, D, true>(p, sh, mk, mv, st)
+               : launch_t<FD_E4M3, __half, D, false>(p, sh, mk, mv, st);
+  return tok ? launch_t<FD_E4M3, __nv_bfloat16, D, true>(p, sh, mk, mv, st)
+             : launch_t<FD_E4M3, __nv_bfloat16, D, false>(p, sh, mk, mv, st);
 }
 
 }  // namespace
@@ -949,7 +1020,7 @@ bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv
   if (paged && (page_size < 1 || page_size > 256)) return false;
   if (paged) {
     // every TMA box must start on a 1024-byte swizzle atom of shared memory
-    const Shape s = make_shape(group, num_kv_heads, head_dim, kv_dtype, page_size);
+    const Shape s = make_shape(group, num_kv_heads, head_dim, kv_dtype, page_size, false);
     if ((s.box_rows * s.row_bytes) % 1024 != 0) return false;
   }
   if (!encode_fn()) return false;
@@ -961,7 +1032,7 @@ bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv
 // 128 KB takes per SM.  The plan charges it in tiles of this shape.
 void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms, int* hc,
                 int* tile, int* grid, int* seg_units) {
-  const Shape s = make_shape(group, num_kv_heads, head_dim, kv_dtype, 0);
+  const Shape s = make_shape(group, num_kv_heads, head_dim, kv_dtype, 0, false);
   *hc = s.hc;
   *tile = s.tile;
   *grid = sms;
@@ -972,7 +1043,7 @@ void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms
 cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {
   if (p.kv_rows >= (1ll << 31)) return cudaErrorInvalidValue;
   Shape sh = make_shape(p.group, p.num_kv_heads, p.head_dim, p.kv_dtype,
-                        p.block_table ? p.page_size : 0);
+                        p.block_table ? p.page_size : 0, p.scale_kind == FD_SCALE_TOKEN);
   if (sh.stages < 2 || sh.tile != p.tile || sh.hc != p.hc) return cudaErrorInvalidValue;
   CUtensorMap mk, mv;
   // Prefer one box per tile covering all hc heads (fewer, larger TMA copies);

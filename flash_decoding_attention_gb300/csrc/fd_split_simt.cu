@@ -106,6 +106,13 @@ __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p
     const int b = seg.s / p.hg;
     const int qh0 = (seg.s - b * p.hg) * G;
     const int kvh = qh0 / p.group;
+    // finer scales: per KV head fold into q and the output, per token into
+    // each score and each V row below
+    float ksc = 1.f, vsc = 1.f;
+    if (p.scale_kind == FD_SCALE_HEAD) {
+      ksc = __ldg(p.k_scales + kvh);
+      vsc = __ldg(p.v_scales + kvh);
+    }
 
     float qv[kSimtMaxGroup][DPL];
     float m[kSimtMaxGroup], l[kSimtMaxGroup], acc[kSimtMaxGroup][DPL];
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p
       for (int j = 0; j < DPL; ++j) {
         acc[i][j] = 0.f;
         qv[i][j] = i < G ? QType<QT>::to_f32(q[((long long)b * p.num_q_heads + qh0 + i) * D +
-                                               lane * DPL + j]) * p.score_scale
+                                               lane * DPL + j]) * (p.score_scale * ksc)
                          : 0.f;
       }
     }
@@ -129,6 +136,11 @@ __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p
       float kf[DPL], vf[DPL];
       KvRow<KVT, DPL>::load(p.k, off, kf);
       KvRow<KVT, DPL>::load(p.v, off, vf);
+      float tks = 1.f, tvs = 1.f;   // per-token scales of this row
+      if (p.scale_kind == FD_SCALE_TOKEN) {
+        tks = __ldg(p.k_scales + row * p.num_kv_heads + kvh);
+        tvs = __ldg(p.v_scales + row * p.num_kv_heads + kvh);
+      }
 #pragma unroll
       for (int i = 0; i < kSimtMaxGroup; ++i) {
         if (i < G) {
@@ -137,12 +149,13 @@ __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p
           for (int j = 0; j < DPL; ++j) s = fmaf(qv[i][j], kf[j], s);
 #pragma unroll
           for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          s *= tks;
           const float mn = fmaxf(m[i], s);
           const float alpha = fast_exp2(m[i] - mn);
           const float pr = fast_exp2(s - mn);
           l[i] = fmaf(l[i], alpha, pr);
 #pragma unroll
-          for (int j = 0; j < DPL; ++j) acc[i][j] = fmaf(acc[i][j], alpha, pr * vf[j]);
+          for (int j = 0; j < DPL; ++j) acc[i][j] = fmaf(acc[i][j], alpha, (pr * tvs) * vf[j]);
           m[i] = mn;
         }
       }
@@ -175,7 +188,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p
         A = fmaf(sm_acc[(w * G + i) * D + d], f, A);
       }
       if (seg.complete) {
-        const float o = L > 0.f ? A * (p.v_scale / L) : 0.f;
+        const float o = L > 0.f ? A * (p.v_scale * vsc / L) : 0.f;
         static_cast<QT*>(p.out)[((long long)b * p.num_q_heads + qh0 + i) * D + d] =
             QType<QT>::from_f32(o);
         if (d == 0 && p.lse)

@@ -135,6 +135,43 @@ fd_status fd_decode_attention(const void *q, const void *k_cache, const void *v_
                               fd_dtype q_dtype, fd_dtype kv_dtype, void *out, float *lse,
                               void *workspace, size_t workspace_bytes, fd_stream_t stream);
 
+/* Granularity of the finer K/V scales of fd_decode_attention_scaled. */
+typedef enum {
+  FD_SCALE_TENSOR = 0, /* none: k_scale / v_scale only                           */
+  FD_SCALE_HEAD = 1,   /* one fp32 per KV head: k_scales[kvh]                     */
+  FD_SCALE_TOKEN = 2   /* one fp32 per cache row and KV head: k_scales[row * KVH + kvh] */
+} fd_scale_kind;
+
+/*
+ * fd_decode_attention with finer FP8 scales ("Learn CUDA from scratch,
+ * chapter 15", section 15.11: KV quantisation with a scale per tensor, per
+ * head or per token).  The K and V elements of cache row `row` and KV head
+ * `kvh` are decoded as
+ *     k = k_scale * ks * dec(code),   v = v_scale * vs * dec(code),
+ * with ks = k_scales[kvh], vs = v_scales[kvh] (FD_SCALE_HEAD) or
+ * ks = k_scales[row * num_kv_heads + kvh], vs likewise (FD_SCALE_TOKEN; `row`
+ * is the cache row of the token, contiguous or paged, the same index the
+ * caches use).  FD_SCALE_TENSOR ignores both arrays and equals
+ * fd_decode_attention.
+ *
+ * k_scales, v_scales  device fp32 arrays, 4-byte aligned: [num_kv_heads]
+ *                     (FD_SCALE_HEAD) or [kv_rows * num_kv_heads]
+ *                     (FD_SCALE_TOKEN); NULL only with FD_SCALE_TENSOR.
+ * Finer scales need kv_dtype FD_E4M3 (else FD_ERR_UNSUPPORTED).  Every other
+ * argument, the workspace contract and the errors are those of
+ * fd_decode_attention.
+ */
+fd_status fd_decode_attention_scaled(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *kv_start_idx, const int32_t *block_table,
+                                     int block_table_stride, const int32_t *seq_len,
+                                     int64_t kv_rows, int batch, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int page_size,
+                                     float softmax_scale, float k_scale, float v_scale,
+                                     fd_scale_kind scale_kind, const float *k_scales,
+                                     const float *v_scales, fd_dtype q_dtype, fd_dtype kv_dtype,
+                                     void *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, fd_stream_t stream);
+
 /*
  * Same computation as fd_decode_attention, for callers that cannot allocate
  * device memory (for example code running inside a framework that does not

@@ -30,10 +30,18 @@ def run(w: fw.Workload, kernel: int = 0, workspace=None, stream=None, check_erro
         lse = torch.full(t["q"].shape[:2], float("nan"), dtype=torch.float32, device="cuda")
         if workspace is None:
             workspace = fda.alloc_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim)
-        fda.fd_decode_attention(t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"],
-                                t["seq_len"], w.kv_rows, w.num_q_heads, w.num_kv_heads,
-                                w.head_dim, w.page_size, float(w.softmax_scale),
-                                float(w.k_scale), float(w.v_scale), out, lse, workspace, stream)
+        if w.scale_kind:
+            fda.fd_decode_attention_scaled(
+                t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
+                w.kv_rows, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                float(w.softmax_scale), float(w.k_scale), float(w.v_scale), w.scale_kind,
+                t["k_scales"], t["v_scales"], out, lse, workspace, stream)
+        else:
+            fda.fd_decode_attention(t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"],
+                                    t["seq_len"], w.kv_rows, w.num_q_heads, w.num_kv_heads,
+                                    w.head_dim, w.page_size, float(w.softmax_scale),
+                                    float(w.k_scale), float(w.v_scale), out, lse, workspace,
+                                    stream)
         torch.cuda.synchronize()
         if check_errors:
             st, info = fda.fd_check_device_error(workspace, stream)

@@ -121,6 +121,27 @@ def test_shared_prefix_pages(P, shared):
     check_workload(w)
 
 
+@pytest.mark.parametrize("kind", [fw.SCALE_HEAD, fw.SCALE_TOKEN], ids=["head", "token"])
+@pytest.mark.parametrize("layout", [0, 16, 64], ids=["contiguous", "paged16", "paged64"])
+@pytest.mark.parametrize("qh,kvh,qdt", [(64, 8, "f16"), (16, 1, "bf16"), (32, 4, "f16")])
+def test_finer_kv_scales(kind, layout, qh, kvh, qdt):
+    """Per-KV-head and per-token FP8 scales (fd_decode_attention_scaled).  The
+    bf16 bar (max-abs 1.6e-2) assumes outputs of the per-tensor workloads'
+    size, and bf16 rounding grows with the value: the bf16 cases draw scales
+    that keep the outputs there."""
+    base = fw.make_contiguous(f"scales-{kind}-{layout}-{qh}-{kvh}", 61,
+                              [1, 100, 1000, 4097, 0, 33], qh, kvh, 128, qdt, "e4m3", gap=3, lead=2)
+    if layout:
+        base = fw.to_paged(base, layout, 62)
+    span = (0.25, 1.0) if qdt == "bf16" else (0.5, 2.0)
+    check_workload(fw.with_scales(base, kind, 63, span=span))
+
+
+@pytest.mark.parametrize("n,kind", [(4, fw.SCALE_TOKEN), (5, fw.SCALE_HEAD), (3, fw.SCALE_TOKEN)])
+def test_config_full_size_finer_scales(n, kind):
+    check_workload(fw.with_scales(config(n), kind, 64 + n), label=f"config{n}-scales{kind}")
+
+
 @pytest.mark.parametrize("qh,kvh", [(8, 8), (8, 4), (16, 4), (32, 4), (64, 8), (16, 1), (32, 1),
                                     (64, 1), (128, 1), (12, 3), (40, 5)])
 def test_head_groupings(qh, kvh):
