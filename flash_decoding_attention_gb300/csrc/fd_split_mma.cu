@@ -68,10 +68,11 @@ struct Shape {
                      // [nx][hc][tile][row_bytes] regions
   int kv_bytes;      // K (or V) bytes of one stage = hc * nx * region_bytes
   int heads_box;     // 1: one TMA box covers all hc heads of a tile
+  int scale_tma;     // 1: per-token scales come by TMA (else by 4-byte cp.async)
   int stages;
   int merge_bytes;
   int qfrag_bytes;
-  int scale_bytes;   // per stage with per-token scales: K and V scales, [2][hc][tile] fp32
+  int scale_bytes;   // per stage with per-token scales: K then V scales, each [tile][hc] fp32
   int smem_bytes;
 };
 
@@ -103,6 +104,7 @@ Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int pa
   s.box_rows = page_size > 0 && page_size < s.tile ? page_size : s.tile;
   s.region_bytes = s.tile * s.row_bytes;
   s.heads_box = 0;   // decided at launch (needs a tensor map over {dims, rows, heads})
+  s.scale_tma = 0;   // decided at launch (needs a tensor map over the scale arrays)
   s.kv_bytes = s.hc * s.nx * s.region_bytes;
   s.merge_bytes = s.wph > 1 ? kConsumerWarps * (16 * (head_dim + head_dim / 8) + 32) * 4 : 0;
   s.qfrag_bytes = s.mt * s.hc * (head_dim / 16) * 512;   // one Q fragment set per head tile
@@ -172,6 +174,16 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
       ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
       "l"(policy)
+      : "memory");
+}
+
+// TMA 2-D tile load into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -316,15 +328,19 @@ struct Shared {
 };
 
 // TOK: per-token K/V scales (fd_scale_kind FD_SCALE_TOKEN).  The producer
-// copies each tile's scales into the stage's scale area with 4-byte cp.async
-// completing on the stage's "full" barrier (one arrival per producer lane);
-// a consumer multiplies each score by its token's K scale and each
-// probability by its token's V scale before the P V product (the softmax sum
-// keeps the unscaled probabilities).
+// brings each tile's scales into the stage's scale area, [tile][hc] fp32 for K
+// then for V: by TMA next to the K/V boxes when the scale arrays allow it
+// (counted on the stage's "full" barrier like them), else by 4-byte cp.async
+// completing on the same barrier (one more arrival per producer lane).  A
+// consumer multiplies each score by its token's K scale and each probability
+// by its token's V scale before the P V product (the softmax sum keeps the
+// unscaled probabilities).
 template <int KVT, typename QT, int D, bool TOK>
 __global__ void __launch_bounds__(kThreads, 1)
     mma_split_kernel(const Params p, const Shape sh, const __grid_constant__ CUtensorMap tmk,
-                     const __grid_constant__ CUtensorMap tmv) {
+                     const __grid_constant__ CUtensorMap tmv,
+                     const __grid_constant__ CUtensorMap tmks,
+                     const __grid_constant__ CUtensorMap tmvs) {
   constexpr int ELEM = KVT == FD_E4M3 ? 1 : 2;
   constexpr bool BF16 = std::is_same<QT, __nv_bfloat16>::value;
   constexpr int KSTEPS = D / 16;
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < sh.stages; ++i) {
-      mbar_init(&sm.full[i], TOK ? 1 + 32 : 1);
+      mbar_init(&sm.full[i], TOK && !sh.scale_tma ? 1 + 32 : 1);
       mbar_init(&sm.empty[i], kConsumerWarps);
     }
     sm.abort_flag = 0;
@@ -436,10 +452,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (pass == 0) {
                   if (ok) bytes += 2u * sh.hc * sh.nx * sh.box_rows * sh.row_bytes;
-                  else bad = 1;
+                  if (ok && TOK && sh.scale_tma) bytes += 2u * sh.hc * sh.box_rows * 4u;
+                  if (!ok) bad = 1;
                   continue;
                 }
                 if (!ok) continue;
+                if constexpr (TOK) {
+                  if (sh.scale_tma) {   // the box rows' scales of the hc heads
+                    float* sk = scl + (size_t)stg * (sh.scale_bytes / 4) +
+                                (size_t)i * sh.box_rows * sh.hc;
+                    tma_load_2d(sk, &tmks, kvh0, (int)row, &sm.full[stg]);
+                    tma_load_2d(sk + sh.hc * sh.tile, &tmvs, kvh0, (int)row, &sm.full[stg]);
+                  }
+                }
                 if (sh.heads_box) {
                   // one box per head-dim slice: all hc heads of the tile's rows
                   for (int x = 0; x < sh.nx; ++x) {
@@ -467,14 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         stop = __shfl_sync(0xffffffffu, stop, 0);
         if (stop) break;
-        if constexpr (TOK) {
-          // the tile's per-token scales of its hc heads (rows past the end,
-          // or outside the cache, read as zero)
+        if (TOK && !sh.scale_tma) {
+          // the tile's per-token scales of its hc heads, element by element
+          // (rows past the end, or outside the cache, read as zero)
           const int stg = (int)(n % S);
           float* dk = scl + (size_t)stg * (sh.scale_bytes / 4);
           float* dv = dk + sh.hc * sh.tile;
           for (int idx = lane; idx < sh.hc * sh.tile; idx += 32) {
-            const int h = idx / sh.tile, tt = idx - h * sh.tile;
+            const int tt = idx / sh.hc, h = idx - tt * sh.hc;
             const int t = t0 + tt;
             long long row = -1;
             if (tt < valid) {
@@ -643,13 +668,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             //      8*jn + 2q + {0,1} of the sub-tile)
             float pr[NJ][4];
             float mx0 = -INFINITY, mx1 = -INFINITY;
-            // per-token scales of this warp's KV head in the stage (TOK)
-            const float* tsk = scl + (size_t)stg * (sh.scale_bytes / 4) + kvl * sh.tile + sub;
+            // per-token scales of this warp's KV head in the stage (TOK):
+            // token tt of the tile at [tt * hc + kvl]
+            const float* tsk = scl + (size_t)stg * (sh.scale_bytes / 4) + sub * sh.hc + kvl;
             const float* tsv = tsk + sh.hc * sh.tile;
 #pragma unroll
             for (int jn = 0; jn < NJ; ++jn) {
               float2 kk2 = make_float2(1.f, 1.f);
-              if constexpr (TOK) kk2 = *reinterpret_cast<const float2*>(tsk + 8 * jn + 2 * q);
+              if constexpr (TOK) {
+                kk2.x = tsk[(8 * jn + 2 * q) * sh.hc];
+                kk2.y = tsk[(8 * jn + 2 * q + 1) * sh.hc];
+              }
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int tok = 8 * jn + 2 * q + (e & 1);
@@ -686,11 +715,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (TOK) {   // V scales weight the probabilities, not their sum
 #pragma unroll
               for (int jn = 0; jn < NJ; ++jn) {
-                const float2 vv = *reinterpret_cast<const float2*>(tsv + 8 * jn + 2 * q);
-                pr[jn][0] *= vv.x;
-                pr[jn][1] *= vv.y;
-                pr[jn][2] *= vv.x;
-                pr[jn][3] *= vv.y;
+                // tokens past the end: their scale slot may hold anything
+                const int tk = 8 * jn + 2 * q;
+                const float vx = tk < left ? tsv[tk * sh.hc] : 0.f;
+                const float vy = tk + 1 < left ? tsv[(tk + 1) * sh.hc] : 0.f;
+                pr[jn][0] *= vx;
+                pr[jn][1] *= vy;
+                pr[jn][2] *= vx;
+                pr[jn][3] *= vy;
               }
             }
             if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {
@@ -981,9 +1013,46 @@ bool get_map(const void* ptr, long long rows, int kvh, int d, int dtype, int box
   return true;
 }
 
+// 2-D view of a per-token scale array [rows][kvh] fp32: box {heads, box_rows},
+// landing as [box_rows][heads].  Needs 16-byte rows and a 16-byte box width.
+constexpr int kScaleMapTag = 99;   // MapKey dtype of scale maps
+
+bool get_scale_map(const float* ptr, long long rows, int kvh, int heads, int box_rows,
+                   CUtensorMap* out) {
+  if ((kvh * 4) % 16 != 0 || (heads * 4) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
+    return false;
+  MapKey key{ptr, rows, kvh, 0, kScaleMapTag, box_rows, 0, heads};
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  for (int i = 0; i < g_map_used; ++i)
+    if (g_keys[i] == key) {
+      *out = g_maps[i];
+      return true;
+    }
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kvh, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kvh * 4};
+  cuuint32_t box[2] = {(cuuint32_t)heads, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUtensorMap m;
+  CUresult res = fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) return false;
+  int slot = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
+  g_keys[slot] = key;
+  g_maps[slot] = m;
+  *out = m;
+  return true;
+}
+
+struct Maps {
+  CUtensorMap k, v, ks, vs;   // caches; per-token scale arrays (when sh.scale_tma)
+};
+
 template <int KVT, typename QT, int D, bool TOK>
-cudaError_t launch_t(const Params& p, const Shape& sh, const CUtensorMap& mk, const CUtensorMap& mv,
-                     cudaStream_t stream) {
+cudaError_t launch_t(const Params& p, const Shape& sh, const Maps& m, cudaStream_t stream) {
   auto kern = mma_split_kernel<KVT, QT, D, TOK>;
   static int configured = 0;
   if (configured < sh.smem_bytes) {
@@ -992,21 +1061,20 @@ cudaError_t launch_t(const Params& p, const Shape& sh, const CUtensorMap& mk, co
     if (e != cudaSuccess) return e;
     configured = kSmemBudget;
   }
-  kern<<<p.grid, kThreads, sh.smem_bytes, stream>>>(p, sh, mk, mv);
+  kern<<<p.grid, kThreads, sh.smem_bytes, stream>>>(p, sh, m.k, m.v, m.ks, m.vs);
   return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_d(const Params& p, const Shape& sh, const CUtensorMap& mk,
-                     const CUtensorMap& mv, cudaStream_t st) {
-  if (p.kv_dtype == FD_F16) return launch_t<FD_F16, __half, D, false>(p, sh, mk, mv, st);
-  if (p.kv_dtype == FD_BF16) return launch_t<FD_BF16, __nv_bfloat16, D, false>(p, sh, mk, mv, st);
+cudaError_t launch_d(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st) {
+  if (p.kv_dtype == FD_F16) return launch_t<FD_F16, __half, D, false>(p, sh, m, st);
+  if (p.kv_dtype == FD_BF16) return launch_t<FD_BF16, __nv_bfloat16, D, false>(p, sh, m, st);
   const bool tok = p.scale_kind == FD_SCALE_TOKEN;
   if (p.q_dtype == FD_F16)
-    return tok ? launch_t<FD_E4M3, __half, D, true>(p, sh, mk, mv, st)
-               : launch_t<FD_E4M3, __half, D, false>(p, sh, mk, mv, st);
-  return tok ? launch_t<FD_E4M3, __nv_bfloat16, D, true>(p, sh, mk, mv, st)
-             : launch_t<FD_E4M3, __nv_bfloat16, D, false>(p, sh, mk, mv, st);
+    return tok ? launch_t<FD_E4M3, __half, D, true>(p, sh, m, st)
+               : launch_t<FD_E4M3, __half, D, false>(p, sh, m, st);
+  return tok ? launch_t<FD_E4M3, __nv_bfloat16, D, true>(p, sh, m, st)
+             : launch_t<FD_E4M3, __nv_bfloat16, D, false>(p, sh, m, st);
 }
 
 }  // namespace
@@ -1045,7 +1113,10 @@ cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {
   Shape sh = make_shape(p.group, p.num_kv_heads, p.head_dim, p.kv_dtype,
                         p.block_table ? p.page_size : 0, p.scale_kind == FD_SCALE_TOKEN);
   if (sh.stages < 2 || sh.tile != p.tile || sh.hc != p.hc) return cudaErrorInvalidValue;
-  CUtensorMap mk, mv;
+  Maps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  CUtensorMap& mk = maps.k;
+  CUtensorMap& mv = maps.v;
   // Prefer one box per tile covering all hc heads (fewer, larger TMA copies);
   // fall back to one box per head when the tile spans several pages or the
   // driver refuses the head-minor view.
@@ -1061,8 +1132,12 @@ cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {
                       sh.row_bytes, 0, &mv)) {
     return cudaErrorInvalidValue;
   }
-  if (p.head_dim == 128) return launch_d<128>(p, sh, mk, mv, stream);
-  return launch_d<64>(p, sh, mk, mv, stream);
+  if (p.scale_kind == FD_SCALE_TOKEN &&
+      get_scale_map(p.k_scales, p.kv_rows, p.num_kv_heads, sh.hc, sh.box_rows, &maps.ks) &&
+      get_scale_map(p.v_scales, p.kv_rows, p.num_kv_heads, sh.hc, sh.box_rows, &maps.vs))
+    sh.scale_tma = 1;
+  if (p.head_dim == 128) return launch_d<128>(p, sh, maps, stream);
+  return launch_d<64>(p, sh, maps, stream);
 }
 
 }  // namespace fd
