@@ -19,6 +19,9 @@ scope (tiny MQA; GQA bf16; FP8 ragged; FP8 paged; long-context MQA):
   FP8-e4m3 tensors as raw bytes (``uint8``).
 * FP8 K and V are quantised per tensor: ``scale = amax / 448`` in fp32, codes
   ``= e4m3fn(clamp(x / scale, -448, 448))`` rounded to nearest even.
+* INT8 K and V (``kv_dtype='i8'``, stored as ``int8``) are quantised
+  symmetrically per tensor: ``scale = amax / 127`` in fp32, codes
+  ``= clamp(rint(x / scale), -127, 127)`` (round half to even, no zero point).
 """
 from __future__ import annotations
 
@@ -29,11 +32,13 @@ from typing import Optional
 import numpy as np
 
 E4M3_MAX = 448.0
+I8_MAX = 127.0
 
 # Values written where no sequence owns a row (gaps between contiguous
 # sequences, unused pages, page tails).  A kernel that reads such a row
 # produces a grossly wrong score or output, so parity fails loudly.
 POISON_E4M3 = 0x7E          # +448
+POISON_I8 = 127
 
 SCALE_TENSOR, SCALE_HEAD, SCALE_TOKEN = 0, 1, 2
 POISON_F16 = 30000.0
@@ -47,7 +52,7 @@ class Workload:
     num_kv_heads: int
     head_dim: int
     q_dtype: str              # 'f16' | 'bf16'  (out has the same dtype)
-    kv_dtype: str             # 'f16' | 'bf16' | 'e4m3'
+    kv_dtype: str             # 'f16' | 'bf16' | 'e4m3' | 'i8'
     softmax_scale: np.float32
     k_scale: np.float32
     v_scale: np.float32
@@ -81,7 +86,7 @@ class Workload:
 
     @property
     def kv_elem_bytes(self) -> int:
-        return 1 if self.kv_dtype == "e4m3" else 2
+        return 1 if self.kv_dtype in ("e4m3", "i8") else 2
 
     def algorithmic_bytes(self) -> int:
         """Bytes one decode step must move: K and V rows of every sequence,
@@ -124,6 +129,12 @@ def f32_to_e4m3_bytes(x: np.ndarray, scale: np.float32) -> np.ndarray:
     return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
 
 
+def f32_to_i8(x: np.ndarray, scale: np.float32) -> np.ndarray:
+    """Symmetric per-tensor INT8 quantisation (round half to even, clamp 127)."""
+    t = np.ascontiguousarray(x, dtype=np.float32) / np.float32(scale)
+    return np.clip(np.rint(t), -I8_MAX, I8_MAX).astype(np.int8)
+
+
 def _cast16(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "f16":
         return f32_to_f16_bits(x)
@@ -135,21 +146,25 @@ def _cast16(x: np.ndarray, dtype: str) -> np.ndarray:
 def _poison_value(dtype: str):
     if dtype == "e4m3":
         return np.uint8(POISON_E4M3)
+    if dtype == "i8":
+        return np.int8(POISON_I8)
     return _cast16(np.array([POISON_F16], np.float32), dtype)[0]
 
 
 def _quantise_pair(k: np.ndarray, v: np.ndarray, kv_dtype: str):
     """Cast the logical K/V draws to the stored format; return codes and scales."""
-    if kv_dtype == "e4m3":
+    if kv_dtype in ("e4m3", "i8"):
+        top = np.float32(E4M3_MAX if kv_dtype == "e4m3" else I8_MAX)
         k_amax = np.float32(np.abs(k).max()) if k.size else np.float32(1.0)
         v_amax = np.float32(np.abs(v).max()) if v.size else np.float32(1.0)
-        k_scale = np.float32(k_amax / np.float32(E4M3_MAX))
-        v_scale = np.float32(v_amax / np.float32(E4M3_MAX))
+        k_scale = np.float32(k_amax / top)
+        v_scale = np.float32(v_amax / top)
         if k_scale == 0:
             k_scale = np.float32(1.0)
         if v_scale == 0:
             v_scale = np.float32(1.0)
-        return f32_to_e4m3_bytes(k, k_scale), f32_to_e4m3_bytes(v, v_scale), k_scale, v_scale
+        quant = f32_to_e4m3_bytes if kv_dtype == "e4m3" else f32_to_i8
+        return quant(k, k_scale), quant(v, v_scale), k_scale, v_scale
     return _cast16(k, kv_dtype), _cast16(v, kv_dtype), np.float32(1.0), np.float32(1.0)
 
 
@@ -246,9 +261,9 @@ def to_paged(w: Workload, page_size: int, seed: int, oversize: float = 1.2,
 def with_scales(w: Workload, kind: int, seed: int, powers_of_two: bool = False,
                 span=(0.5, 2.0)) -> Workload:
     """Adds per-KV-head (kind 1) or per-token (kind 2) K/V scales to an e4m3
-    workload.  They multiply k_scale / v_scale; seeded draws from ``span``,
+    or i8 workload.  They multiply k_scale / v_scale; seeded draws from ``span``,
     or from {1/4, 1/2, 1, 2, 4} with ``powers_of_two`` (products stay exact)."""
-    assert w.kv_dtype == "e4m3" and kind in (SCALE_HEAD, SCALE_TOKEN)
+    assert w.kv_dtype in ("e4m3", "i8") and kind in (SCALE_HEAD, SCALE_TOKEN)
     rng = np.random.Generator(np.random.PCG64(seed))
     shape = (w.num_kv_heads,) if kind == SCALE_HEAD else (w.kv_rows, w.num_kv_heads)
 
@@ -298,12 +313,17 @@ def gqa_bf16(batch: int = 16, seq: int = 4096) -> Workload:
                            "bf16", "bf16")
 
 
-def fp8_ragged(batch: int = 32, lo: int = 512, hi: int = 32768) -> Workload:
+def _kv_tag(kv_dtype: str) -> str:
+    return "" if kv_dtype == "e4m3" else f"-{kv_dtype}"
+
+
+def fp8_ragged(batch: int = 32, lo: int = 512, hi: int = 32768, kv_dtype: str = "e4m3") -> Workload:
     """B=32, seq_len ~ U{512..32768}, 32/8 heads, D=128, fp16 Q, e4m3 KV,
-    contiguous, seed 2."""
+    contiguous, seed 2 (``kv_dtype='i8'``: the same draws quantised to INT8)."""
     rng = np.random.Generator(np.random.PCG64(2))
     seq = rng.integers(lo, hi, size=batch, endpoint=True).astype(np.int32)
-    return make_contiguous(f"fp8-ragged-B{batch}", 2, seq, 32, 8, 128, "f16", "e4m3", rng=rng)
+    return make_contiguous(f"fp8-ragged-B{batch}{_kv_tag(kv_dtype)}", 2, seq, 32, 8, 128, "f16",
+                           kv_dtype, rng=rng)
 
 
 def lognormal_lengths(rng: np.random.Generator, batch: int, median: float = 2048.0,
@@ -312,19 +332,22 @@ def lognormal_lengths(rng: np.random.Generator, batch: int, median: float = 2048
     return np.clip(np.rint(median * np.exp(z)), lo, hi).astype(np.int32)
 
 
-def fp8_paged(batch: int = 64, page_size: int = 64) -> Workload:
+def fp8_paged(batch: int = 64, page_size: int = 64, kv_dtype: str = "e4m3") -> Workload:
     """B=64, seq_len lognormal (median 2048, sigma 1, clipped to [16, 16384]),
-    64/8 heads, D=128, fp16 Q, e4m3 KV, page_size 64, 1.2x pool, seed 3."""
+    64/8 heads, D=128, fp16 Q, e4m3 KV, page_size 64, 1.2x pool, seed 3
+    (``kv_dtype='i8'``: the same draws quantised to INT8)."""
     rng = np.random.Generator(np.random.PCG64(3))
     seq = lognormal_lengths(rng, batch)
-    w = make_contiguous(f"fp8-paged-B{batch}", 3, seq, 64, 8, 128, "f16", "e4m3", rng=rng)
+    w = make_contiguous(f"fp8-paged-B{batch}{_kv_tag(kv_dtype)}", 3, seq, 64, 8, 128, "f16",
+                        kv_dtype, rng=rng)
     return to_paged(w, page_size, 3, rng=rng)
 
 
-def long_mqa(batch: int = 4, seq: int = 131072) -> Workload:
-    """B=4, seq_len 131072, 16/1 heads, D=128, fp16 Q, e4m3 KV, contiguous, seed 4."""
-    return make_contiguous(f"long-mqa-fp8-B{batch}-T{seq}", 4, [seq] * batch, 16, 1, 128,
-                           "f16", "e4m3")
+def long_mqa(batch: int = 4, seq: int = 131072, kv_dtype: str = "e4m3") -> Workload:
+    """B=4, seq_len 131072, 16/1 heads, D=128, fp16 Q, e4m3 KV, contiguous, seed 4
+    (``kv_dtype='i8'``: the same draws quantised to INT8)."""
+    return make_contiguous(f"long-mqa-fp8-B{batch}-T{seq}{_kv_tag(kv_dtype)}", 4, [seq] * batch,
+                           16, 1, 128, "f16", kv_dtype)
 
 
 CONFIGS = {
@@ -352,7 +375,8 @@ CONFIG_NAMES = {
 def torch_dtypes(w: Workload):
     import torch
     qd = torch.float16 if w.q_dtype == "f16" else torch.bfloat16
-    kd = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.uint8}[w.kv_dtype]
+    kd = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.uint8,
+          "i8": torch.int8}[w.kv_dtype]
     return qd, kd
 
 

@@ -24,7 +24,7 @@ SOURCE = os.path.join(_HERE, "fd_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libfd_oracle.so")
 
-_DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2}
+_DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2, "i8": 3}
 _ERRORS = {1: "bad argument", 2: "cache row out of range", 3: "NaN FP8 code", 4: "out of memory"}
 
 
@@ -62,6 +62,8 @@ class Oracle:
         lib = ctypes.CDLL(lib_path)
         lib.fdo_e4m3_value.restype = ctypes.c_double
         lib.fdo_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.fdo_i8_value.restype = ctypes.c_double
+        lib.fdo_i8_value.argtypes = [ctypes.c_uint8]
         lib.fdo_f16_value.restype = ctypes.c_double
         lib.fdo_f16_value.argtypes = [ctypes.c_uint16]
         lib.fdo_bf16_value.restype = ctypes.c_double
@@ -79,6 +81,9 @@ class Oracle:
 
     def e4m3_value(self, code: int) -> float:
         return self.lib.fdo_e4m3_value(int(code))
+
+    def i8_value(self, code: int) -> float:
+        return self.lib.fdo_i8_value(int(code))
 
     def f16_value(self, bits: int) -> float:
         return self.lib.fdo_f16_value(int(bits))
@@ -171,6 +176,10 @@ def default() -> Oracle:
 
 def e4m3_value(code: int) -> float:
     return default().e4m3_value(code)
+
+
+def i8_value(code: int) -> float:
+    return default().i8_value(code)
 
 
 def f16_value(bits: int) -> float:

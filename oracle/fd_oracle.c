@@ -39,15 +39,17 @@
  *    (page * page_size + offset) rows into a [page, offset, head, dim] pool);
  *  - GQA grouping (group = QH / KVH query heads per KV head): same chapter,
  *    section 15.12;
- *  - FP8 scales: the decoded code times a fp32 scale, the KV quantisation of
- *    section 15.11 of the same chapter, which names the scale granularity
- *    (one per tensor, per head or per token) as part of the method.
+ *  - FP8 and INT8 scales: the decoded code times a fp32 scale, the KV
+ *    quantisation of section 15.11 of the same chapter (FP8 or INT8 K/V
+ *    payloads with scale metadata read next to them), which names the scale
+ *    granularity (one per tensor, per head or per token) as part of the method.
  *
  * Readings where the pages are silent: the contiguous cache is token-major
  * [rows, KVH, D] with kv_start_idx in rows; LSE is in natural log of the
  * scaled scores (softmax_scale and k_scale included); seq_len = 0 gives
  * out = 0 and lse = -inf.  FP8 is OCP e4m3fn (bias 7, no infinities, S.1111.111
- * is NaN and is rejected).
+ * is NaN and is rejected).  INT8 is a symmetric signed code: the value is the
+ * two's-complement integer (-128 .. 127) itself, with no zero point.
  *
  * All arithmetic is IEEE fp64 (build without -ffast-math).
  */
@@ -59,7 +61,7 @@
 #include <omp.h>
 #endif
 
-enum { FDO_F16 = 0, FDO_BF16 = 1, FDO_E4M3 = 2 };
+enum { FDO_F16 = 0, FDO_BF16 = 1, FDO_E4M3 = 2, FDO_I8 = 3 };
 enum { FDO_SCALE_TENSOR = 0, FDO_SCALE_HEAD = 1, FDO_SCALE_TOKEN = 2 };
 
 enum {
@@ -84,6 +86,13 @@ double fdo_e4m3_value(uint8_t code) {
   else
     mag = ldexp(1.0 + (double)m / 8.0, e - 7);
   return s ? -mag : mag;
+}
+
+/* Signed 8-bit integer, two's complement: codes 0x80 .. 0xFF are -128 .. -1. */
+double fdo_i8_value(uint8_t code) {
+  int v = code;
+  if (v >= 128) v -= 256;
+  return (double)v;
 }
 
 /* IEEE 754 binary16: 1 sign, 5 exponent bits with bias 15, 10 mantissa bits. */
@@ -113,6 +122,7 @@ double fdo_bf16_value(uint16_t bits) {
 
 static double decode_elem(const void *base, int dtype, size_t idx) {
   if (dtype == FDO_E4M3) return fdo_e4m3_value(((const uint8_t *)base)[idx]);
+  if (dtype == FDO_I8) return fdo_i8_value(((const uint8_t *)base)[idx]);
   if (dtype == FDO_BF16) return fdo_bf16_value(((const uint16_t *)base)[idx]);
   return fdo_f16_value(((const uint16_t *)base)[idx]);
 }
@@ -168,7 +178,8 @@ int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const 
   if (num_q_heads % num_kv_heads != 0) return FDO_BAD_ARG;
   if (block_table && page_size <= 0) return FDO_BAD_ARG;
   if (q_dtype != FDO_F16 && q_dtype != FDO_BF16) return FDO_BAD_ARG;
-  if (kv_dtype != FDO_F16 && kv_dtype != FDO_BF16 && kv_dtype != FDO_E4M3) return FDO_BAD_ARG;
+  if (kv_dtype != FDO_F16 && kv_dtype != FDO_BF16 && kv_dtype != FDO_E4M3 && kv_dtype != FDO_I8)
+    return FDO_BAD_ARG;
   if (scale_kind < FDO_SCALE_TENSOR || scale_kind > FDO_SCALE_TOKEN) return FDO_BAD_ARG;
   if (scale_kind != FDO_SCALE_TENSOR && (!k_scales || !v_scales)) return FDO_BAD_ARG;
 

@@ -4,7 +4,7 @@ Each ``pin_*`` takes an ``oracle.Oracle`` instance and raises AssertionError
 (or the oracle's own error) when the oracle disagrees with
 
 * the number formats' definitions, decoded by independent library routines
-  (numpy float16, torch bfloat16 and float8_e4m3fn);
+  (numpy float16 and int8, torch bfloat16 and float8_e4m3fn);
 * closed forms of softmax attention (identical rows, one key, two keys,
   uniform weights, a dominant key, the empty sequence);
 * invariants (weights sum to one, key permutation, GQA == MHA with
@@ -44,13 +44,15 @@ def lib_decode(arr: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "e4m3":
         t = torch.from_numpy(arr.view(np.uint8).copy()).view(torch.float8_e4m3fn)
         return t.to(torch.float64).numpy()
+    if dtype == "i8":
+        return arr.view(np.int8).astype(np.float64)
     raise ValueError(dtype)
 
 
 def custom(q32, k32, v32, seq_len, q_dtype="f16", kv_dtype="f16", softmax_scale=0.125,
            k_scale=1.0, v_scale=1.0, kv_start_idx=None, name="custom") -> fw.Workload:
     """A contiguous workload from explicit float arrays (cast to the stored
-    formats; e4m3 codes are taken from the values with scale 1)."""
+    formats; e4m3 and i8 codes are taken from the values with scale 1)."""
     q32 = np.asarray(q32, np.float32)
     k32 = np.asarray(k32, np.float32)
     v32 = np.asarray(v32, np.float32)
@@ -63,6 +65,9 @@ def custom(q32, k32, v32, seq_len, q_dtype="f16", kv_dtype="f16", softmax_scale=
     if kv_dtype == "e4m3":
         k = fw.f32_to_e4m3_bytes(k32, np.float32(1.0))
         v = fw.f32_to_e4m3_bytes(v32, np.float32(1.0))
+    elif kv_dtype == "i8":
+        k = np.clip(np.rint(k32), -128, 127).astype(np.int8)
+        v = np.clip(np.rint(v32), -128, 127).astype(np.int8)
     else:
         k = fw._cast16(k32, kv_dtype)
         v = fw._cast16(v32, kv_dtype)
@@ -175,6 +180,16 @@ def pin_e4m3_codes(orc):
     assert orc.e4m3_value(0x38) == 1.0
     assert orc.e4m3_value(0xB8) == -1.0
     assert math.copysign(1.0, orc.e4m3_value(0x80)) == -1.0 and orc.e4m3_value(0x80) == 0.0
+
+
+def pin_i8_codes(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    ref = lib_decode(codes, "i8")
+    got = np.array([orc.i8_value(int(c)) for c in codes])
+    assert np.array_equal(got, ref), "i8 decode differs from numpy int8"
+    # two's complement ends and the sign boundary
+    assert orc.i8_value(0x7F) == 127.0 and orc.i8_value(0x80) == -128.0
+    assert orc.i8_value(0xFF) == -1.0 and orc.i8_value(0x00) == 0.0
 
 
 def pin_f16_codes(orc):
@@ -395,11 +410,15 @@ def pin_online_recurrence(orc):
 def materialize_scales(w: fw.Workload) -> fw.Workload:
     """The same attention with the finer scales multiplied into an f16 cache
     (per-tensor scales only).  Exact when the scales are powers of two: an
-    e4m3 value times 2^-2 .. 2^2 is an f16 value."""
+    e4m3 value or an i8 code times 2^-2 .. 2^2 is an f16 value.  With
+    per-tensor scales only, the codes are decoded into the f16 cache as they
+    are."""
     KVH, D = w.num_kv_heads, w.head_dim
-    kd = lib_decode(w.k_cache, "e4m3").reshape(-1, KVH, D)
-    vd = lib_decode(w.v_cache, "e4m3").reshape(-1, KVH, D)
-    if w.scale_kind == fw.SCALE_HEAD:
+    kd = lib_decode(w.k_cache, w.kv_dtype).reshape(-1, KVH, D)
+    vd = lib_decode(w.v_cache, w.kv_dtype).reshape(-1, KVH, D)
+    if w.scale_kind == fw.SCALE_TENSOR:
+        ks = vs = np.float64(1.0)
+    elif w.scale_kind == fw.SCALE_HEAD:
         ks = w.k_scales.astype(np.float64)[None, :, None]
         vs = w.v_scales.astype(np.float64)[None, :, None]
     else:
@@ -463,8 +482,44 @@ def pin_token_scales_single_key(orc):
         _close(lse[0, qh], 0.25 * 0.5 * ks * float(qf[qh] @ kf[h]), 1e-12, 1e-14, "single key lse")
 
 
+def pin_i8_materialized(orc):
+    """An INT8 cache equals an f16 cache holding its decoded codes times the
+    finer scales: per tensor, per KV head (GQA, bf16 q) and per token through
+    a shuffled page pool."""
+    base = fw.make_contiguous("i8", 38, [1, 33, 150], 8, 2, 64, "f16", "i8", gap=4, lead=1)
+    assert base.k_cache.dtype == np.int8 and base.k_cache.min() < -100 < 100 < base.k_cache.max()
+    b16 = fw.make_contiguous("i8b", 39, [5, 70], 16, 4, 128, "bf16", "i8", gap=2)
+    cases = [base, fw.with_scales(b16, fw.SCALE_HEAD, 40, powers_of_two=True),
+             fw.with_scales(fw.to_paged(base, 16, 41), fw.SCALE_TOKEN, 42, powers_of_two=True)]
+    for w in cases:
+        a = orc.decode_attention(w)
+        b = orc.decode_attention(materialize_scales(w))
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), w.name
+
+
+def pin_i8_single_key_all_codes(orc):
+    """Sequences of one key each: out = v_scale * V code row (every code
+    -128 .. 127 appears in some V row) and lse = softmax_scale * k_scale *
+    q . (K code row), closed forms."""
+    rng = np.random.default_rng(43)
+    D = 128
+    q = rng.standard_normal((2, 2, D))
+    codes = np.arange(-128, 128, dtype=np.float64).reshape(2, 1, D)
+    k = codes[::-1] * 0.5
+    w = custom(q, k, codes, [1, 1], kv_dtype="i8", softmax_scale=0.0625, k_scale=0.25,
+               v_scale=0.125)
+    out, lse = orc.decode_attention(w)
+    qf = lib_decode(w.q, "f16").reshape(2, 2, D)
+    kf = np.clip(np.rint(k), -128, 127)
+    for b in range(2):
+        for qh in range(2):
+            _close(out[b, qh], 0.125 * codes[b, 0], 0, 0, "i8 single key out")
+            _close(lse[b, qh], 0.0625 * 0.25 * float(qf[b, qh] @ kf[b, 0]), 1e-12, 1e-14,
+                   "i8 single key lse")
+
+
 ALL_PINS = [
-    pin_e4m3_codes, pin_f16_codes, pin_bf16_codes, pin_identical_v_rows, pin_single_key,
+    pin_e4m3_codes, pin_i8_codes, pin_i8_materialized, pin_i8_single_key_all_codes, pin_f16_codes, pin_bf16_codes, pin_identical_v_rows, pin_single_key,
     pin_zero_query, pin_identical_k_rows, pin_two_keys, pin_dominant_key, pin_empty_sequence,
     pin_weights_sum_to_one, pin_key_permutation, pin_gqa_equals_replicated_mha,
     pin_paged_equals_contiguous, pin_scale_factors, pin_score_shift, pin_online_recurrence,

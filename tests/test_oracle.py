@@ -48,6 +48,10 @@ MUTATIONS = [
      "scale_at(scale_kind, k_scales, t, num_kv_heads, kvh)", "token scale by position"),
     ("scale_at(scale_kind, v_scales, rows[t], num_kv_heads, kvh)",
      "scale_at(scale_kind, k_scales, rows[t], num_kv_heads, kvh)", "V scaled by K scales"),
+    ("if (v >= 128) v -= 256;", "if (v > 128) v -= 256;", "i8 code 0x80 read as +128"),
+    ("  return (double)v;\n}", "  return (double)code;\n}", "i8 read as unsigned"),
+    ("if (dtype == FDO_I8) return fdo_i8_value(", "if (dtype == FDO_I8) return fdo_e4m3_value(",
+     "i8 cache decoded as e4m3"),
     ("qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + d);",
      "qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + (head_dim - 1 - d));",
      "q transposed"),
