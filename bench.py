@@ -45,7 +45,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--scales", default="tensor", choices=["tensor", "head", "token"],
-                    help="FP8 workloads: finer K/V scales per KV head or per token")
+                    help="8-bit workloads: finer K/V scales per KV head or per token")
+    ap.add_argument("--kv", default="e4m3", choices=["e4m3", "i8"],
+                    help="8-bit K/V format of the FP8 workloads (configs 3-5): e4m3, or the same "
+                         "draws quantised to INT8 (symmetric, amax/127)")
     ap.add_argument("--shared-prefix", type=int, default=0,
                     help="paged workloads: every sequence's first pages alias those of "
                          "sequence 0 up to this many tokens (prefix-cache hits)")
@@ -111,14 +114,19 @@ def oracle_sample(w: fw.Workload, budget_s: float):
 
 
 def make_workload(args) -> fw.Workload:
-    w = fw.CONFIGS[args.config]()
+    if args.kv != "e4m3":
+        if args.config < 3:
+            raise SystemExit("--kv needs an 8-bit workload (configs 3-5)")
+        w = fw.CONFIGS[args.config](kv_dtype=args.kv)
+    else:
+        w = fw.CONFIGS[args.config]()
     if args.shared_prefix:
         if not w.paged:
             raise SystemExit("--shared-prefix needs a paged workload")
         w = fw.share_prefix(w, args.shared_prefix)
     if args.scales != "tensor":
-        if w.kv_dtype != "e4m3":
-            raise SystemExit("--scales needs an FP8 workload")
+        if w.kv_dtype not in ("e4m3", "i8"):
+            raise SystemExit("--scales needs an 8-bit workload")
         kind = fw.SCALE_HEAD if args.scales == "head" else fw.SCALE_TOKEN
         w = fw.with_scales(w, kind, 90 + args.config)
     return w
@@ -128,6 +136,8 @@ def workload_config(args) -> dict:
     c = {"workload": fw.CONFIG_NAMES[args.config]}
     if args.shared_prefix:
         c["shared_prefix_tokens"] = args.shared_prefix
+    if args.kv != "e4m3":
+        c["kv_dtype"] = f"{args.kv} (the workload's draws quantised to INT8, per-tensor amax/127)"
     if args.scales != "tensor":
         c["kv_scales"] = f"per {args.scales} (fp32, on top of the per-tensor scales)"
     return c
@@ -287,7 +297,7 @@ def run_gpu(args):
     ws = fda.alloc_workspace(B, QH, KVH, D, dev)
     stream = torch.cuda.current_stream(dev)
     sel = fda.fd_selected_kernel(QH, KVH, D, 0 if w.q_dtype == "f16" else 1,
-                                 {"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype], w.paged,
+                                 fda.DTYPE_CODES[w.kv_dtype], w.paged,
                                  max(w.page_size, 1))
     kname = {1: "simt", 2: "mma"}.get(sel, "none")
 
@@ -427,7 +437,8 @@ def run_gpu(args):
         "us_per_step_max": round(max(step_ms) * 1e3, 2),
         "slow_steps": int(sum(1 for x in step_ms if x > 1.5 * float(np.median(step_ms)))),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3->f16 mma, f32 acc" if w.kv_dtype == "e4m3" else f"{w.kv_dtype} mma, f32 acc",
+        "dtype": (f"{w.kv_dtype}->{w.q_dtype} mma, f32 acc" if w.kv_dtype in ("e4m3", "i8")
+                  else f"{w.kv_dtype} mma, f32 acc"),
         "data": "synthetic",
         "config": {**workload_config(args), "kernel": kname,
                    "algorithmic_bytes_per_step": alg, "sum_seq_len": int(w.seq_len.sum()),

@@ -35,6 +35,10 @@ FD_ERR_DEVICE_TIMEOUT = 6
 FD_F16 = 0
 FD_BF16 = 1
 FD_E4M3 = 2
+FD_I8 = 3
+
+# element format names used by the input generators -> fd_dtype codes
+DTYPE_CODES = {"f16": FD_F16, "bf16": FD_BF16, "e4m3": FD_E4M3, "i8": FD_I8}
 
 FD_KERNEL_AUTO = 0
 FD_KERNEL_SIMT = 1
@@ -136,7 +140,10 @@ def _kv_dtype(t: torch.Tensor) -> int:
         return FD_BF16
     if t.dtype in (torch.uint8, torch.float8_e4m3fn):
         return FD_E4M3
-    raise ValueError(f"k/v cache must be float16, bfloat16 or e4m3 bytes, got {t.dtype}")
+    if t.dtype == torch.int8:
+        return FD_I8
+    raise ValueError(f"k/v cache must be float16, bfloat16, e4m3 bytes (uint8) or int8 codes, "
+                     f"got {t.dtype}")
 
 
 # ---------------------------------------------------------------------------

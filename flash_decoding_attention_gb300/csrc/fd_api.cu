@@ -47,7 +47,7 @@ constexpr int kSimtTile = 32;
 
 bool dtypes_ok(int q_dtype, int kv_dtype) {
   if (q_dtype != FD_F16 && q_dtype != FD_BF16) return false;
-  if (kv_dtype == FD_E4M3) return true;
+  if (kv_dtype == FD_E4M3 || kv_dtype == FD_I8) return true;
   return kv_dtype == q_dtype;
 }
 
@@ -162,7 +162,8 @@ size_t fd_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head
   if (sms <= 0) return 0;
   size_t need = 0;
   // Largest layout over every kernel and dtype choice for these sizes.
-  const int dts[4][2] = {{FD_F16, FD_F16}, {FD_BF16, FD_BF16}, {FD_F16, FD_E4M3}, {FD_BF16, FD_E4M3}};
+  const int dts[6][2] = {{FD_F16, FD_F16}, {FD_BF16, FD_BF16}, {FD_F16, FD_E4M3},
+                         {FD_BF16, FD_E4M3}, {FD_F16, FD_I8}, {FD_BF16, FD_I8}};
   for (int pref : {FD_KERNEL_SIMT, FD_KERNEL_MMA}) {
     for (auto& dt : dts) {
       for (int paged : {0, 1}) {
@@ -207,7 +208,7 @@ fd_status fd_decode_attention_scaled(const void* q, const void* k_cache, const v
   if (scale_kind != FD_SCALE_TENSOR) {
     if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4))
       return FD_ERR_INVALID_ARG;
-    if (kv_dtype != FD_E4M3) return FD_ERR_UNSUPPORTED;
+    if (kv_elem_bytes(kv_dtype) != 1) return FD_ERR_UNSUPPORTED;
   }
   if (!q || !k_cache || !v_cache || !seq_len || !out || !workspace) return FD_ERR_INVALID_ARG;
   if ((kv_start_idx == nullptr) == (block_table == nullptr)) return FD_ERR_INVALID_ARG;
@@ -224,7 +225,8 @@ fd_status fd_decode_attention_scaled(const void* q, const void* k_cache, const v
   if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
     return FD_ERR_INVALID_ARG;
   if (q_dtype != FD_F16 && q_dtype != FD_BF16) return FD_ERR_INVALID_ARG;
-  if (kv_dtype != FD_F16 && kv_dtype != FD_BF16 && kv_dtype != FD_E4M3) return FD_ERR_INVALID_ARG;
+  if (kv_dtype != FD_F16 && kv_dtype != FD_BF16 && kv_dtype != FD_E4M3 && kv_dtype != FD_I8)
+    return FD_ERR_INVALID_ARG;
   if (!dtypes_ok(q_dtype, kv_dtype)) return FD_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return FD_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
@@ -334,7 +336,8 @@ fd_status fd_debug_gather_kv(const void* cache, const int32_t* kv_start_idx,
   if ((kv_start_idx == nullptr) == (block_table == nullptr)) return FD_ERR_INVALID_ARG;
   if (block_table && (!is_pow2(page_size) || page_size > 256 || block_table_stride <= 0))
     return FD_ERR_INVALID_ARG;
-  if (kv_dtype != FD_F16 && kv_dtype != FD_BF16 && kv_dtype != FD_E4M3) return FD_ERR_INVALID_ARG;
+  if (kv_dtype != FD_F16 && kv_dtype != FD_BF16 && kv_dtype != FD_E4M3 && kv_dtype != FD_I8)
+    return FD_ERR_INVALID_ARG;
   Params p;
   std::memset(&p, 0, sizeof(p));
   p.k = cache;
@@ -346,7 +349,7 @@ fd_status fd_debug_gather_kv(const void* cache, const int32_t* kv_start_idx,
   p.page_size = block_table ? page_size : 1;
   p.page_shift = block_table ? log2i(page_size) : 0;
   p.ws = static_cast<WsHeader*>(workspace);
-  const int row_bytes = num_kv_heads * head_dim * (kv_dtype == FD_E4M3 ? 1 : 2);
+  const int row_bytes = num_kv_heads * head_dim * kv_elem_bytes(kv_dtype);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   gather_kernel<<<batch, 128, 0, st>>>(p, static_cast<uint8_t*>(dst), row_bytes);
   return cudaGetLastError() == cudaSuccess ? FD_OK : FD_ERR_CUDA;

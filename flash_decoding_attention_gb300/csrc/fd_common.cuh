@@ -32,6 +32,11 @@ static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Bytes of one K/V element: 1 for the 8-bit codes (e4m3, int8), else 2.
+__host__ __device__ constexpr int kv_elem_bytes(int kv_dtype) {
+  return kv_dtype == FD_E4M3 || kv_dtype == FD_I8 ? 1 : 2;
+}
+
 // Workspace = header | prefix int32[num_streams + 1] | ml float2[2*grid][hq] |
 // acc float[2*grid][hq][head_dim].  Every partial slot belongs to one CTA:
 // slot 2c holds the CTA's first segment when that segment continues a stream
@@ -284,6 +289,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Signed 8-bit code (the low byte of `bits`, two's complement) -> its value
+// as fp32, exactly, by the exponent-bias construction of IEEE-754 binary32:
+// the biased byte u = code + 128 placed in the low mantissa bits of 2^23 reads
+// as 2^23 + u, and subtracting 2^23 + 128 leaves the code.
+__device__ __forceinline__ float i8_to_f32(uint32_t bits) {
+  return __uint_as_float(0x4B000000u | ((bits ^ 0x80u) & 0xFFu)) - 8388736.0f;
 }
 
 constexpr float kLog2e = 1.4426950408889634f;

@@ -28,8 +28,9 @@
 //    the online softmax update in registers, and O += P V with P taken
 //    straight from the S accumulators (tokens become the K depth), then
 //    releases the stage on its "empty" mbarrier.
-// FP8 bytes are widened to f16 (or bf16) pairs in registers right before the
-// MMAs.  The head-dim order inside each MMA is permuted consistently on Q and
+// 8-bit codes (FP8 e4m3, or INT8 as in the KV quantisation of "Learn CUDA
+// from scratch, chapter 15", section 15.11) are widened exactly to f16 (or
+// bf16) pairs in registers right before the MMAs.  The head-dim order inside each MMA is permuted consistently on Q and
 // K (a dot product does not depend on it), and the token and head-dim orders
 // of the V operand are chosen so that every shared-memory load is a 16-byte,
 // bank-conflict-free access under the TMA swizzle.
@@ -85,7 +86,7 @@ __host__ __device__ inline int next_pow2(int x) {
 Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int page_size,
                  bool token_scales) {
   Shape s;
-  const int elem = kv_dtype == FD_E4M3 ? 1 : 2;
+  const int elem = kv_elem_bytes(kv_dtype);
   s.mt = next_pow2((group + 15) / 16);
   int hc = kConsumerWarps / s.mt;
   while (hc > 1 && num_kv_heads % hc != 0) hc >>= 1;
@@ -267,6 +268,44 @@ __device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t pair16) {
   }
 }
 
+// Two int8 codes (low byte first) -> two f16 (or bf16) in one register, exact.
+// f16: each biased byte u = code + 128 becomes the low mantissa byte of 1024.0
+// (exponent-bias construction: the half reads 1024 + u), then one packed
+// subtraction of 1152 leaves the codes.  bf16 has too few mantissa bits for
+// that; it goes through exact fp32 values.
+template <bool BF16>
+__device__ __forceinline__ uint32_t widen_i8x2(uint32_t pair16) {
+  if constexpr (BF16) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(i8_to_f32(pair16), i8_to_f32(pair16 >> 8));
+    return *reinterpret_cast<uint32_t*>(&b);
+  } else {
+    const uint32_t biased = __byte_perm(pair16 ^ 0x8080u, 0x64u, 0x4140);
+    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&biased), __half2half2(__ushort_as_half(0x6480)));
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// Four 8-bit codes of the cache format KVT (one word, low byte first) -> two
+// registers of f16 (or bf16) pairs: bytes 0, 1 in .x and bytes 2, 3 in .y,
+// exact.  For int8 with f16 the sign flip of all four bytes is one XOR and
+// each pair is one byte permutation into 1024.0 patterns plus one packed
+// subtraction (see widen_i8x2).
+template <int KVT, bool BF16>
+__device__ __forceinline__ uint2 widen8x4(uint32_t w) {
+  if constexpr (KVT == FD_I8 && !BF16) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t lo = __byte_perm(u, 0x64u, 0x4140), hi = __byte_perm(u, 0x64u, 0x4342);
+    const __half2 bias = __half2half2(__ushort_as_half(0x6480));
+    __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), bias);
+    __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), bias);
+    return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  } else if constexpr (KVT == FD_I8) {
+    return make_uint2(widen_i8x2<BF16>(w), widen_i8x2<BF16>(w >> 16));
+  } else {
+    return make_uint2(widen_e4m3x2<BF16>(w), widen_e4m3x2<BF16>(w >> 16));
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_f32x2(float lo, float hi, bool bf16) {
   if (bf16) {
     __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
@@ -341,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ CUtensorMap tmks,
                      const __grid_constant__ CUtensorMap tmvs) {
-  constexpr int ELEM = KVT == FD_E4M3 ? 1 : 2;
+  constexpr int ELEM = kv_elem_bytes(KVT);
   constexpr bool BF16 = std::is_same<QT, __nv_bfloat16>::value;
   constexpr int KSTEPS = D / 16;
   constexpr int NT = D / 8;     // n-tiles of the PV product
@@ -563,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long qrow0 = (long long)b * p.num_q_heads + j * p.hq;   // first head of stream
       // score and output factors of this warp's KV head (per-KV-head scales)
       float sc = p.score_scale, vsc = p.v_scale;
-      if (ELEM == 1 && p.scale_kind == FD_SCALE_HEAD) {   // finer scales: FP8 caches only
+      if (ELEM == 1 && p.scale_kind == FD_SCALE_HEAD) {   // finer scales: 8-bit caches only
         const int kvh = j * sh.hc + kvl;
         sc *= __ldg(p.k_scales + kvh);
         vsc *= __ldg(p.v_scales + kvh);
@@ -623,9 +662,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int kk = 0; kk < 8; ++kk) {
                 const uint4 a = lds128(qf + kk * 512);
 #pragma unroll
-                for (int jn = 0; jn < NJ; ++jn)
-                  mma16816<BF16>(s[jn], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w[jn][kk]),
-                                 widen_e4m3x2<BF16>(w[jn][kk] >> 16));
+                for (int jn = 0; jn < NJ; ++jn) {
+                  const uint2 kb = widen8x4<KVT, BF16>(w[jn][kk]);
+                  mma16816<BF16>(s[jn], a.x, a.y, a.z, a.w, kb.x, kb.y);
+                }
               }
             } else if constexpr (ELEM == 1) {   // D == 64, 64-byte rows
               uint32_t w[NJ][4];
@@ -638,9 +678,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int kk = 0; kk < 4; ++kk) {
                 const uint4 a = lds128(qf + kk * 512);
 #pragma unroll
-                for (int jn = 0; jn < NJ; ++jn)
-                  mma16816<BF16>(s[jn], a.x, a.y, a.z, a.w, widen_e4m3x2<BF16>(w[jn][kk]),
-                                 widen_e4m3x2<BF16>(w[jn][kk] >> 16));
+                for (int jn = 0; jn < NJ; ++jn) {
+                  const uint2 kb = widen8x4<KVT, BF16>(w[jn][kk]);
+                  mma16816<BF16>(s[jn], a.x, a.y, a.z, a.w, kb.x, kb.y);
+                }
               }
             } else {   // 16-bit: chunk pairs (2q, 2q+1) of each 128-byte region
 #pragma unroll
@@ -758,14 +799,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
                   const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
                   const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
-                  mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01),
-                                 widen_e4m3x2<BF16>(lo89));
-                  mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01 >> 16),
-                                 widen_e4m3x2<BF16>(lo89 >> 16));
-                  mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01),
-                                 widen_e4m3x2<BF16>(hi89));
-                  mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01 >> 16),
-                                 widen_e4m3x2<BF16>(hi89 >> 16));
+                  const uint2 l01 = widen8x4<KVT, BF16>(lo01), l89 = widen8x4<KVT, BF16>(lo89);
+                  const uint2 h01 = widen8x4<KVT, BF16>(hi01), h89 = widen8x4<KVT, BF16>(hi89);
+                  mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, l01.x, l89.x);
+                  mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, l01.y, l89.y);
+                  mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, h01.x, h89.x);
+                  mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, h01.y, h89.y);
                 }
               } else if constexpr (ELEM == 1) {   // D == 64: 8 bytes per token
                 const int c = r >> 1, half = (r & 1) * 8;
@@ -782,14 +821,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
                   const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
                   const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
-                  mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01),
-                                 widen_e4m3x2<BF16>(lo89));
-                  mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(lo01 >> 16),
-                                 widen_e4m3x2<BF16>(lo89 >> 16));
-                  mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01),
-                                 widen_e4m3x2<BF16>(hi89));
-                  mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, widen_e4m3x2<BF16>(hi01 >> 16),
-                                 widen_e4m3x2<BF16>(hi89 >> 16));
+                  const uint2 l01 = widen8x4<KVT, BF16>(lo01), l89 = widen8x4<KVT, BF16>(lo89);
+                  const uint2 h01 = widen8x4<KVT, BF16>(hi01), h89 = widen8x4<KVT, BF16>(hi89);
+                  mma16816<BF16>(o[4 * wd + 0], pa0, pa1, pa2, pa3, l01.x, l89.x);
+                  mma16816<BF16>(o[4 * wd + 1], pa0, pa1, pa2, pa3, l01.y, l89.y);
+                  mma16816<BF16>(o[4 * wd + 2], pa0, pa1, pa2, pa3, h01.x, h89.x);
+                  mma16816<BF16>(o[4 * wd + 3], pa0, pa1, pa2, pa3, h01.y, h89.y);
                 }
               } else {   // 16-bit: chunk r of each 128-byte region holds 8 dims
 #pragma unroll
@@ -985,9 +1022,9 @@ bool get_map(const void* ptr, long long rows, int kvh, int d, int dtype, int box
     }
   auto fn = encode_fn();
   if (!fn) return false;
-  const int elem = dtype == FD_E4M3 ? 1 : 2;
-  CUtensorMapDataType dt = dtype == FD_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                                            : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const int elem = kv_elem_bytes(dtype);
+  CUtensorMapDataType dt = elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : CU_TENSOR_MAP_DATA_TYPE_UINT16;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)kvh, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)d * elem, (cuuint64_t)d * elem * kvh};
   cuuint32_t box[3] = {(cuuint32_t)(row_bytes / elem), 1u, (cuuint32_t)box_rows};
@@ -1065,16 +1102,23 @@ cudaError_t launch_t(const Params& p, const Shape& sh, const Maps& m, cudaStream
   return cudaGetLastError();
 }
 
+// 8-bit caches: q dtype x per-token scales or not.
+template <int KVT, int D>
+cudaError_t launch_8bit(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st) {
+  const bool tok = p.scale_kind == FD_SCALE_TOKEN;
+  if (p.q_dtype == FD_F16)
+    return tok ? launch_t<KVT, __half, D, true>(p, sh, m, st)
+               : launch_t<KVT, __half, D, false>(p, sh, m, st);
+  return tok ? launch_t<KVT, __nv_bfloat16, D, true>(p, sh, m, st)
+             : launch_t<KVT, __nv_bfloat16, D, false>(p, sh, m, st);
+}
+
 template <int D>
 cudaError_t launch_d(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st) {
   if (p.kv_dtype == FD_F16) return launch_t<FD_F16, __half, D, false>(p, sh, m, st);
   if (p.kv_dtype == FD_BF16) return launch_t<FD_BF16, __nv_bfloat16, D, false>(p, sh, m, st);
-  const bool tok = p.scale_kind == FD_SCALE_TOKEN;
-  if (p.q_dtype == FD_F16)
-    return tok ? launch_t<FD_E4M3, __half, D, true>(p, sh, m, st)
-               : launch_t<FD_E4M3, __half, D, false>(p, sh, m, st);
-  return tok ? launch_t<FD_E4M3, __nv_bfloat16, D, true>(p, sh, m, st)
-             : launch_t<FD_E4M3, __nv_bfloat16, D, false>(p, sh, m, st);
+  if (p.kv_dtype == FD_I8) return launch_8bit<FD_I8, D>(p, sh, m, st);
+  return launch_8bit<FD_E4M3, D>(p, sh, m, st);
 }
 
 }  // namespace

@@ -83,6 +83,17 @@ template <int DPL> struct KvRow<FD_E4M3, DPL> {
   }
 };
 
+template <int DPL> struct KvRow<FD_I8, DPL> {
+  static __device__ __forceinline__ void load(const void* base, long long off, float* f) {
+    const uint8_t* p = static_cast<const uint8_t*>(base) + off;
+    uint32_t u;
+    if constexpr (DPL == 4) u = __ldg(reinterpret_cast<const unsigned int*>(p));
+    else u = __ldg(reinterpret_cast<const unsigned short*>(p));
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) f[k] = i8_to_f32(u >> (8 * k));
+  }
+};
+
 template <int KVT, typename QT, int D>
 __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p) {
   constexpr int DPL = D / 32;
@@ -222,6 +233,9 @@ template <int D>
 cudaError_t launch_d(const Params& p, cudaStream_t stream) {
   if (p.kv_dtype == FD_F16) return launch_t<FD_F16, __half, D>(p, stream);
   if (p.kv_dtype == FD_BF16) return launch_t<FD_BF16, __nv_bfloat16, D>(p, stream);
+  if (p.kv_dtype == FD_I8)
+    return p.q_dtype == FD_F16 ? launch_t<FD_I8, __half, D>(p, stream)
+                               : launch_t<FD_I8, __nv_bfloat16, D>(p, stream);
   if (p.q_dtype == FD_F16) return launch_t<FD_E4M3, __half, D>(p, stream);
   return launch_t<FD_E4M3, __nv_bfloat16, D>(p, stream);
 }

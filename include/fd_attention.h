@@ -76,7 +76,11 @@ typedef enum {
   FD_ERR_DEVICE_TIMEOUT = 6        /* a kernel's bounded wait expired */
 } fd_status;
 
-typedef enum { FD_F16 = 0, FD_BF16 = 1, FD_E4M3 = 2 } fd_dtype;
+/* Element formats.  FD_I8 is a symmetric signed 8-bit code: the element's
+ * value is the two's-complement integer (-128 .. 127) times its scales, no
+ * zero point ("Learn CUDA from scratch, chapter 15", section 15.11: INT8 K/V
+ * payloads with fp32 scales). */
+typedef enum { FD_F16 = 0, FD_BF16 = 1, FD_E4M3 = 2, FD_I8 = 3 } fd_dtype;
 
 /* Kernel selection for the split (partial attention) phase. */
 typedef enum {
@@ -117,8 +121,9 @@ size_t fd_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head
  * page_size    paged mode: power of two in [1, 256]; contiguous mode: ignored.
  * softmax_scale, k_scale, v_scale
  *              finite fp32 factors (scores use softmax_scale * k_scale).
- * kv_dtype     FD_F16 (with q FD_F16), FD_BF16 (with q FD_BF16) or FD_E4M3
- *              (OCP e4m3fn, with either q dtype).
+ * kv_dtype     FD_F16 (with q FD_F16), FD_BF16 (with q FD_BF16), FD_E4M3
+ *              (OCP e4m3fn, with either q dtype) or FD_I8 (signed 8-bit
+ *              codes, with either q dtype).
  * out          [batch, num_q_heads, head_dim] of q_dtype.
  * lse          fp32 [batch, num_q_heads], or NULL if not wanted.
  * workspace    device scratch of workspace_bytes >= fd_workspace_bytes(...),
@@ -143,7 +148,7 @@ typedef enum {
 } fd_scale_kind;
 
 /*
- * fd_decode_attention with finer FP8 scales ("Learn CUDA from scratch,
+ * fd_decode_attention with finer FP8 / INT8 scales ("Learn CUDA from scratch,
  * chapter 15", section 15.11: KV quantisation with a scale per tensor, per
  * head or per token).  The K and V elements of cache row `row` and KV head
  * `kvh` are decoded as
@@ -157,7 +162,7 @@ typedef enum {
  * k_scales, v_scales  device fp32 arrays, 4-byte aligned: [num_kv_heads]
  *                     (FD_SCALE_HEAD) or [kv_rows * num_kv_heads]
  *                     (FD_SCALE_TOKEN); NULL only with FD_SCALE_TENSOR.
- * Finer scales need kv_dtype FD_E4M3 (else FD_ERR_UNSUPPORTED).  Every other
+ * Finer scales need kv_dtype FD_E4M3 or FD_I8 (else FD_ERR_UNSUPPORTED).  Every other
  * argument, the workspace contract and the errors are those of
  * fd_decode_attention.
  */

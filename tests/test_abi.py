@@ -76,6 +76,8 @@ def _call(fda, **over):
     (dict(kv_start=None, bt=0x9000, bt_stride=4, page=16, kv_rows=100), 1),  # rows % page
     (dict(kv_rows=0), 1),
     (dict(qdt=2), 1),                                      # q cannot be e4m3
+    (dict(qdt=3), 1),                                      # q cannot be int8
+    (dict(kvdt=4), 1),                                     # unknown cache format
     (dict(qdt=0, kvdt=1), 2),                              # f16 q with bf16 cache
     (dict(ss=float("nan")), 1),
     (dict(q=0x1001), 1),                                   # misaligned q
@@ -83,6 +85,27 @@ def _call(fda, **over):
 ])
 def test_host_validation(fda, over, status):
     assert _call(fda, **over) == status
+
+
+def _call_scaled(fda, kind, k_scales, v_scales, kvdt):
+    """fd_decode_attention_scaled with fake pointers; only argument errors
+    are asked for, so nothing is ever launched."""
+    lib = fda.load_library()
+    return lib.fd_decode_attention_scaled(0x1000, 0x2000, 0x3000, 0x4000, None, 0, 0x5000, 100, 2,
+                                          8, 2, 128, 0, 0.125, 1.0, 1.0, kind, k_scales, v_scales,
+                                          0, kvdt, 0x6000, 0x7000, 0x8000, 1 << 20, None)
+
+
+@pytest.mark.parametrize("kind,ks,vs,kvdt,status", [
+    (3, 0xA000, 0xB000, 2, 1),          # unknown scale kind
+    (1, None, 0xB000, 2, 1),            # missing K scales
+    (2, 0xA000, None, 3, 1),            # missing V scales
+    (2, 0xA002, 0xB000, 3, 1),          # misaligned K scales
+    (1, 0xA000, 0xB000, 0, 2),          # finer scales on an f16 cache
+    (2, 0xA000, 0xB000, 1, 2),          # finer scales on a bf16 cache
+])
+def test_scaled_host_validation(fda, kind, ks, vs, kvdt, status):
+    assert _call_scaled(fda, kind, ks, vs, kvdt) == status
 
 
 def test_set_kernel_rejects_unknown(fda):

@@ -32,7 +32,7 @@ def test_device_plan_matches_restatement(kernel, case):
     fda.fd_set_kernel(kernel)
     ok = fda.fd_selected_kernel(w.num_q_heads, w.num_kv_heads, w.head_dim,
                                 0 if w.q_dtype == "f16" else 1,
-                                {"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype], w.paged, 1) == kernel
+                                fda.DTYPE_CODES[w.kv_dtype], w.paged, 1) == kernel
     fda.fd_set_kernel(0)
     if not ok:
         pytest.skip("kernel does not support this shape")

@@ -25,7 +25,7 @@ def kernels_for(w):
         fda.fd_set_kernel(k)
         sel = fda.fd_selected_kernel(w.num_q_heads, w.num_kv_heads, w.head_dim,
                                      0 if w.q_dtype == "f16" else 1,
-                                     {"f16": 0, "bf16": 1, "e4m3": 2}[w.kv_dtype], w.paged,
+                                     fda.DTYPE_CODES[w.kv_dtype], w.paged,
                                      max(w.page_size, 1))
         fda.fd_set_kernel(0)
         if sel == k:
@@ -62,7 +62,7 @@ EDGE_LENGTHS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 1000
 
 
 @pytest.mark.parametrize("q_dtype,kv_dtype", [("f16", "f16"), ("bf16", "bf16"), ("f16", "e4m3"),
-                                              ("bf16", "e4m3")])
+                                              ("bf16", "e4m3"), ("f16", "i8"), ("bf16", "i8")])
 @pytest.mark.parametrize("D", [64, 128])
 def test_edge_lengths_with_poisoned_gaps(q_dtype, kv_dtype, D):
     w = fw.make_contiguous(f"edge-{q_dtype}-{kv_dtype}-{D}", 100 + D, EDGE_LENGTHS, 8, 2, D,
@@ -121,16 +121,17 @@ def test_shared_prefix_pages(P, shared):
     check_workload(w)
 
 
+@pytest.mark.parametrize("kv", ["e4m3", "i8"])
 @pytest.mark.parametrize("kind", [fw.SCALE_HEAD, fw.SCALE_TOKEN], ids=["head", "token"])
 @pytest.mark.parametrize("layout", [0, 16, 64], ids=["contiguous", "paged16", "paged64"])
 @pytest.mark.parametrize("qh,kvh,qdt", [(64, 8, "f16"), (16, 1, "bf16"), (32, 4, "f16")])
-def test_finer_kv_scales(kind, layout, qh, kvh, qdt):
-    """Per-KV-head and per-token FP8 scales (fd_decode_attention_scaled).  The
-    bf16 bar (max-abs 1.6e-2) assumes outputs of the per-tensor workloads'
+def test_finer_kv_scales(kv, kind, layout, qh, kvh, qdt):
+    """Per-KV-head and per-token FP8 / INT8 scales (fd_decode_attention_scaled).
+    The bf16 bar (max-abs 1.6e-2) assumes outputs of the per-tensor workloads'
     size, and bf16 rounding grows with the value: the bf16 cases draw scales
     that keep the outputs there."""
-    base = fw.make_contiguous(f"scales-{kind}-{layout}-{qh}-{kvh}", 61,
-                              [1, 100, 1000, 4097, 0, 33], qh, kvh, 128, qdt, "e4m3", gap=3, lead=2)
+    base = fw.make_contiguous(f"scales-{kv}-{kind}-{layout}-{qh}-{kvh}", 61,
+                              [1, 100, 1000, 4097, 0, 33], qh, kvh, 128, qdt, kv, gap=3, lead=2)
     if layout:
         base = fw.to_paged(base, layout, 62)
     span = (0.25, 1.0) if qdt == "bf16" else (0.5, 2.0)
@@ -140,6 +141,28 @@ def test_finer_kv_scales(kind, layout, qh, kvh, qdt):
 @pytest.mark.parametrize("n,kind", [(4, fw.SCALE_TOKEN), (5, fw.SCALE_HEAD), (3, fw.SCALE_TOKEN)])
 def test_config_full_size_finer_scales(n, kind):
     check_workload(fw.with_scales(config(n), kind, 64 + n), label=f"config{n}-scales{kind}")
+
+
+@pytest.mark.parametrize("n,kind", [(3, fw.SCALE_TENSOR), (4, fw.SCALE_TENSOR), (5, fw.SCALE_TENSOR),
+                                    (5, fw.SCALE_TOKEN)])
+def test_config_full_size_int8(n, kind):
+    """The 8-bit workloads with the same draws quantised to INT8."""
+    w = fw.CONFIGS[n](kv_dtype="i8")
+    assert w.k_cache.dtype == np.int8
+    if kind:
+        w = fw.with_scales(w, kind, 74 + n)
+    check_workload(w, label=f"config{n}-i8-scales{kind}")
+
+
+@pytest.mark.parametrize("qh,kvh,D,P", [(16, 1, 64, 0), (64, 8, 128, 32), (40, 5, 128, 0),
+                                        (8, 8, 64, 1), (32, 4, 128, 256)])
+def test_int8_shapes(qh, kvh, D, P):
+    """INT8 caches across head groupings, both head dims and page sizes."""
+    w = fw.make_contiguous(f"i8-{qh}-{kvh}-{D}-{P}", 80 + qh + P, [3, 257, 1900, 0, 64], qh, kvh, D,
+                           "bf16" if qh == 40 else "f16", "i8", gap=2, lead=1)
+    if P:
+        w = fw.to_paged(w, P, 81)
+    check_workload(w)
 
 
 @pytest.mark.parametrize("qh,kvh", [(8, 8), (8, 4), (16, 4), (32, 4), (64, 8), (16, 1), (32, 1),
