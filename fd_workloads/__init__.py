@@ -296,6 +296,23 @@ def share_prefix(w: Workload, shared_tokens: int) -> Workload:
     return dataclasses.replace(w, name=w.name + f"-shared{int(shared_tokens)}", block_table=table)
 
 
+def new_tokens(w: Workload, seed: int, std: float = 1.0):
+    """K and V of one new token per sequence, [B, KVH, D] 16-bit patterns of
+    the workload's q dtype (the projection's output dtype): N(0, std^2) draws,
+    K then V."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shape = (w.batch, w.num_kv_heads, w.head_dim)
+    k = rng.standard_normal(shape, dtype=np.float32) * np.float32(std)
+    v = rng.standard_normal(shape, dtype=np.float32) * np.float32(std)
+    return _cast16(k, w.q_dtype), _cast16(v, w.q_dtype)
+
+
+def last_positions(w: Workload) -> np.ndarray:
+    """Index of each sequence's last token (the slot a decode step appends
+    into when seq_len already counts the new token); -1 for empty ones."""
+    return np.where(w.seq_len > 0, w.seq_len - 1, -1).astype(np.int32)
+
+
 # ----------------------------------------------------------------------------
 # the five decode workloads
 # ----------------------------------------------------------------------------

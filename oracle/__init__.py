@@ -76,6 +76,15 @@ class Oracle:
             ctypes.c_double, ctypes.c_double, ctypes.c_double,
             ctypes.c_int, vp, vp,
             vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp]
+        lib.fdo_e4m3_encode.restype = ctypes.c_uint8
+        lib.fdo_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.fdo_i8_encode.restype = ctypes.c_uint8
+        lib.fdo_i8_encode.argtypes = [ctypes.c_float]
+        lib.fdo_append_kv.restype = ctypes.c_int
+        lib.fdo_append_kv.argtypes = [
+            vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int64,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+            ctypes.c_float, ctypes.c_int, vp, vp]
         self.lib = lib
         self.path = lib_path
 
@@ -84,6 +93,38 @@ class Oracle:
 
     def i8_value(self, code: int) -> float:
         return self.lib.fdo_i8_value(int(code))
+
+    def e4m3_encode(self, x: float) -> int:
+        return int(self.lib.fdo_e4m3_encode(float(x)))
+
+    def i8_encode(self, x: float) -> int:
+        return int(self.lib.fdo_i8_encode(float(x)))
+
+    def append_kv(self, w, k_new, v_new, positions):
+        """The KV append on copies of the workload's caches (and per-token
+        scale arrays).  k_new, v_new: [B, KVH, D] 16-bit patterns of the
+        workload's q dtype; positions: int32 [B] (< 0: no append).  Returns
+        (k_cache, v_cache, k_scales, v_scales); the scale arrays are None for
+        per-tensor scales."""
+        k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+        v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+        positions = np.ascontiguousarray(positions, dtype=np.int32)
+        kc = np.ascontiguousarray(w.k_cache).copy()
+        vc = np.ascontiguousarray(w.v_cache).copy()
+        kind = getattr(w, "scale_kind", 0)
+        ks = vs = None
+        if kind:
+            ks = np.ascontiguousarray(w.k_scales, dtype=np.float32).copy()
+            vs = np.ascontiguousarray(w.v_scales, dtype=np.float32).copy()
+        bt_stride = int(w.block_table.shape[1]) if w.block_table is not None else 0
+        rc = self.lib.fdo_append_kv(
+            _ptr(k_new), _ptr(v_new), _DTYPES[w.q_dtype], _ptr(kc), _ptr(vc), _DTYPES[w.kv_dtype],
+            _ptr(w.kv_start_idx), _ptr(w.block_table), bt_stride, _ptr(positions), int(w.kv_rows), int(w.batch), int(w.num_kv_heads),
+            int(w.head_dim), int(w.page_size), float(w.k_scale), float(w.v_scale), int(kind),
+            _ptr(ks), _ptr(vs))
+        if rc != 0:
+            raise OracleError(_ERRORS.get(rc, f"status {rc}"))
+        return kc, vc, ks, vs
 
     def f16_value(self, bits: int) -> float:
         return self.lib.fdo_f16_value(int(bits))

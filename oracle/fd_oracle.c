@@ -51,7 +51,30 @@
  * is NaN and is rejected).  INT8 is a symmetric signed code: the value is the
  * two's-complement integer (-128 .. 127) itself, with no zero point.
  *
- * All arithmetic is IEEE fp64 (build without -ffast-math).
+ * All attention arithmetic is IEEE fp64 (build without -ffast-math).
+ *
+ * KV append (fdo_append_kv): the write of one new token per sequence into the
+ * cache before the attention read ("Learn CUDA from scratch, chapter 15",
+ * section 15.9: contiguous and paged cache write layouts, and its exercise on
+ * a single-token decode append; quantisation with scales as in section
+ * 15.11).  For each sequence b with positions[b] >= 0 and each KV head h:
+ *
+ *   row       = row(b, positions[b])            (as above)
+ *   x_d       = new[b][h][d]                     (f16 or bf16, exact in fp32)
+ *   16-bit cache: the element is stored as it is (the cache has new's dtype);
+ *   8-bit cache, with QMAX = 448 (e4m3) or 127 (int8):
+ *     s = k_scale                                (per tensor)
+ *       = fl32(k_scale * k_scales[h])            (per KV head)
+ *       = fl32(k_scale * ks), ks = fl32(amax / fl32(QMAX * k_scale)) written to
+ *         k_scales[row * KVH + h], amax = max_d |x_d| (ks = 1 if amax = 0)
+ *                                                (per token: scale from the row)
+ *     code_d = enc(fl32(x_d / s))
+ *   enc: e4m3 -- the nearest finite code, ties to the even code, magnitudes
+ *        above 448 saturate to 448; int8 -- the nearest integer, ties to even,
+ *        clamped to [-127, 127].
+ * V likewise with v_scale and v_scales.  The scale products and the quotient
+ * are taken in IEEE fp32, the precision of the device path, because they
+ * decide integer codes.
  */
 #include <math.h>
 #include <stddef.h>
@@ -125,6 +148,35 @@ static double decode_elem(const void *base, int dtype, size_t idx) {
   if (dtype == FDO_I8) return fdo_i8_value(((const uint8_t *)base)[idx]);
   if (dtype == FDO_BF16) return fdo_bf16_value(((const uint16_t *)base)[idx]);
   return fdo_f16_value(((const uint16_t *)base)[idx]);
+}
+
+/* Nearest e4m3 code to x (finite), ties to the even code, |x| > 448 -> 448.
+ * Found by search over the 127 non-negative finite codes; sign kept (so -0
+ * and negative values that round to zero give 0x80). */
+uint8_t fdo_e4m3_encode(float x) {
+  const int neg = signbit(x) != 0;
+  double a = fabs((double)x);
+  if (a > 448.0) a = 448.0;
+  int best = 0;
+  double best_err = a;   /* code 0 is 0.0 */
+  for (int c = 1; c <= 0x7E; ++c) {
+    double err = fabs(fdo_e4m3_value((uint8_t)c) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(best | (neg ? 0x80 : 0));
+}
+
+/* Nearest integer to x, ties to even, clamped to [-127, 127]; two's complement. */
+uint8_t fdo_i8_encode(float x) {
+  double r = floor((double)x);
+  double f = (double)x - r;
+  if (f > 0.5 || (f == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  if (r > 127.0) r = 127.0;
+  if (r < -127.0) r = -127.0;
+  return (uint8_t)(int8_t)(int)r;
 }
 
 /* Row of the cache holding token t of sequence b, or -1 if out of range. */
@@ -270,4 +322,80 @@ int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const 
   }
   if (threads_used) *threads_used = used;
   return status;
+}
+
+/* fp32 value of a 16-bit element (f16 or bf16 bits); exact. */
+static float elem16_to_f32(const uint16_t *base, int dtype, size_t idx) {
+  return (float)(dtype == FDO_BF16 ? fdo_bf16_value(base[idx]) : fdo_f16_value(base[idx]));
+}
+
+/* One tensor (K or V) of the append; see the file comment. */
+static int append_one(const uint16_t *x_new, int new_dtype, void *cache, int kv_dtype,
+                      const int32_t *kv_start_idx, const int32_t *block_table,
+                      int block_table_stride, const int32_t *positions, int64_t kv_rows,
+                      int batch, int num_kv_heads, int head_dim, int page_size, float scale,
+                      int scale_kind, float *scales) {
+  int status = FDO_OK;
+  const float qmax = kv_dtype == FDO_I8 ? 127.0f : 448.0f;
+  for (int b = 0; b < batch; ++b) {
+    if (positions[b] < 0) continue;
+    int64_t row = cache_row(kv_start_idx, block_table, block_table_stride, page_size, b,
+                            positions[b], kv_rows);
+    if (row < 0) { status = FDO_ROW_OUT_OF_RANGE; continue; }
+    for (int h = 0; h < num_kv_heads; ++h) {
+      const size_t src = ((size_t)b * num_kv_heads + h) * head_dim;
+      const size_t dst = ((size_t)row * num_kv_heads + h) * head_dim;
+      if (kv_dtype == FDO_F16 || kv_dtype == FDO_BF16) {
+        for (int d = 0; d < head_dim; ++d) ((uint16_t *)cache)[dst + d] = x_new[src + d];
+        continue;
+      }
+      float s = scale;
+      if (scale_kind == FDO_SCALE_HEAD) {
+        s = scale * scales[h];
+      } else if (scale_kind == FDO_SCALE_TOKEN) {
+        float amax = 0.0f;
+        for (int d = 0; d < head_dim; ++d) {
+          float a = fabsf(elem16_to_f32(x_new, new_dtype, src + d));
+          if (a > amax) amax = a;
+        }
+        const float denom = qmax * scale;
+        const float ks = amax > 0.0f ? amax / denom : 1.0f;
+        scales[(size_t)row * num_kv_heads + h] = ks;
+        s = scale * ks;
+      }
+      for (int d = 0; d < head_dim; ++d) {
+        const float q = elem16_to_f32(x_new, new_dtype, src + d) / s;
+        ((uint8_t *)cache)[dst + d] = kv_dtype == FDO_I8 ? fdo_i8_encode(q) : fdo_e4m3_encode(q);
+      }
+    }
+  }
+  return status;
+}
+
+/*
+ * Writes the new token of every sequence into k_cache / v_cache (see the file
+ * comment).  k_new, v_new: [batch][KVH][D] 16-bit patterns of new_dtype.
+ * positions: [batch] token index of the new token (< 0: no append).
+ * k_scales / v_scales: read (per KV head) or written (per token).
+ */
+int fdo_append_kv(const void *k_new, const void *v_new, int new_dtype, void *k_cache,
+                  void *v_cache, int kv_dtype, const int32_t *kv_start_idx,
+                  const int32_t *block_table, int block_table_stride, const int32_t *positions,
+                  int64_t kv_rows, int batch, int num_kv_heads, int head_dim, int page_size,
+                  float k_scale, float v_scale, int scale_kind, float *k_scales, float *v_scales) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !positions) return FDO_BAD_ARG;
+  if ((kv_start_idx == NULL) == (block_table == NULL)) return FDO_BAD_ARG;
+  if (new_dtype != FDO_F16 && new_dtype != FDO_BF16) return FDO_BAD_ARG;
+  if ((kv_dtype == FDO_F16 || kv_dtype == FDO_BF16) && kv_dtype != new_dtype) return FDO_BAD_ARG;
+  if (kv_dtype != FDO_F16 && kv_dtype != FDO_BF16 && kv_dtype != FDO_E4M3 && kv_dtype != FDO_I8)
+    return FDO_BAD_ARG;
+  if (scale_kind != FDO_SCALE_TENSOR && (!k_scales || !v_scales)) return FDO_BAD_ARG;
+  if (block_table && page_size <= 0) return FDO_BAD_ARG;
+  int a = append_one((const uint16_t *)k_new, new_dtype, k_cache, kv_dtype, kv_start_idx,
+                     block_table, block_table_stride, positions, kv_rows, batch, num_kv_heads,
+                     head_dim, page_size, k_scale, scale_kind, k_scales);
+  int b = append_one((const uint16_t *)v_new, new_dtype, v_cache, kv_dtype, kv_start_idx,
+                     block_table, block_table_stride, positions, kv_rows, batch, num_kv_heads,
+                     head_dim, page_size, v_scale, scale_kind, v_scales);
+  return a != FDO_OK ? a : b;
 }

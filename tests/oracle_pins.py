@@ -518,10 +518,131 @@ def pin_i8_single_key_all_codes(orc):
                    "i8 single key lse")
 
 
+# ----------------------------------------------------------------------------
+# KV append: encoders against library casts, placement and scales
+# ----------------------------------------------------------------------------
+
+def lib_e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """torch's float8_e4m3fn cast (round to nearest even) after clamping to
+    the finite range, as codes."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).clamp(-448.0, 448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def lib_i8_encode(x: np.ndarray) -> np.ndarray:
+    return np.clip(np.rint(np.asarray(x, np.float32)), -127, 127).astype(np.int8).view(np.uint8)
+
+
+def _encoder_inputs(rng):
+    vals = lib_decode(np.arange(0x7F, dtype=np.uint8), "e4m3")       # every finite magnitude
+    mids = (vals[:-1] + vals[1:]) / 2                                  # ties (exact in fp32)
+    x = np.concatenate([vals, -vals, mids, -mids, rng.standard_normal(3000) * 60,
+                        rng.standard_normal(500) * 1e-3, [448.0, 463.9, 464.0, 500.0, 1e6, -1e6,
+                                                          0.0, -0.0, 1e-12, -1e-12]])
+    return x.astype(np.float32)
+
+
+def pin_e4m3_encoder(orc):
+    x = _encoder_inputs(np.random.default_rng(44))
+    got = np.array([orc.e4m3_encode(v) for v in x], np.uint8)
+    ref = lib_e4m3_encode(x)
+    assert np.array_equal(got, ref), f"e4m3 encode differs at {x[got != ref][:5]}"
+
+
+def pin_i8_encoder(orc):
+    rng = np.random.default_rng(45)
+    x = np.concatenate([np.arange(-131, 132), np.arange(-131, 131) + 0.5,
+                        rng.standard_normal(2000) * 50, [1e6, -1e6, 0.0, -0.0, 0.49999997]])
+    x = x.astype(np.float32)
+    got = np.array([orc.i8_encode(v) for v in x], np.uint8)
+    assert np.array_equal(got, lib_i8_encode(x))
+
+
+def _appended_rows(w, positions):
+    """Cache rows the append of ``positions`` writes (row per sequence or -1)."""
+    rows = []
+    for b in range(w.batch):
+        t = int(positions[b])
+        if t < 0:
+            rows.append(-1)
+        elif w.paged:
+            rows.append(int(w.block_table[b, t // w.page_size]) * w.page_size + t % w.page_size)
+        else:
+            rows.append(int(w.kv_start_idx[b]) + t)
+    return rows
+
+
+def _check_append(orc, w, seed):
+    k_new, v_new = fw.new_tokens(w, seed, std=3.0)
+    pos = fw.last_positions(w)
+    pos[0] = -1   # the first sequence gets no append
+    kc, vc, ks, vs = orc.append_kv(w, k_new, v_new, pos)
+    KVH, D = w.num_kv_heads, w.head_dim
+    rows = _appended_rows(w, pos)
+    for cache, old, new, scale, sarr, sarr_old in (
+            (kc, w.k_cache, k_new, w.k_scale, ks, w.k_scales),
+            (vc, w.v_cache, v_new, w.v_scale, vs, w.v_scales)):
+        c2 = cache.reshape(-1, KVH, D)
+        o2 = np.asarray(old).reshape(-1, KVH, D)
+        touched = np.zeros(c2.shape[0], bool)
+        touched[[r for r in rows if r >= 0]] = True
+        assert np.array_equal(c2[~touched], o2[~touched]), f"{w.name}: rows outside the append changed"
+        if sarr is not None and w.scale_kind == fw.SCALE_TOKEN:
+            s2 = sarr.reshape(-1, KVH)
+            assert np.array_equal(s2[~touched], np.asarray(sarr_old).reshape(-1, KVH)[~touched])
+        x = lib_decode(new, w.q_dtype).astype(np.float32)      # [B, KVH, D], exact
+        for b, r in enumerate(rows):
+            if r < 0:
+                continue
+            if w.kv_dtype in ("f16", "bf16"):
+                assert np.array_equal(c2[r], new[b]), "16-bit append must store the bits"
+                continue
+            qmax = 448.0 if w.kv_dtype == "e4m3" else 127.0
+            for h in range(KVH):
+                if w.scale_kind == fw.SCALE_TOKEN:
+                    seff = np.float32(scale) * np.float32(sarr.reshape(-1, KVH)[r, h])
+                elif w.scale_kind == fw.SCALE_HEAD:
+                    seff = np.float32(scale) * np.float32(sarr[h])
+                else:
+                    seff = np.float32(scale)
+                q = x[b, h] / seff                                   # numpy fp32 IEEE division
+                enc = lib_e4m3_encode(q) if w.kv_dtype == "e4m3" else lib_i8_encode(q)
+                assert np.array_equal(c2[r, h].view(np.uint8), enc), f"{w.name} row {r} head {h}"
+                if w.scale_kind == fw.SCALE_TOKEN:
+                    # the row's largest element lands on the largest code, and
+                    # nothing beyond it (no element saturates)
+                    top = np.abs(lib_decode(c2[r, h], w.kv_dtype)).max()
+                    assert top == qmax, (w.name, top)
+                    assert abs(float(np.abs(q).max()) - qmax) <= qmax * 1e-6, (w.name, np.abs(q).max())
+
+
+def pin_append_kv(orc):
+    """The append writes exactly the new token's rows (contiguous with gaps
+    and paged), stores 16-bit elements as they are and 8-bit codes equal to
+    the library casts of x / s in fp32, with per-tensor, per-head and
+    per-token scales; per-token scales put each row's largest element on the
+    largest code and leave other rows' scales alone."""
+    cases = []
+    c1 = fw.make_contiguous("ap1", 46, [5, 1, 40, 0, 200], 8, 2, 64, "f16", "e4m3", gap=2, lead=1)
+    cases.append(c1)
+    cases.append(fw.with_scales(c1, fw.SCALE_HEAD, 47, powers_of_two=False))
+    cases.append(fw.with_scales(fw.to_paged(c1, 16, 48), fw.SCALE_TOKEN, 49))
+    c2 = fw.make_contiguous("ap2", 50, [9, 3, 70, 33], 16, 4, 128, "bf16", "i8", gap=1)
+    cases.append(c2)
+    cases.append(fw.with_scales(fw.to_paged(c2, 8, 51), fw.SCALE_TOKEN, 52))
+    cases.append(fw.with_scales(c2, fw.SCALE_HEAD, 53))
+    cases.append(fw.make_contiguous("ap3", 54, [4, 17], 4, 1, 64, "f16", "f16", gap=1))
+    cases.append(fw.to_paged(fw.make_contiguous("ap4", 55, [4, 17, 2], 8, 2, 128, "bf16", "bf16"),
+                             4, 56))
+    for i, w in enumerate(cases):
+        _check_append(orc, w, 60 + i)
+
+
 ALL_PINS = [
     pin_e4m3_codes, pin_i8_codes, pin_i8_materialized, pin_i8_single_key_all_codes, pin_f16_codes, pin_bf16_codes, pin_identical_v_rows, pin_single_key,
     pin_zero_query, pin_identical_k_rows, pin_two_keys, pin_dominant_key, pin_empty_sequence,
     pin_weights_sum_to_one, pin_key_permutation, pin_gqa_equals_replicated_mha,
     pin_paged_equals_contiguous, pin_scale_factors, pin_score_shift, pin_online_recurrence,
     pin_head_scales_materialized, pin_token_scales_materialized, pin_token_scales_single_key,
+    pin_e4m3_encoder, pin_i8_encoder, pin_append_kv,
 ]

@@ -52,6 +52,19 @@ MUTATIONS = [
     ("  return (double)v;\n}", "  return (double)code;\n}", "i8 read as unsigned"),
     ("if (dtype == FDO_I8) return fdo_i8_value(", "if (dtype == FDO_I8) return fdo_e4m3_value(",
      "i8 cache decoded as e4m3"),
+    ("if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {",
+     "if (err < best_err) {", "e4m3 encoder ties to the lower code"),
+    ("if (f > 0.5 || (f == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;",
+     "if (f >= 0.5) r += 1.0;", "int8 encoder ties away from zero"),
+    ("if (r > 127.0) r = 127.0;", "if (r > 128.0) r = 128.0;", "int8 encoder clamps at 128"),
+    ("positions[b], kv_rows);\n    if (row < 0) { status = FDO_ROW_OUT_OF_RANGE; continue; }",
+     "positions[b] + 1, kv_rows);\n    if (row < 0) { status = FDO_ROW_OUT_OF_RANGE; continue; }",
+     "append one token late"),
+    ("        s = scale * scales[h];\n", "        s = scale;\n", "append ignores head scales"),
+    ("          if (a > amax) amax = a;", "          if (a > amax && d == 0) amax = a;",
+     "token scale from the first element"),
+    ("        const float denom = qmax * scale;", "        const float denom = qmax;",
+     "token scale ignores the per-tensor scale"),
     ("qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + d);",
      "qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + (head_dim - 1 - d));",
      "q transposed"),
