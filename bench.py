@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--kv", default="e4m3", choices=["e4m3", "i8"],
                     help="8-bit K/V format of the FP8 workloads (configs 3-5): e4m3, or the same "
                          "draws quantised to INT8 (symmetric, amax/127)")
+    ap.add_argument("--append", action="store_true",
+                    help="the step also writes each sequence's last token (its K/V rows, "
+                         "quantised for 8-bit caches) before attending, in one call")
     ap.add_argument("--shared-prefix", type=int, default=0,
                     help="paged workloads: every sequence's first pages alias those of "
                          "sequence 0 up to this many tokens (prefix-cache hits)")
@@ -99,7 +102,8 @@ def oracle_sample(w: fw.Workload, budget_s: float):
             w.q, w.q_dtype, w.k_cache, w.v_cache, w.kv_dtype, w.seq_len, w.num_q_heads,
             w.num_kv_heads, w.head_dim, w.softmax_scale, w.k_scale, w.v_scale,
             kv_start_idx=w.kv_start_idx, block_table=w.block_table, page_size=w.page_size,
-            kv_rows=w.kv_rows, pairs=pairs)
+            kv_rows=w.kv_rows, pairs=pairs, scale_kind=w.scale_kind, k_scales=w.k_scales,
+            v_scales=w.v_scales)
         elapsed += time.perf_counter() - t0
         T = int(w.seq_len[b])
         idx = (4 + 4 * (-(-T // w.page_size))) if w.paged else 8
@@ -138,6 +142,10 @@ def workload_config(args) -> dict:
         c["shared_prefix_tokens"] = args.shared_prefix
     if args.kv != "e4m3":
         c["kv_dtype"] = f"{args.kv} (the workload's draws quantised to INT8, per-tensor amax/127)"
+    if args.append:
+        c["append"] = ("each step first writes every sequence's last token (K/V rows of the "
+                       "projection dtype, quantised for 8-bit caches) into the cache, then "
+                       "attends over it: fd_decode_attention_append")
     if args.scales != "tensor":
         c["kv_scales"] = f"per {args.scales} (fp32, on top of the per-tensor scales)"
     return c
@@ -153,7 +161,24 @@ def run_reference(args):
     threads = 0
     desc = ""
     for i in range(args.warmup + args.steps):
-        gbs, threads, desc, el = oracle_sample(w, budget_s=2.0)
+        if args.append:
+            # the oracle's append of the whole batch, then the attention sample
+            import dataclasses
+            import oracle
+            k_new, v_new = fw.new_tokens(w, 500 + args.config)
+            t0 = time.perf_counter()
+            kc, vc, ks, vs = oracle.default().append_kv(w, k_new, v_new, fw.last_positions(w))
+            t_app = time.perf_counter() - t0
+            wa = dataclasses.replace(w, k_cache=kc, v_cache=vc)
+            if w.scale_kind == fw.SCALE_TOKEN:
+                wa = dataclasses.replace(wa, k_scales=ks, v_scales=vs)
+            gbs, threads, desc, el = oracle_sample(wa, budget_s=2.0)
+            el_all = el + t_app
+            gbs = (gbs * el + fw.append_bytes(w) / 1e9) / el_all
+            el = el_all
+            desc += f"; plus the append of all {w.batch} new tokens ({t_app:.3f} s)"
+        else:
+            gbs, threads, desc, el = oracle_sample(w, budget_s=2.0)
         if i >= args.warmup:
             per_step.append(el)
             gbs_all.append(gbs)
@@ -301,7 +326,21 @@ def run_gpu(args):
                                  max(w.page_size, 1))
     kname = {1: "simt", 2: "mma"}.get(sel, "none")
 
+    if args.append:
+        k_new, v_new = fw.new_tokens(w, 500 + args.config)
+        qd, _ = fw.torch_dtypes(w)
+        t["k_new"] = torch.from_numpy(k_new.view(np.int16)).view(qd).to(dev)
+        t["v_new"] = torch.from_numpy(v_new.view(np.int16)).view(qd).to(dev)
+        t["positions"] = torch.from_numpy(fw.last_positions(w)).to(dev)
+
     def step():
+        if args.append:
+            fda.fd_decode_attention_append(
+                t["q"], t["k_new"], t["v_new"], t["k"], t["v"], t["kv_start_idx"],
+                t["block_table"], t["positions"], t["seq_len"], w.kv_rows, QH, KVH, D,
+                w.page_size, float(w.softmax_scale), float(w.k_scale), float(w.v_scale),
+                w.scale_kind, t["k_scales"], t["v_scales"], out, lse, ws, stream)
+            return
         if w.scale_kind:
             fda.fd_decode_attention_scaled(
                 t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
@@ -373,7 +412,7 @@ def run_gpu(args):
     if pg:
         total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / K
-    alg = w.algorithmic_bytes()
+    alg = w.algorithmic_bytes() + (fw.append_bytes(w) if args.append else 0)
     value = whole_job_throughput(alg, world, ms_per_step * 1e-3) / 1e9
 
     # end to end through the public API: pinned host inputs in, result out
@@ -381,6 +420,9 @@ def run_gpu(args):
     e2e = None
     if e2e_steps > 0:
         h = fw.to_torch(w, "cpu", pin=True)
+        if args.append:
+            for key in ("k_new", "v_new", "positions"):
+                h[key] = t[key].cpu().pin_memory()
         h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
         dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in h.items()}
@@ -395,7 +437,9 @@ def run_gpu(args):
                                  kv_start_idx=dev_in["kv_start_idx"], block_table=dev_in["block_table"],
                                  softmax_scale=float(w.softmax_scale), k_scale=float(w.k_scale),
                                  v_scale=float(w.v_scale), workspace=ws, out=out, lse=lse,
-                                 k_scales=dev_in.get("k_scales"), v_scales=dev_in.get("v_scales"))
+                                 k_scales=dev_in.get("k_scales"), v_scales=dev_in.get("v_scales"),
+                                 k_new=dev_in.get("k_new"), v_new=dev_in.get("v_new"),
+                                 positions=dev_in.get("positions"))
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 

@@ -307,6 +307,17 @@ def new_tokens(w: Workload, seed: int, std: float = 1.0):
     return _cast16(k, w.q_dtype), _cast16(v, w.q_dtype)
 
 
+def append_bytes(w: Workload) -> int:
+    """Bytes the KV append of one new token per sequence must move: the new
+    K/V rows read (q dtype), the same rows written to the cache, the
+    positions, and per-token scales written."""
+    rows = w.batch * w.num_kv_heads * w.head_dim
+    b = 2 * rows * 2 + 2 * rows * w.kv_elem_bytes + 4 * w.batch
+    if w.scale_kind == SCALE_TOKEN:
+        b += 2 * 4 * w.batch * w.num_kv_heads
+    return b
+
+
 def last_positions(w: Workload) -> np.ndarray:
     """Index of each sequence's last token (the slot a decode step appends
     into when seq_len already counts the new token); -1 for empty ones."""

@@ -52,6 +52,7 @@ EXPORTED = [
     "fd_workspace_bytes", "fd_decode_attention", "fd_check_device_error", "fd_status_string",
     "fd_set_kernel", "fd_selected_kernel", "fd_set_split_events", "fd_debug_read_plan",
     "fd_debug_gather_kv", "fd_decode_attention_noalloc", "fd_decode_attention_scaled",
+    "fd_append_kv", "fd_decode_attention_append",
 ]
 
 
@@ -87,6 +88,13 @@ def load_library(path: Optional[str] = None):
         lib.fd_decode_attention_scaled.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32,
                                                    i32, i32, f32, f32, f32, i32, vp, vp, i32, i32,
                                                    vp, vp, vp, sz, vp]
+        lib.fd_append_kv.restype = i32
+        lib.fd_append_kv.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, i32, f32,
+                                     f32, i32, vp, vp, i32, i32, vp, sz, vp]
+        lib.fd_decode_attention_append.restype = i32
+        lib.fd_decode_attention_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i64,
+                                                   i32, i32, i32, i32, i32, f32, f32, f32, i32,
+                                                   vp, vp, i32, i32, vp, vp, vp, sz, vp]
         lib.fd_decode_attention_noalloc.restype = i32
         lib.fd_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32,
                                                     i32, i32, i32, f32, f32, f32, i32, i32, vp,
@@ -207,6 +215,56 @@ def fd_decode_attention_scaled(q, k_cache, v_cache, kv_start_idx, block_table, s
     return st
 
 
+def fd_append_kv(k_new, v_new, k_cache, v_cache, kv_start_idx, block_table, positions,
+                 kv_rows: int, num_kv_heads: int, head_dim: int, page_size: int, k_scale: float,
+                 v_scale: float, scale_kind: int, k_scales, v_scales, workspace, stream=None,
+                 new_dtype: Optional[int] = None, kv_dtype: Optional[int] = None,
+                 check: bool = True) -> int:
+    """Writes one new token per sequence (k_new, v_new: [B, KVH, D]) into the
+    caches at ``positions`` (int32 [B], < 0: none), quantising for 8-bit
+    caches; per-token scales are written into ``k_scales`` / ``v_scales``."""
+    lib = load_library()
+    batch = int(positions.shape[0])
+    stride = int(block_table.shape[1]) if block_table is not None else 0
+    st = lib.fd_append_kv(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(kv_start_idx),
+        _ptr(block_table), stride, _ptr(positions), int(kv_rows), batch, int(num_kv_heads),
+        int(head_dim), int(page_size), float(k_scale), float(v_scale), int(scale_kind),
+        _ptr(k_scales), _ptr(v_scales),
+        _q_dtype(k_new) if new_dtype is None else int(new_dtype),
+        _kv_dtype(k_cache) if kv_dtype is None else int(kv_dtype),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_append_kv")
+    return st
+
+
+def fd_decode_attention_append(q, k_new, v_new, k_cache, v_cache, kv_start_idx, block_table,
+                               positions, seq_len, kv_rows: int, num_q_heads: int,
+                               num_kv_heads: int, head_dim: int, page_size: int,
+                               softmax_scale: float, k_scale: float, v_scale: float,
+                               scale_kind: int, k_scales, v_scales, out, lse, workspace,
+                               stream=None, q_dtype: Optional[int] = None,
+                               kv_dtype: Optional[int] = None, check: bool = True) -> int:
+    """fd_append_kv of the step's new token, then the attention over the
+    caches holding it (``seq_len`` counts the new token), in one call."""
+    lib = load_library()
+    batch = int(seq_len.shape[0])
+    stride = int(block_table.shape[1]) if block_table is not None else 0
+    st = lib.fd_decode_attention_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(kv_start_idx),
+        _ptr(block_table), stride, _ptr(positions), _ptr(seq_len), int(kv_rows), batch,
+        int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size), float(softmax_scale),
+        float(k_scale), float(v_scale), int(scale_kind), _ptr(k_scales), _ptr(v_scales),
+        _q_dtype(q) if q_dtype is None else int(q_dtype),
+        _kv_dtype(k_cache) if kv_dtype is None else int(kv_dtype),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_decode_attention_append")
+    return st
+
+
 def fd_decode_attention_noalloc(q, k_cache, v_cache, kv_start_idx, block_table, seq_len,
                                 kv_rows: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                                 page_size: int, softmax_scale: float, k_scale: float,
@@ -299,11 +357,16 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                      workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                      lse: Optional[torch.Tensor] = None, stream=None,
                      k_scales: Optional[torch.Tensor] = None,
-                     v_scales: Optional[torch.Tensor] = None):
+                     v_scales: Optional[torch.Tensor] = None,
+                     k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+                     positions: Optional[torch.Tensor] = None):
     """Decode attention over a contiguous ([rows, KVH, D]) or paged
-    ([pages, page_size, KVH, D]) cache; returns (out, lse).  Optional FP8
+    ([pages, page_size, KVH, D]) cache; returns (out, lse).  Optional 8-bit
     ``k_scales`` / ``v_scales``: fp32 [KVH] (per KV head) or [kv_rows, KVH]
-    (per token, by cache row), multiplying ``k_scale`` / ``v_scale``."""
+    (per token, by cache row), multiplying ``k_scale`` / ``v_scale``.  With
+    ``k_new`` / ``v_new`` ([B, KVH, D], q's dtype) and ``positions`` (int32
+    [B]) the step's new token is first written into the caches (quantised for
+    8-bit caches, per-token scales written), and ``seq_len`` counts it."""
     B, QH, D = q.shape
     if block_table is not None:
         pages, P, KVH, D2 = k_cache.shape
@@ -320,7 +383,14 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         lse = torch.empty((B, QH), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = alloc_workspace(B, QH, KVH, D, q.device)
-    if k_scales is None:
+    if k_new is not None:
+        kind = FD_SCALE_TENSOR if k_scales is None else (
+            FD_SCALE_HEAD if k_scales.dim() == 1 else FD_SCALE_TOKEN)
+        fd_decode_attention_append(q, k_new, v_new, k_cache, v_cache, kv_start_idx, block_table,
+                                   positions, seq_len, kv_rows, QH, KVH, D, P, softmax_scale,
+                                   k_scale, v_scale, kind, k_scales, v_scales, out, lse,
+                                   workspace, stream)
+    elif k_scales is None:
         fd_decode_attention(q, k_cache, v_cache, kv_start_idx, block_table, seq_len, kv_rows, QH,
                             KVH, D, P, softmax_scale, k_scale, v_scale, out, lse, workspace,
                             stream)

@@ -88,6 +88,39 @@ int log2i(int x) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The new token's rows and where they go (KV append).
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* positions;
+  void* k_cache;
+  void* v_cache;
+  float* k_scales;   // written with per-token scales
+  float* v_scales;
+};
+
+// Checks of the append's own arguments; the cache, layout and scale-kind
+// arguments are checked by the caller.  8-bit codes divide by the scales.
+fd_status check_append(const AppendArgs& a, int kv_dtype, float k_scale, float v_scale) {
+  if (!a.k_new || !a.v_new || !a.positions || !a.k_cache || !a.v_cache) return FD_ERR_INVALID_ARG;
+  if (!aligned(a.k_new, 16) || !aligned(a.v_new, 16) || !aligned(a.positions, 4))
+    return FD_ERR_INVALID_ARG;
+  if (kv_elem_bytes(kv_dtype) == 1 && !(k_scale > 0.f && v_scale > 0.f)) return FD_ERR_INVALID_ARG;
+  return FD_OK;
+}
+
+void set_append(Params& p, const AppendArgs& a, float k_scale, float v_scale) {
+  p.k_new = a.k_new;
+  p.v_new = a.v_new;
+  p.positions = a.positions;
+  p.k_dst = a.k_cache;
+  p.v_dst = a.v_cache;
+  p.k_scales_dst = p.scale_kind == FD_SCALE_TOKEN ? a.k_scales : nullptr;
+  p.v_scales_dst = p.scale_kind == FD_SCALE_TOKEN ? a.v_scales : nullptr;
+  p.k_scale_raw = k_scale;
+  p.v_scale_raw = v_scale;
+}
+
 // Gather of the stored K or V slice of every token, with the kernels'
 // addressing (test hook).  CTA b copies sequence b; its destination offset
 // is the sum of the earlier sequences' lengths.
@@ -192,16 +225,18 @@ fd_status fd_decode_attention(const void* q, const void* k_cache, const void* v_
                                     out, lse, workspace, workspace_bytes, stream);
 }
 
-fd_status fd_decode_attention_scaled(const void* q, const void* k_cache, const void* v_cache,
-                                     const int32_t* kv_start_idx, const int32_t* block_table,
-                                     int block_table_stride, const int32_t* seq_len,
-                                     int64_t kv_rows, int batch, int num_q_heads,
-                                     int num_kv_heads, int head_dim, int page_size,
-                                     float softmax_scale, float k_scale, float v_scale,
-                                     fd_scale_kind scale_kind, const float* k_scales,
-                                     const float* v_scales, fd_dtype q_dtype, fd_dtype kv_dtype,
-                                     void* out, float* lse, void* workspace,
-                                     size_t workspace_bytes, fd_stream_t stream) {
+// The attention of one decode step, optionally preceded by the KV append of
+// the step's new token (then the split kernel runs as a programmatic
+// dependent of the append and waits for it before reading the caches).
+static fd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* kv_start_idx, const int32_t* block_table,
+                             int block_table_stride, const int32_t* seq_len, int64_t kv_rows,
+                             int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                             int page_size, float softmax_scale, float k_scale, float v_scale,
+                             fd_scale_kind scale_kind, const float* k_scales,
+                             const float* v_scales, fd_dtype q_dtype, fd_dtype kv_dtype, void* out,
+                             float* lse, void* workspace, size_t workspace_bytes,
+                             fd_stream_t stream, const AppendArgs* app) {
   if (scale_kind != FD_SCALE_TENSOR && scale_kind != FD_SCALE_HEAD &&
       scale_kind != FD_SCALE_TOKEN)
     return FD_ERR_INVALID_ARG;
@@ -232,6 +267,10 @@ fd_status fd_decode_attention_scaled(const void* q, const void* k_cache, const v
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
     return FD_ERR_INVALID_ARG;
+  if (app) {
+    const fd_status st = check_append(*app, kv_dtype, k_scale, v_scale);
+    if (st != FD_OK) return st;
+  }
 
   const int sms = current_sms();
   if (sms <= 0) return FD_ERR_CUDA;
@@ -282,6 +321,11 @@ fd_status fd_decode_attention_scaled(const void* q, const void* k_cache, const v
   p.v_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : v_scales;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (app) {
+    set_append(p, *app, k_scale, v_scale);
+    if (launch_append(p, st) != cudaSuccess) return FD_ERR_CUDA;
+    p.pdl = 1;
+  }
   const bool timed = t_ev_before != nullptr;
   if (timed && cudaEventRecord(t_ev_before, st) != cudaSuccess) return FD_ERR_CUDA;
   cudaError_t e = c.kernel == FD_KERNEL_MMA ? launch_split_mma(p, st) : launch_split_simt(p, st);
@@ -290,6 +334,100 @@ fd_status fd_decode_attention_scaled(const void* q, const void* k_cache, const v
   e = launch_combine(p, st);
   if (e != cudaSuccess) return FD_ERR_CUDA;
   return FD_OK;
+}
+
+fd_status fd_decode_attention_scaled(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* kv_start_idx, const int32_t* block_table,
+                                     int block_table_stride, const int32_t* seq_len,
+                                     int64_t kv_rows, int batch, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int page_size,
+                                     float softmax_scale, float k_scale, float v_scale,
+                                     fd_scale_kind scale_kind, const float* k_scales,
+                                     const float* v_scales, fd_dtype q_dtype, fd_dtype kv_dtype,
+                                     void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, fd_stream_t stream) {
+  return decode_impl(q, k_cache, v_cache, kv_start_idx, block_table, block_table_stride, seq_len,
+                     kv_rows, batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                     softmax_scale, k_scale, v_scale, scale_kind, k_scales, v_scales, q_dtype,
+                     kv_dtype, out, lse, workspace, workspace_bytes, stream, nullptr);
+}
+
+fd_status fd_decode_attention_append(const void* q, const void* k_new, const void* v_new,
+                                     void* k_cache, void* v_cache, const int32_t* kv_start_idx,
+                                     const int32_t* block_table, int block_table_stride,
+                                     const int32_t* positions, const int32_t* seq_len,
+                                     int64_t kv_rows, int batch, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int page_size,
+                                     float softmax_scale, float k_scale, float v_scale,
+                                     fd_scale_kind scale_kind, float* k_scales, float* v_scales,
+                                     fd_dtype q_dtype, fd_dtype kv_dtype, void* out, float* lse,
+                                     void* workspace, size_t workspace_bytes, fd_stream_t stream) {
+  const AppendArgs app{k_new, v_new, positions, k_cache, v_cache, k_scales, v_scales};
+  return decode_impl(q, k_cache, v_cache, kv_start_idx, block_table, block_table_stride, seq_len,
+                     kv_rows, batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                     softmax_scale, k_scale, v_scale, scale_kind, k_scales, v_scales, q_dtype,
+                     kv_dtype, out, lse, workspace, workspace_bytes, stream, &app);
+}
+
+fd_status fd_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                       const int32_t* kv_start_idx, const int32_t* block_table,
+                       int block_table_stride, const int32_t* positions, int64_t kv_rows,
+                       int batch, int num_kv_heads, int head_dim, int page_size, float k_scale,
+                       float v_scale, fd_scale_kind scale_kind, float* k_scales, float* v_scales,
+                       fd_dtype new_dtype, fd_dtype kv_dtype, void* workspace,
+                       size_t workspace_bytes, fd_stream_t stream) {
+  if (scale_kind != FD_SCALE_TENSOR && scale_kind != FD_SCALE_HEAD &&
+      scale_kind != FD_SCALE_TOKEN)
+    return FD_ERR_INVALID_ARG;
+  if (scale_kind != FD_SCALE_TENSOR) {
+    if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4))
+      return FD_ERR_INVALID_ARG;
+    if (kv_elem_bytes(kv_dtype) != 1) return FD_ERR_UNSUPPORTED;
+  }
+  const AppendArgs app{k_new, v_new, positions, k_cache, v_cache, k_scales, v_scales};
+  if (!workspace || !aligned(workspace, 256)) return FD_ERR_INVALID_ARG;
+  if ((kv_start_idx == nullptr) == (block_table == nullptr)) return FD_ERR_INVALID_ARG;
+  if (batch <= 0 || batch > (1 << 24) || num_kv_heads <= 0 || num_kv_heads > 4096)
+    return FD_ERR_INVALID_ARG;
+  if (kv_rows <= 0 || kv_rows > (int64_t(1) << 40)) return FD_ERR_INVALID_ARG;
+  const int paged = block_table != nullptr;
+  if (paged) {
+    if (!is_pow2(page_size) || page_size > 256) return FD_ERR_UNSUPPORTED;
+    if (block_table_stride <= 0 || kv_rows % page_size != 0) return FD_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return FD_ERR_INVALID_ARG;
+  if (new_dtype != FD_F16 && new_dtype != FD_BF16) return FD_ERR_INVALID_ARG;
+  if (kv_dtype != FD_F16 && kv_dtype != FD_BF16 && kv_dtype != FD_E4M3 && kv_dtype != FD_I8)
+    return FD_ERR_INVALID_ARG;
+  if (!dtypes_ok(new_dtype, kv_dtype)) return FD_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return FD_ERR_UNSUPPORTED;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return FD_ERR_INVALID_ARG;
+  const fd_status cs = check_append(app, kv_dtype, k_scale, v_scale);
+  if (cs != FD_OK) return cs;
+  if (workspace_bytes < sizeof(WsHeader)) return FD_ERR_WORKSPACE_TOO_SMALL;
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.k = k_cache;
+  p.v = v_cache;
+  p.kv_start = kv_start_idx;
+  p.block_table = block_table;
+  p.bt_stride = paged ? block_table_stride : 0;
+  p.ws = static_cast<WsHeader*>(workspace);
+  p.kv_rows = kv_rows;
+  p.batch = batch;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.page_size = paged ? page_size : 1;
+  p.page_shift = paged ? log2i(page_size) : 0;
+  p.q_dtype = new_dtype;
+  p.kv_dtype = kv_dtype;
+  p.scale_kind = scale_kind;
+  p.k_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : k_scales;
+  p.v_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : v_scales;
+  set_append(p, app, k_scale, v_scale);
+  return launch_append(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FD_OK
+                                                                                : FD_ERR_CUDA;
 }
 
 fd_status fd_check_device_error(void* workspace, fd_stream_t stream, int64_t* info) {

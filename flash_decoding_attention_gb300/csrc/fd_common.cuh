@@ -94,6 +94,16 @@ struct Params {
   int scale_kind;            // fd_scale_kind: finer K/V scales on top of the two above
   const float* k_scales;     // FD_SCALE_HEAD: [KVH]; FD_SCALE_TOKEN: [kv_rows][KVH]
   const float* v_scales;
+  int pdl;                   // split kernel launched as a programmatic dependent (of the append)
+  // KV append (fd_append.cu); q_dtype is the dtype of k_new / v_new
+  const void* k_new;         // [batch][KVH][D]
+  const void* v_new;
+  const int32_t* positions;  // [batch] token index of the new token, < 0: none
+  void* k_dst;               // the caches, written
+  void* v_dst;
+  float* k_scales_dst;       // FD_SCALE_TOKEN: per-token scales, written
+  float* v_scales_dst;
+  float k_scale_raw, v_scale_raw;   // the per-tensor scales as given
 };
 
 // ---------------------------------------------------------------------------
@@ -282,6 +292,14 @@ __device__ __forceinline__ void allow_dependent_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Waits until the grid this one depends on programmatically (the KV append,
+// when the split kernel is launched after it with programmatic stream
+// serialisation) has completed and its writes are visible.  Returns at once
+// for a grid launched in plain stream order.
+__device__ __forceinline__ void wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Small math helpers
 // ---------------------------------------------------------------------------
@@ -312,10 +330,30 @@ template <> struct QType<__nv_bfloat16> {
   static __device__ __forceinline__ __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
 };
 
+// Launches a split kernel, as a programmatic dependent of the previous
+// kernel in the stream when p.pdl (the kernel calls wait_prior_grid before
+// it reads the caches).
+template <typename Kernel, typename... Args>
+inline cudaError_t launch_split(const Params& p, Kernel kern, dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launchers (defined in their .cu files).
 cudaError_t launch_split_simt(const Params& p, cudaStream_t stream);
 cudaError_t launch_split_mma(const Params& p, cudaStream_t stream);
 cudaError_t launch_combine(const Params& p, cudaStream_t stream);
+cudaError_t launch_append(const Params& p, cudaStream_t stream);
 int simt_ctas_per_sm();
 bool simt_supports(int group, int head_dim);
 int simt_heads_per_stream(int group);

@@ -415,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   prefetch_index_arrays(p);
   const PlanResult plan = compute_plan(p, sm.red);   // contains __syncthreads
   allow_dependent_launch();
+  wait_prior_grid();   // a KV append launched just before may still be writing rows
 
   const int S = sh.stages;
   if (warp == kConsumerWarps) {
@@ -1098,8 +1099,8 @@ cudaError_t launch_t(const Params& p, const Shape& sh, const Maps& m, cudaStream
     if (e != cudaSuccess) return e;
     configured = kSmemBudget;
   }
-  kern<<<p.grid, kThreads, sh.smem_bytes, stream>>>(p, sh, m.k, m.v, m.ks, m.vs);
-  return cudaGetLastError();
+  return launch_split(p, kern, dim3(p.grid), dim3(kThreads), sh.smem_bytes, stream, p, sh, m.k,
+                      m.v, m.ks, m.vs);
 }
 
 // 8-bit caches: q dtype x per-token scales or not.

@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p
 
   const PlanResult plan = compute_plan(p, red);
   allow_dependent_launch();
+  wait_prior_grid();   // a KV append launched just before may still be writing rows
   SegmentIter it;
   it.init(p, plan);
 
@@ -225,8 +226,7 @@ cudaError_t launch_t(const Params& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<p.grid, kSimtThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_split(p, kern, dim3(p.grid), dim3(kSimtThreads), smem, stream, p);
 }
 
 template <int D>

@@ -238,3 +238,7 @@ def decode_attention_raw(*args, **kwargs):
 def decode_attention(w, pairs=None, nthreads: int = 0, want_weights: bool = False):
     return default().decode_attention(w, pairs=pairs, nthreads=nthreads,
                                       want_weights=want_weights)
+
+
+def append_kv(w, k_new, v_new, positions):
+    return default().append_kv(w, k_new, v_new, positions)

@@ -108,6 +108,50 @@ def test_scaled_host_validation(fda, kind, ks, vs, kvdt, status):
     assert _call_scaled(fda, kind, ks, vs, kvdt) == status
 
 
+def _call_append(fda, **over):
+    """fd_append_kv with fake pointers; only argument errors are asked for."""
+    a = dict(kn=0x1000, vn=0x2000, k=0x3000, v=0x4000, kv_start=0x5000, bt=None, bt_stride=0,
+             pos=0x6000, kv_rows=100, batch=2, kvh=2, d=128, page=0, ks=1.0, vs=1.0, kind=0,
+             kss=None, vss=None, ndt=0, kvdt=2, ws=0x8000, wsb=256)
+    a.update(over)
+    return fda.load_library().fd_append_kv(
+        a["kn"], a["vn"], a["k"], a["v"], a["kv_start"], a["bt"], a["bt_stride"], a["pos"],
+        a["kv_rows"], a["batch"], a["kvh"], a["d"], a["page"], a["ks"], a["vs"], a["kind"],
+        a["kss"], a["vss"], a["ndt"], a["kvdt"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(kn=None), 1),
+    (dict(pos=None), 1),
+    (dict(k=None), 1),
+    (dict(ws=None), 1),
+    (dict(kn=0x1008), 1),                                  # k_new not 16-byte aligned
+    (dict(kv_start=None), 1),                              # no layout
+    (dict(bt=0x9000, bt_stride=2, page=16), 1),            # both layouts
+    (dict(ks=0.0), 1),                                     # 8-bit codes divide by the scale
+    (dict(vs=-1.0), 1),
+    (dict(ks=float("inf")), 1),
+    (dict(ndt=2), 1),                                      # new rows cannot be e4m3
+    (dict(ndt=0, kvdt=1), 2),                              # f16 rows into a bf16 cache
+    (dict(d=96), 2),
+    (dict(kind=2, kvdt=0, kss=0xA000, vss=0xB000), 2),     # finer scales on an f16 cache
+    (dict(kind=1), 1),                                     # head scales missing
+    (dict(wsb=128), 3),                                    # workspace below the header
+    (dict(batch=0), 1),
+])
+def test_append_host_validation(fda, over, status):
+    assert _call_append(fda, **over) == status
+
+
+def test_decode_with_append_validates_the_append(fda):
+    """fd_decode_attention_append refuses a missing new row before any launch."""
+    lib = fda.load_library()
+    st = lib.fd_decode_attention_append(0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, None, 0,
+                                        0x6000, 0x7000, 100, 2, 8, 2, 128, 0, 0.125, 1.0, 1.0, 0,
+                                        None, None, 0, 2, 0x8000, 0x9000, 0xA000, 1 << 20, None)
+    assert st == 1
+
+
 def test_set_kernel_rejects_unknown(fda):
     assert fda.load_library().fd_set_kernel(7) == 1
     assert fda.load_library().fd_set_kernel(0) == 0
