@@ -68,6 +68,9 @@ class Workload:
     scale_kind: int = 0
     k_scales: Optional[np.ndarray] = None
     v_scales: Optional[np.ndarray] = None
+    # query tokens per sequence: q is [B, QH, q_len, D] when q_len > 1 (the
+    # last q_len tokens of each sequence, causal among themselves)
+    q_len: int = 1
 
     @property
     def paged(self) -> bool:
@@ -94,7 +97,7 @@ class Workload:
         B, QH, KVH, D = self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim
         total = int(self.seq_len.astype(np.int64).sum())
         kv = total * KVH * D * self.kv_elem_bytes * 2
-        qo = 2 * B * QH * D * 2
+        qo = 2 * B * QH * self.q_len * D * 2
         if self.paged:
             pages = int(sum((int(t) + self.page_size - 1) // self.page_size for t in self.seq_len))
             idx = 4 * B + 4 * pages
@@ -175,11 +178,12 @@ def _quantise_pair(k: np.ndarray, v: np.ndarray, kv_dtype: str):
 def make_contiguous(name: str, seed: int, seq_len, num_q_heads: int, num_kv_heads: int,
                     head_dim: int, q_dtype: str, kv_dtype: str, softmax_scale=None,
                     gap: int = 0, lead: int = 0, tail: int = 0,
-                    rng: Optional[np.random.Generator] = None) -> Workload:
+                    rng: Optional[np.random.Generator] = None, q_len: int = 1) -> Workload:
     """Token-major contiguous cache.  ``gap`` poisoned rows separate consecutive
     sequences, ``lead``/``tail`` poisoned rows sit before the first and after the
     last one.  With all three zero, ``kv_start_idx`` is the exclusive prefix sum
-    of ``seq_len``."""
+    of ``seq_len``.  ``q_len`` > 1 draws q as [B, QH, q_len, D] (the same
+    stream of draws as q_len = 1 extended)."""
     if rng is None:
         rng = np.random.Generator(np.random.PCG64(seed))
     seq_len = np.asarray(seq_len, dtype=np.int32)
@@ -189,7 +193,9 @@ def make_contiguous(name: str, seed: int, seq_len, num_q_heads: int, num_kv_head
         softmax_scale = 1.0 / math.sqrt(D)
     total = int(seq_len.astype(np.int64).sum())
 
-    q32 = rng.standard_normal((B, QH, D), dtype=np.float32)
+    q32 = rng.standard_normal((B, QH, q_len, D), dtype=np.float32)
+    if q_len == 1:
+        q32 = q32.reshape(B, QH, D)
     k32 = rng.standard_normal((total, KVH, D), dtype=np.float32)
     v32 = rng.standard_normal((total, KVH, D), dtype=np.float32)
     q = _cast16(q32, q_dtype)
@@ -216,7 +222,7 @@ def make_contiguous(name: str, seed: int, seq_len, num_q_heads: int, num_kv_head
                     q_dtype=q_dtype, kv_dtype=kv_dtype,
                     softmax_scale=np.float32(softmax_scale), k_scale=k_scale, v_scale=v_scale,
                     seq_len=seq_len, q=q, k_cache=k_cache, v_cache=v_cache,
-                    page_size=0, kv_start_idx=starts, block_table=None)
+                    page_size=0, kv_start_idx=starts, block_table=None, q_len=q_len)
 
 
 def to_paged(w: Workload, page_size: int, seed: int, oversize: float = 1.2,
@@ -376,6 +382,19 @@ def long_mqa(batch: int = 4, seq: int = 131072, kv_dtype: str = "e4m3") -> Workl
     (``kv_dtype='i8'``: the same draws quantised to INT8)."""
     return make_contiguous(f"long-mqa-fp8-B{batch}-T{seq}{_kv_tag(kv_dtype)}", 4, [seq] * batch,
                            16, 1, 128, "f16", kv_dtype)
+
+
+def with_q_len(w: Workload, q_len: int, seed: int) -> Workload:
+    """The workload as a verify step of ``q_len`` query tokens per sequence
+    (speculative decoding): the caches and lengths stay, and q is redrawn as
+    [B, QH, q_len, D] from its own seed (the last q_len cached tokens of each
+    sequence are the new ones)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q32 = rng.standard_normal((w.batch, w.num_q_heads, q_len, w.head_dim), dtype=np.float32)
+    q = _cast16(q32, w.q_dtype)
+    if q_len == 1:
+        q = q.reshape(w.batch, w.num_q_heads, w.head_dim)
+    return dataclasses.replace(w, name=w.name + f"-q{q_len}", q=q, q_len=q_len)
 
 
 CONFIGS = {

@@ -69,10 +69,10 @@ class Oracle:
         lib.fdo_bf16_value.restype = ctypes.c_double
         lib.fdo_bf16_value.argtypes = [ctypes.c_uint16]
         vp = ctypes.c_void_p
-        lib.fdo_decode_attention.restype = ctypes.c_int
-        lib.fdo_decode_attention.argtypes = [
+        lib.fdo_decode_attention_q.restype = ctypes.c_int
+        lib.fdo_decode_attention_q.argtypes = [
             vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int64,
-            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_double, ctypes.c_double, ctypes.c_double,
             ctypes.c_int, vp, vp,
             vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp]
@@ -137,13 +137,15 @@ class Oracle:
                              v_scale, kv_start_idx=None, block_table=None, page_size=0,
                              kv_rows=None, pairs: Optional[Sequence[Tuple[int, int]]] = None,
                              nthreads: int = 0, want_weights: bool = False, scale_kind: int = 0,
-                             k_scales=None, v_scales=None):
+                             k_scales=None, v_scales=None, q_len: int = 1):
         """Oracle on raw arrays.  Returns (out [B,QH,D] f64, lse [B,QH] f64,
         weights [B,QH,maxT] or None, threads used).  With ``pairs`` only those
         (b, qh) rows are computed; the rest of ``out``/``lse`` stays NaN.
         ``scale_kind`` 1 (per KV head, arrays [KVH]) or 2 (per token, arrays
         [kv_rows, KVH]) multiplies K and V elements by ``k_scales`` and
-        ``v_scales`` on top of ``k_scale`` and ``v_scale``."""
+        ``v_scales`` on top of ``k_scale`` and ``v_scale``.  With ``q_len`` > 1,
+        q is [B, QH, q_len, D] (the last q_len tokens of each sequence, causal
+        among themselves) and out / lse / weights carry a q_len axis after QH."""
         q = np.ascontiguousarray(q)
         k_cache = np.ascontiguousarray(k_cache)
         v_cache = np.ascontiguousarray(v_cache)
@@ -158,13 +160,14 @@ class Oracle:
         if kv_rows is None:
             kv_rows = (k_cache.shape[0] * k_cache.shape[1]) if block_table is not None \
                 else k_cache.shape[0]
-        out = np.full((B, num_q_heads, head_dim), np.nan, np.float64)
-        lse = np.full((B, num_q_heads), np.nan, np.float64)
+        qax = (q_len,) if q_len > 1 else ()
+        out = np.full((B, num_q_heads) + qax + (head_dim,), np.nan, np.float64)
+        lse = np.full((B, num_q_heads) + qax, np.nan, np.float64)
         weights = None
         wstride = 0
         if want_weights:
             wstride = max(1, int(seq_len.max()) if B else 1)
-            weights = np.zeros((B, num_q_heads, wstride), np.float64)
+            weights = np.zeros((B, num_q_heads) + qax + (wstride,), np.float64)
         pairs_arr = None
         n_pairs = 0
         if pairs is not None:
@@ -176,10 +179,10 @@ class Oracle:
         else:
             k_scales = v_scales = None
         used = ctypes.c_int(0)
-        rc = self.lib.fdo_decode_attention(
+        rc = self.lib.fdo_decode_attention_q(
             _ptr(q), _DTYPES[q_dtype], _ptr(k_cache), _ptr(v_cache), _DTYPES[kv_dtype],
             _ptr(kv_start_idx), _ptr(block_table), bt_stride, _ptr(seq_len), int(kv_rows),
-            B, int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size),
+            B, int(q_len), int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size),
             float(softmax_scale), float(k_scale), float(v_scale),
             int(scale_kind), _ptr(k_scales), _ptr(v_scales),
             _ptr(pairs_arr), n_pairs, int(nthreads), _ptr(out), _ptr(lse), _ptr(weights),
@@ -197,7 +200,7 @@ class Oracle:
             kv_start_idx=w.kv_start_idx, block_table=w.block_table, page_size=w.page_size,
             kv_rows=w.kv_rows, pairs=pairs, nthreads=nthreads, want_weights=want_weights,
             scale_kind=getattr(w, "scale_kind", 0), k_scales=getattr(w, "k_scales", None),
-            v_scales=getattr(w, "v_scales", None))
+            v_scales=getattr(w, "v_scales", None), q_len=getattr(w, "q_len", 1))
         if want_weights:
             return out, lse, weights
         return out, lse

@@ -25,6 +25,13 @@
  *   out[d]   = sum_t (w_t / Z) * v_t[d]
  *   lse      = M + ln Z           (natural log of sum_t exp(s_t))
  *
+ * With q_len > 1 query tokens per sequence (fdo_decode_attention_q: a
+ * speculative-decoding verify batch, "Learn CUDA from scratch, chapter 15",
+ * section 15.21), the last q_len tokens of each sequence are the new ones:
+ * query token j (q[b][qh][j], j < q_len) sits at position T_b - q_len + j and
+ * attends over t = 0 .. T_b - q_len + j (its own and every earlier key), with
+ * the same definition; a query with no key gets out = 0 and lse = -inf.
+ *
  * Sources, by page and section:
  *  - scaled dot product, softmax and the weighted sum of V rows: "SGLang
  *    Prefill optimisation: dissecting FlashAttention kernel bottlenecks with
@@ -216,14 +223,15 @@ static double scale_at(int kind, const float *arr, int64_t row, int num_kv_heads
  * weights: NULL, or [B][QH][weights_stride] receiving w_t / Z.
  * threads_used: NULL, or receives the number of threads that ran.
  */
-int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const void *v_cache,
-                         int kv_dtype, const int32_t *kv_start_idx, const int32_t *block_table,
-                         int block_table_stride, const int32_t *seq_len, int64_t kv_rows,
-                         int batch, int num_q_heads, int num_kv_heads, int head_dim,
-                         int page_size, double softmax_scale, double k_scale, double v_scale,
-                         int scale_kind, const float *k_scales, const float *v_scales,
-                         const int32_t *pairs, int n_pairs, int nthreads, double *out,
-                         double *lse, double *weights, int weights_stride, int *threads_used) {
+int fdo_decode_attention_q(const void *q, int q_dtype, const void *k_cache, const void *v_cache,
+                           int kv_dtype, const int32_t *kv_start_idx, const int32_t *block_table,
+                           int block_table_stride, const int32_t *seq_len, int64_t kv_rows,
+                           int batch, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                           int page_size, double softmax_scale, double k_scale, double v_scale,
+                           int scale_kind, const float *k_scales, const float *v_scales,
+                           const int32_t *pairs, int n_pairs, int nthreads, double *out,
+                           double *lse, double *weights, int weights_stride, int *threads_used) {
+  if (q_len < 1) return FDO_BAD_ARG;
   if (!q || !k_cache || !v_cache || !seq_len || !out || !lse) return FDO_BAD_ARG;
   if ((kv_start_idx == NULL) == (block_table == NULL)) return FDO_BAD_ARG;
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return FDO_BAD_ARG;
@@ -259,69 +267,90 @@ int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const 
       continue;
     }
     int kvh = qh / group;
-    int T = seq_len[b];
-    double *o = out + ((size_t)b * num_q_heads + qh) * head_dim;
-    double *l = lse + (size_t)b * num_q_heads + qh;
-    if (T <= 0) {
-      for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
-      *l = -INFINITY;
-      continue;
-    }
-    double *s = (double *)malloc(sizeof(double) * (size_t)T);
-    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)T);
-    double *qv = (double *)malloc(sizeof(double) * (size_t)head_dim);
-    if (!s || !rows || !qv) {
-      free(s); free(rows); free(qv);
+    for (int j = 0; j < q_len; ++j) {
+      /* query token j sits at position seq_len - q_len + j and sees the keys up
+         to and including its own position */
+      int T = seq_len[b] - (q_len - 1 - j);
+      const size_t qi = ((size_t)b * num_q_heads + qh) * q_len + j;   /* [B][QH][q_len] */
+      double *o = out + qi * head_dim;
+      double *l = lse + qi;
+      if (T <= 0) {
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        *l = -INFINITY;
+        continue;
+      }
+      double *s = (double *)malloc(sizeof(double) * (size_t)T);
+      int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)T);
+      double *qv = (double *)malloc(sizeof(double) * (size_t)head_dim);
+      if (!s || !rows || !qv) {
+        free(s); free(rows); free(qv);
 #pragma omp atomic write
-      status = FDO_NO_MEMORY;
-      continue;
-    }
-    int bad = 0;
-    for (int d = 0; d < head_dim; ++d)
-      qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + d);
+        status = FDO_NO_MEMORY;
+        continue;
+      }
+      int bad = 0;
+      for (int d = 0; d < head_dim; ++d)
+        qv[d] = decode_elem(q, q_dtype, qi * head_dim + d);
 
-    /* scores s_t = softmax_scale * q . (k_scale * ks(t) * dec(k_t)) */
-    for (int t = 0; t < T && !bad; ++t) {
-      rows[t] = cache_row(kv_start_idx, block_table, block_table_stride, page_size, b, t, kv_rows);
-      if (rows[t] < 0) { bad = FDO_ROW_OUT_OF_RANGE; break; }
-      size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;
-      const double ks = k_scale * scale_at(scale_kind, k_scales, rows[t], num_kv_heads, kvh);
-      double dot = 0.0;
-      for (int d = 0; d < head_dim; ++d) {
-        double kd = decode_elem(k_cache, kv_dtype, base + d);
-        if (isnan(kd)) { bad = FDO_NAN_CODE; break; }
-        dot += qv[d] * (ks * kd);
-      }
-      s[t] = softmax_scale * dot;
-    }
-    if (!bad) {
-      /* two-pass softmax: max, then normalised exponentials */
-      double M = s[0];
-      for (int t = 1; t < T; ++t) if (s[t] > M) M = s[t];
-      double Z = 0.0;
-      for (int t = 0; t < T; ++t) { s[t] = exp(s[t] - M); Z += s[t]; }
-      for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+      /* scores s_t = softmax_scale * q . (k_scale * ks(t) * dec(k_t)) */
       for (int t = 0; t < T && !bad; ++t) {
-        double wt = s[t] / Z;
-        if (weights) weights[((size_t)b * num_q_heads + qh) * weights_stride + t] = wt;
+        rows[t] = cache_row(kv_start_idx, block_table, block_table_stride, page_size, b, t, kv_rows);
+        if (rows[t] < 0) { bad = FDO_ROW_OUT_OF_RANGE; break; }
         size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;
-        const double vs = v_scale * scale_at(scale_kind, v_scales, rows[t], num_kv_heads, kvh);
+        const double ks = k_scale * scale_at(scale_kind, k_scales, rows[t], num_kv_heads, kvh);
+        double dot = 0.0;
         for (int d = 0; d < head_dim; ++d) {
-          double vd = decode_elem(v_cache, kv_dtype, base + d);
-          if (isnan(vd)) { bad = FDO_NAN_CODE; break; }
-          o[d] += wt * (vs * vd);
+          double kd = decode_elem(k_cache, kv_dtype, base + d);
+          if (isnan(kd)) { bad = FDO_NAN_CODE; break; }
+          dot += qv[d] * (ks * kd);
         }
+        s[t] = softmax_scale * dot;
       }
-      *l = M + log(Z);
-    }
-    if (bad) {
+      if (!bad) {
+        /* two-pass softmax: max, then normalised exponentials */
+        double M = s[0];
+        for (int t = 1; t < T; ++t) if (s[t] > M) M = s[t];
+        double Z = 0.0;
+        for (int t = 0; t < T; ++t) { s[t] = exp(s[t] - M); Z += s[t]; }
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        for (int t = 0; t < T && !bad; ++t) {
+          double wt = s[t] / Z;
+          if (weights) weights[qi * weights_stride + t] = wt;
+          size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;
+          const double vs = v_scale * scale_at(scale_kind, v_scales, rows[t], num_kv_heads, kvh);
+          for (int d = 0; d < head_dim; ++d) {
+            double vd = decode_elem(v_cache, kv_dtype, base + d);
+            if (isnan(vd)) { bad = FDO_NAN_CODE; break; }
+            o[d] += wt * (vs * vd);
+          }
+        }
+        *l = M + log(Z);
+      }
+      if (bad) {
 #pragma omp atomic write
-      status = bad;
+        status = bad;
+      }
+      free(s); free(rows); free(qv);
     }
-    free(s); free(rows); free(qv);
   }
   if (threads_used) *threads_used = used;
   return status;
+}
+
+/* One query token per sequence (q_len = 1): q, out [B][QH][D], lse [B][QH]. */
+int fdo_decode_attention(const void *q, int q_dtype, const void *k_cache, const void *v_cache,
+                         int kv_dtype, const int32_t *kv_start_idx, const int32_t *block_table,
+                         int block_table_stride, const int32_t *seq_len, int64_t kv_rows,
+                         int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                         int page_size, double softmax_scale, double k_scale, double v_scale,
+                         int scale_kind, const float *k_scales, const float *v_scales,
+                         const int32_t *pairs, int n_pairs, int nthreads, double *out,
+                         double *lse, double *weights, int weights_stride, int *threads_used) {
+  return fdo_decode_attention_q(q, q_dtype, k_cache, v_cache, kv_dtype, kv_start_idx,
+                                block_table, block_table_stride, seq_len, kv_rows, batch, 1,
+                                num_q_heads, num_kv_heads, head_dim, page_size, softmax_scale,
+                                k_scale, v_scale, scale_kind, k_scales, v_scales, pairs, n_pairs,
+                                nthreads, out, lse, weights, weights_stride, threads_used);
 }
 
 /* fp32 value of a 16-bit element (f16 or bf16 bits); exact. */

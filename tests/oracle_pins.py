@@ -638,11 +638,58 @@ def pin_append_kv(orc):
         _check_append(orc, w, 60 + i)
 
 
+# ----------------------------------------------------------------------------
+# multi-token query (speculative verify): causal among the new tokens
+# ----------------------------------------------------------------------------
+
+def pin_multi_token_equals_truncated_single(orc):
+    """Query token j of q_len sees exactly the first T - (q_len - 1 - j)
+    keys: each token's result equals the one-token oracle on the sequence
+    cut there (bit for bit), with GQA, gaps, a paged pool, finer scales and
+    sequences shorter than q_len."""
+    base = fw.make_contiguous("mt", 88, [1, 2, 5, 40, 0, 130], 16, 4, 64, "f16", "e4m3", gap=2,
+                              q_len=4)
+    cases = [base, fw.with_scales(fw.to_paged(base, 8, 89), fw.SCALE_TOKEN, 90),
+             fw.with_q_len(fw.make_contiguous("mt2", 91, [3, 77], 8, 1, 128, "bf16", "bf16"), 3, 92)]
+    for w in cases:
+        L = w.q_len
+        out, lse = orc.decode_attention(w)
+        assert out.shape == (w.batch, w.num_q_heads, L, w.head_dim)
+        for j in range(L):
+            cut = np.maximum(w.seq_len.astype(np.int64) - (L - 1 - j), 0).astype(np.int32)
+            wj = dataclasses.replace(w, q=np.ascontiguousarray(w.q[:, :, j]), q_len=1, seq_len=cut)
+            o1, l1 = orc.decode_attention(wj)
+            assert np.array_equal(out[:, :, j], o1), (w.name, j)
+            assert np.array_equal(lse[:, :, j], l1), (w.name, j)
+
+
+def pin_multi_token_closed_form(orc):
+    """All keys new (T = q_len) and identical: token j's weights are uniform
+    over keys 0..j, so out_j = mean(v_0..v_j) and lse_j = s + ln(j + 1)."""
+    rng = np.random.default_rng(93)
+    L, D = 5, 64
+    q = rng.standard_normal((1, 2, L, D))
+    k = np.repeat(rng.standard_normal((1, 1, D)), L, axis=0)
+    v = rng.standard_normal((L, 1, D))
+    w = custom(q.reshape(1, 2 * L, D), k, v, [L], softmax_scale=0.125)
+    w = dataclasses.replace(w, q=w.q.reshape(1, 2, L, D), num_q_heads=2, q_len=L)
+    out, lse = orc.decode_attention(w)
+    qf = lib_decode(w.q, "f16").reshape(2, L, D)
+    kf = lib_decode(w.k_cache, "f16")[0, 0]
+    vf = lib_decode(w.v_cache, "f16")[:, 0]
+    for h in range(2):
+        for j in range(L):
+            _close(out[0, h, j], vf[: j + 1].mean(axis=0), 1e-14, 1e-15, "multi-token mean")
+            _close(lse[0, h, j], 0.125 * float(qf[h, j] @ kf) + math.log(j + 1), 1e-13, 1e-14,
+                   "multi-token lse")
+
+
 ALL_PINS = [
     pin_e4m3_codes, pin_i8_codes, pin_i8_materialized, pin_i8_single_key_all_codes, pin_f16_codes, pin_bf16_codes, pin_identical_v_rows, pin_single_key,
     pin_zero_query, pin_identical_k_rows, pin_two_keys, pin_dominant_key, pin_empty_sequence,
     pin_weights_sum_to_one, pin_key_permutation, pin_gqa_equals_replicated_mha,
     pin_paged_equals_contiguous, pin_scale_factors, pin_score_shift, pin_online_recurrence,
     pin_head_scales_materialized, pin_token_scales_materialized, pin_token_scales_single_key,
-    pin_e4m3_encoder, pin_i8_encoder, pin_append_kv,
+    pin_e4m3_encoder, pin_i8_encoder, pin_append_kv, pin_multi_token_equals_truncated_single,
+    pin_multi_token_closed_form,
 ]

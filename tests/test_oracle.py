@@ -36,8 +36,8 @@ MUTATIONS = [
      "else mag = ldexp(1.0 + (double)m / 256.0, e - 127);", "bf16 mantissa"),
     ("for (int t = 0; t < T; ++t) { s[t] = exp(s[t] - M); Z += s[t]; }",
      "for (int t = 0; t < T; ++t) { s[t] = exp(s[t] - M); Z += s[t] * s[t]; }", "wrong sum"),
-    ("size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;\n        const double vs",
-     "size_t base = ((size_t)rows[t] * num_kv_heads + 0) * head_dim;\n        const double vs",
+    ("size_t base = ((size_t)rows[t] * num_kv_heads + kvh) * head_dim;\n          const double vs",
+     "size_t base = ((size_t)rows[t] * num_kv_heads + 0) * head_dim;\n          const double vs",
      "V read from head 0"),
     ("if (kind == FDO_SCALE_HEAD) return (double)arr[kvh];",
      "if (kind == FDO_SCALE_HEAD) return (double)arr[0];", "head scale of head 0"),
@@ -65,8 +65,15 @@ MUTATIONS = [
      "token scale from the first element"),
     ("        const float denom = qmax * scale;", "        const float denom = qmax;",
      "token scale ignores the per-tensor scale"),
-    ("qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + d);",
-     "qv[d] = decode_elem(q, q_dtype, ((size_t)b * num_q_heads + qh) * head_dim + (head_dim - 1 - d));",
+    ("int T = seq_len[b] - (q_len - 1 - j);", "int T = seq_len[b] - (q_len - j);",
+     "causal limit one key short"),
+    ("int T = seq_len[b] - (q_len - 1 - j);", "int T = seq_len[b];",
+     "new tokens see every key"),
+    ("const size_t qi = ((size_t)b * num_q_heads + qh) * q_len + j;",
+     "const size_t qi = ((size_t)b * num_q_heads + qh) * q_len + (q_len - 1 - j);",
+     "query tokens reversed"),
+    ("qv[d] = decode_elem(q, q_dtype, qi * head_dim + d);",
+     "qv[d] = decode_elem(q, q_dtype, qi * head_dim + (head_dim - 1 - d));",
      "q transposed"),
 ]
 
