@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--kv", default="e4m3", choices=["e4m3", "i8"],
                     help="8-bit K/V format of the FP8 workloads (configs 3-5): e4m3, or the same "
                          "draws quantised to INT8 (symmetric, amax/127)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per sequence (a speculative-decoding verify step: the "
+                         "last q_len cached tokens, causal among themselves)")
     ap.add_argument("--append", action="store_true",
                     help="the step also writes each sequence's last token (its K/V rows, "
                          "quantised for 8-bit caches) before attending, in one call")
@@ -94,7 +97,7 @@ def oracle_sample(w: fw.Workload, budget_s: float):
     threads = 0
     nseq = 0
     heads = w.num_q_heads
-    per_seq_qo = 2 * heads * w.head_dim * 2
+    per_seq_qo = 2 * heads * w.q_len * w.head_dim * 2
     for b in range(w.batch):
         pairs = [(b, h) for h in range(heads)]
         t0 = time.perf_counter()
@@ -103,7 +106,7 @@ def oracle_sample(w: fw.Workload, budget_s: float):
             w.num_kv_heads, w.head_dim, w.softmax_scale, w.k_scale, w.v_scale,
             kv_start_idx=w.kv_start_idx, block_table=w.block_table, page_size=w.page_size,
             kv_rows=w.kv_rows, pairs=pairs, scale_kind=w.scale_kind, k_scales=w.k_scales,
-            v_scales=w.v_scales)
+            v_scales=w.v_scales, q_len=w.q_len)
         elapsed += time.perf_counter() - t0
         T = int(w.seq_len[b])
         idx = (4 + 4 * (-(-T // w.page_size))) if w.paged else 8
@@ -124,6 +127,10 @@ def make_workload(args) -> fw.Workload:
         w = fw.CONFIGS[args.config](kv_dtype=args.kv)
     else:
         w = fw.CONFIGS[args.config]()
+    if args.q_len > 1:
+        if args.append:
+            raise SystemExit("--append takes one query token per sequence")
+        w = fw.with_q_len(w, args.q_len, 540 + args.config)
     if args.shared_prefix:
         if not w.paged:
             raise SystemExit("--shared-prefix needs a paged workload")
@@ -142,6 +149,8 @@ def workload_config(args) -> dict:
         c["shared_prefix_tokens"] = args.shared_prefix
     if args.kv != "e4m3":
         c["kv_dtype"] = f"{args.kv} (the workload's draws quantised to INT8, per-tensor amax/127)"
+    if args.q_len > 1:
+        c["q_len"] = args.q_len
     if args.append:
         c["append"] = ("each step first writes every sequence's last token (K/V rows of the "
                        "projection dtype, quantised for 8-bit caches) into the cache, then "
@@ -318,10 +327,10 @@ def run_gpu(args):
     t = fw.to_torch(w, dev)
     B, QH, KVH, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
     out = torch.empty_like(t["q"])
-    lse = torch.empty((B, QH), dtype=torch.float32, device=dev)
-    ws = fda.alloc_workspace(B, QH, KVH, D, dev)
+    lse = torch.empty(t["q"].shape[:-1], dtype=torch.float32, device=dev)
+    ws = fda.alloc_workspace(B, QH * w.q_len, KVH, D, dev)
     stream = torch.cuda.current_stream(dev)
-    sel = fda.fd_selected_kernel(QH, KVH, D, 0 if w.q_dtype == "f16" else 1,
+    sel = fda.fd_selected_kernel(QH * w.q_len, KVH, D, 0 if w.q_dtype == "f16" else 1,
                                  fda.DTYPE_CODES[w.kv_dtype], w.paged,
                                  max(w.page_size, 1))
     kname = {1: "simt", 2: "mma"}.get(sel, "none")
@@ -334,6 +343,12 @@ def run_gpu(args):
         t["positions"] = torch.from_numpy(fw.last_positions(w)).to(dev)
 
     def step():
+        if w.q_len > 1:
+            fda.fd_decode_attention_multi(
+                t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
+                w.kv_rows, QH, KVH, D, w.page_size, float(w.softmax_scale), float(w.k_scale),
+                float(w.v_scale), w.scale_kind, t["k_scales"], t["v_scales"], out, lse, ws, stream)
+            return
         if args.append:
             fda.fd_decode_attention_append(
                 t["q"], t["k_new"], t["v_new"], t["k"], t["v"], t["kv_start_idx"],

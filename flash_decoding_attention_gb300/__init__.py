@@ -52,7 +52,7 @@ EXPORTED = [
     "fd_workspace_bytes", "fd_decode_attention", "fd_check_device_error", "fd_status_string",
     "fd_set_kernel", "fd_selected_kernel", "fd_set_split_events", "fd_debug_read_plan",
     "fd_debug_gather_kv", "fd_decode_attention_noalloc", "fd_decode_attention_scaled",
-    "fd_append_kv", "fd_decode_attention_append",
+    "fd_append_kv", "fd_decode_attention_append", "fd_decode_attention_multi",
 ]
 
 
@@ -88,6 +88,10 @@ def load_library(path: Optional[str] = None):
         lib.fd_decode_attention_scaled.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32,
                                                    i32, i32, f32, f32, f32, i32, vp, vp, i32, i32,
                                                    vp, vp, vp, sz, vp]
+        lib.fd_decode_attention_multi.restype = i32
+        lib.fd_decode_attention_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32,
+                                                  i32, i32, i32, f32, f32, f32, i32, vp, vp, i32,
+                                                  i32, vp, vp, vp, sz, vp]
         lib.fd_append_kv.restype = i32
         lib.fd_append_kv.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, i32, f32,
                                      f32, i32, vp, vp, i32, i32, vp, sz, vp]
@@ -212,6 +216,32 @@ def fd_decode_attention_scaled(q, k_cache, v_cache, kv_start_idx, block_table, s
         _stream_handle(stream))
     if check and st != FD_OK:
         raise FdError(st, "fd_decode_attention_scaled")
+    return st
+
+
+def fd_decode_attention_multi(q, k_cache, v_cache, kv_start_idx, block_table, seq_len,
+                              kv_rows: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                              page_size: int, softmax_scale: float, k_scale: float,
+                              v_scale: float, scale_kind: int, k_scales, v_scales, out, lse,
+                              workspace, stream=None, q_dtype: Optional[int] = None,
+                              kv_dtype: Optional[int] = None, check: bool = True) -> int:
+    """q_len query tokens per sequence (q, out: [B, QH, q_len, D]; lse
+    [B, QH, q_len]), causal among the last q_len tokens of each sequence."""
+    lib = load_library()
+    batch = int(seq_len.shape[0])
+    q_len = int(q.shape[2])
+    stride = int(block_table.shape[1]) if block_table is not None else 0
+    st = lib.fd_decode_attention_multi(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_start_idx), _ptr(block_table), stride,
+        _ptr(seq_len), int(kv_rows), batch, q_len, int(num_q_heads), int(num_kv_heads),
+        int(head_dim), int(page_size), float(softmax_scale), float(k_scale), float(v_scale),
+        int(scale_kind), _ptr(k_scales), _ptr(v_scales),
+        _q_dtype(q) if q_dtype is None else int(q_dtype),
+        _kv_dtype(k_cache) if kv_dtype is None else int(kv_dtype),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    if check and st != FD_OK:
+        raise FdError(st, "fd_decode_attention_multi")
     return st
 
 
@@ -366,8 +396,13 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     (per token, by cache row), multiplying ``k_scale`` / ``v_scale``.  With
     ``k_new`` / ``v_new`` ([B, KVH, D], q's dtype) and ``positions`` (int32
     [B]) the step's new token is first written into the caches (quantised for
-    8-bit caches, per-token scales written), and ``seq_len`` counts it."""
-    B, QH, D = q.shape
+    8-bit caches, per-token scales written), and ``seq_len`` counts it.  A 4-d
+    ``q`` ([B, QH, q_len, D]) asks for q_len query tokens per sequence, the
+    last q_len cached tokens, causal among themselves (out and lse carry the
+    q_len axis too)."""
+    multi = q.dim() == 4              # [B, QH, q_len, D]: multi-token queries
+    B, QH, D = q.shape[0], q.shape[1], q.shape[-1]
+    q_len = q.shape[2] if multi else 1
     if block_table is not None:
         pages, P, KVH, D2 = k_cache.shape
         kv_rows = pages * P
@@ -380,10 +415,18 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, QH), dtype=torch.float32, device=q.device)
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     if workspace is None:
-        workspace = alloc_workspace(B, QH, KVH, D, q.device)
-    if k_new is not None:
+        workspace = alloc_workspace(B, QH * q_len, KVH, D, q.device)
+    if multi:
+        if k_new is not None:
+            raise ValueError("the KV append takes one query token per sequence")
+        kind = FD_SCALE_TENSOR if k_scales is None else (
+            FD_SCALE_HEAD if k_scales.dim() == 1 else FD_SCALE_TOKEN)
+        fd_decode_attention_multi(q, k_cache, v_cache, kv_start_idx, block_table, seq_len,
+                                  kv_rows, QH, KVH, D, P, softmax_scale, k_scale, v_scale, kind,
+                                  k_scales, v_scales, out, lse, workspace, stream)
+    elif k_new is not None:
         kind = FD_SCALE_TENSOR if k_scales is None else (
             FD_SCALE_HEAD if k_scales.dim() == 1 else FD_SCALE_TOKEN)
         fd_decode_attention_append(q, k_new, v_new, k_cache, v_cache, kv_start_idx, block_table,

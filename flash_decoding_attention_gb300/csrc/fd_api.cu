@@ -236,7 +236,13 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
                              fd_scale_kind scale_kind, const float* k_scales,
                              const float* v_scales, fd_dtype q_dtype, fd_dtype kv_dtype, void* out,
                              float* lse, void* workspace, size_t workspace_bytes,
-                             fd_stream_t stream, const AppendArgs* app) {
+                             fd_stream_t stream, const AppendArgs* app, int q_len = 1) {
+  // q_len query tokens per sequence run as q_len virtual query heads per head
+  if (q_len < 1 || q_len > 16 || (app && q_len != 1)) return FD_ERR_INVALID_ARG;
+  if (num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
+      (num_q_heads / num_kv_heads) * q_len > 128)
+    return FD_ERR_UNSUPPORTED;
+  const int virt_heads = num_q_heads * q_len;
   if (scale_kind != FD_SCALE_TENSOR && scale_kind != FD_SCALE_HEAD &&
       scale_kind != FD_SCALE_TOKEN)
     return FD_ERR_INVALID_ARG;
@@ -275,7 +281,7 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
   const int sms = current_sms();
   if (sms <= 0) return FD_ERR_CUDA;
   Config c;
-  if (!choose(g_kernel.load(), num_q_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, paged,
+  if (!choose(g_kernel.load(), virt_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, paged,
               page_size, sms, &c))
     return FD_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(batch * c.hg, c.grid, c.hq, head_dim);
@@ -299,12 +305,13 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
   p.kv_rows = kv_rows;
   p.bt_stride = paged ? block_table_stride : 0;
   p.batch = batch;
-  p.num_q_heads = num_q_heads;
+  p.num_q_heads = virt_heads;
   p.num_kv_heads = num_kv_heads;
   p.head_dim = head_dim;
   p.page_size = paged ? page_size : 1;
   p.page_shift = paged ? log2i(page_size) : 0;
-  p.group = num_q_heads / num_kv_heads;
+  p.group = virt_heads / num_kv_heads;
+  p.q_len = q_len;
   p.hc = c.hc;
   p.hg = c.hg;
   p.hq = c.hq;
@@ -350,6 +357,22 @@ fd_status fd_decode_attention_scaled(const void* q, const void* k_cache, const v
                      kv_rows, batch, num_q_heads, num_kv_heads, head_dim, page_size,
                      softmax_scale, k_scale, v_scale, scale_kind, k_scales, v_scales, q_dtype,
                      kv_dtype, out, lse, workspace, workspace_bytes, stream, nullptr);
+}
+
+fd_status fd_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* kv_start_idx, const int32_t* block_table,
+                                    int block_table_stride, const int32_t* seq_len,
+                                    int64_t kv_rows, int batch, int q_len, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int page_size,
+                                    float softmax_scale, float k_scale, float v_scale,
+                                    fd_scale_kind scale_kind, const float* k_scales,
+                                    const float* v_scales, fd_dtype q_dtype, fd_dtype kv_dtype,
+                                    void* out, float* lse, void* workspace,
+                                    size_t workspace_bytes, fd_stream_t stream) {
+  return decode_impl(q, k_cache, v_cache, kv_start_idx, block_table, block_table_stride, seq_len,
+                     kv_rows, batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                     softmax_scale, k_scale, v_scale, scale_kind, k_scales, v_scales, q_dtype,
+                     kv_dtype, out, lse, workspace, workspace_bytes, stream, nullptr, q_len);
 }
 
 fd_status fd_decode_attention_append(const void* q, const void* k_new, const void* v_new,

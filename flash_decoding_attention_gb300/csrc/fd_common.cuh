@@ -95,6 +95,11 @@ struct Params {
   const float* k_scales;     // FD_SCALE_HEAD: [KVH]; FD_SCALE_TOKEN: [kv_rows][KVH]
   const float* v_scales;
   int pdl;                   // split kernel launched as a programmatic dependent (of the append)
+  // Query tokens per sequence.  With q_len > 1 the kernels see q_len virtual
+  // query heads per query head (num_q_heads and group above already count
+  // them): virtual head v = qh * q_len + j is token j of query head qh, and
+  // it attends to the first T - (q_len - 1 - j) keys of its sequence.
+  int q_len;
   // KV append (fd_append.cu); q_dtype is the dtype of k_new / v_new
   const void* k_new;         // [batch][KVH][D]
   const void* v_new;

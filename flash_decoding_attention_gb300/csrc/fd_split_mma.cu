@@ -575,6 +575,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // local query heads (within the stream) of rows r and r + 8
     const int h0 = mtile * 16 + r, h1 = h0 + 8;
     const bool v0 = h0 < G, v1 = h1 < G;
+    // multi-token queries: rows r and r + 8 stop this many keys before the
+    // sequence's end (0 for one query token per sequence)
+    const int cut0 = p.q_len - 1 - h0 % p.q_len, cut1 = p.q_len - 1 - h1 % p.q_len;
     const int li0 = kvl * G + h0, li1 = kvl * G + h1;   // slot rows
     // this head tile's Q fragments in shared memory: [kk][lane] x 16 bytes
     const uint32_t qf = qfrag0 + (uint32_t)ht * KSTEPS * 512 + lane * 16;
@@ -644,6 +647,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sub = ts * SUB * sh.r + SUB * rr;   // first token of the sub-tile in the tile
             const int left = seg.t_end - (t0 + sub);      // valid tokens from the sub-tile start
             if (left <= 0) break;
+            // valid keys of rows r and r + 8 from the sub-tile start: the
+            // segment's end, and for multi-token queries the causal limit
+            int left0 = left, left1 = left;
+            if (p.q_len > 1) {
+              const int tail = seg.T - (t0 + sub);
+              left0 = min(left, tail - cut0);
+              left1 = min(left, tail - cut1);
+            }
+            const bool edge = min(left0, left1) < SUB;
             // ---- S = Q K^T over NJ n-tiles of 8 tokens.  Each Q fragment is
             //      read from shared memory once and used for every n-tile.
             float s[NJ][4];
@@ -726,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tok = 8 * jn + 2 * q + (e & 1);
                 float v = s[jn][e] * sc;
                 if constexpr (TOK) v *= (e & 1) ? kk2.y : kk2.x;
-                if (left < SUB && tok >= left) v = -INFINITY;   // ragged end of the segment
+                if (edge && tok >= ((e & 2) ? left1 : left0)) v = -INFINITY;   // ragged end
                 pr[jn][e] = v;
               }
               mx0 = fmaxf(mx0, fmaxf(pr[jn][0], pr[jn][1]));

@@ -128,6 +128,11 @@ __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p
 
     float qv[kSimtMaxGroup][DPL];
     float m[kSimtMaxGroup], l[kSimtMaxGroup], acc[kSimtMaxGroup][DPL];
+    // keys each (virtual) head attends to: all T, or for multi-token queries
+    // up to its token's own position
+    int lim[kSimtMaxGroup];
+#pragma unroll
+    for (int i = 0; i < kSimtMaxGroup; ++i) lim[i] = seg.T - (p.q_len - 1 - (qh0 + i) % p.q_len);
 #pragma unroll
     for (int i = 0; i < kSimtMaxGroup; ++i) {
       m[i] = -INFINITY;
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p
       }
 #pragma unroll
       for (int i = 0; i < kSimtMaxGroup; ++i) {
-        if (i < G) {
+        if (i < G && t < lim[i]) {
           float s = 0.f;
 #pragma unroll
           for (int j = 0; j < DPL; ++j) s = fmaf(qv[i][j], kf[j], s);

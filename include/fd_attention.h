@@ -94,7 +94,8 @@ typedef enum {
  * device (host function, no device work).  Returns 0 for invalid sizes.
  * The figure covers the partial (m, l, acc) states of the split phase, the
  * per-stream tile prefix of the split plan and a 256-byte header; it grows
- * with the device's SM count, not with sequence lengths.
+ * with the device's SM count, not with sequence lengths.  For
+ * fd_decode_attention_multi pass num_q_heads * q_len as num_q_heads.
  */
 size_t fd_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim);
 
@@ -176,6 +177,36 @@ fd_status fd_decode_attention_scaled(const void *q, const void *k_cache, const v
                                      const float *v_scales, fd_dtype q_dtype, fd_dtype kv_dtype,
                                      void *out, float *lse, void *workspace,
                                      size_t workspace_bytes, fd_stream_t stream);
+
+/*
+ * Decode attention for q_len query tokens per sequence (a speculative-decoding
+ * verify batch, "Learn CUDA from scratch, chapter 15", section 15.21: the
+ * target model checks q_len drafted tokens in one pass).  The last q_len
+ * tokens of each sequence are the new ones and are already in the cache
+ * (seq_len counts them): query token j (0 <= j < q_len) sits at position
+ * seq_len[b] - q_len + j and attends to keys 0 .. seq_len[b] - q_len + j, its
+ * own and every earlier one (causal among the new tokens), with the
+ * definition of fd_decode_attention.  A query with no key (seq_len[b] <
+ * q_len - j) gets out = 0 and lse = -inf.
+ *
+ * q, out  [batch, num_q_heads, q_len, head_dim] of q_dtype (head-major: the
+ *         q_len tokens of one head are adjacent rows).
+ * lse     fp32 [batch, num_q_heads, q_len], or NULL.
+ * q_len   1 .. 16, with (num_q_heads / num_kv_heads) * q_len <= 128 (else
+ *         FD_ERR_UNSUPPORTED); q_len = 1 equals fd_decode_attention_scaled.
+ * workspace_bytes >= fd_workspace_bytes(batch, num_q_heads * q_len, ...).
+ * Every other argument as for fd_decode_attention_scaled.
+ */
+fd_status fd_decode_attention_multi(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *kv_start_idx, const int32_t *block_table,
+                                    int block_table_stride, const int32_t *seq_len,
+                                    int64_t kv_rows, int batch, int q_len, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int page_size,
+                                    float softmax_scale, float k_scale, float v_scale,
+                                    fd_scale_kind scale_kind, const float *k_scales,
+                                    const float *v_scales, fd_dtype q_dtype, fd_dtype kv_dtype,
+                                    void *out, float *lse, void *workspace,
+                                    size_t workspace_bytes, fd_stream_t stream);
 
 /*
  * KV-cache append of one new token per sequence ("Learn CUDA from scratch,

@@ -27,10 +27,17 @@ def run(w: fw.Workload, kernel: int = 0, workspace=None, stream=None, check_erro
     try:
         t = fw.to_torch(w, "cuda")
         out = torch.full(t["q"].shape, float("nan"), dtype=t["q"].dtype, device="cuda")
-        lse = torch.full(t["q"].shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+        lse = torch.full(t["q"].shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
         if workspace is None:
-            workspace = fda.alloc_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim)
-        if w.scale_kind:
+            workspace = fda.alloc_workspace(w.batch, w.num_q_heads * w.q_len, w.num_kv_heads,
+                                            w.head_dim)
+        if w.q_len > 1:
+            fda.fd_decode_attention_multi(
+                t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
+                w.kv_rows, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
+                float(w.softmax_scale), float(w.k_scale), float(w.v_scale), w.scale_kind,
+                t["k_scales"], t["v_scales"], out, lse, workspace, stream)
+        elif w.scale_kind:
             fda.fd_decode_attention_scaled(
                 t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
                 w.kv_rows, w.num_q_heads, w.num_kv_heads, w.head_dim, w.page_size,
