@@ -66,6 +66,22 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def device_env(dev) -> dict:
+    """GPU name, SM count, L2 size, CUDA runtime and driver versions."""
+    import torch
+    prop = torch.cuda.get_device_properties(dev)
+    env = {"gpu": prop.name, "sms": prop.multi_processor_count,
+           "l2_bytes": prop.L2_cache_size, "cuda_runtime": torch.version.cuda,
+           "torch": torch.__version__}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                              "-i", str(dev.index or 0)], capture_output=True, text=True, timeout=20)
+        env["driver"] = out.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        env["driver"] = None
+    return env
+
+
 def max_over_ranks(value: float, device) -> float:
     """Largest value over the ranks of the default process group (the
     slowest replica sets the whole job's time)."""
@@ -86,7 +102,7 @@ def whole_job_throughput(units_per_rank: float, world: int, max_seconds: float) 
 # CPU baseline: the oracle as it stands, on the host cores
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w: fw.Workload, budget_s: float):
+def oracle_sample(w: fw.Workload, budget_s: float, nthreads: int = 0):
     """Times the oracle on whole sequences (all query heads) of the workload,
     taken in order until about `budget_s` seconds of wall time; returns
     (GB/s by the algorithmic-bytes formula, threads used, description)."""
@@ -106,7 +122,7 @@ def oracle_sample(w: fw.Workload, budget_s: float):
             w.num_kv_heads, w.head_dim, w.softmax_scale, w.k_scale, w.v_scale,
             kv_start_idx=w.kv_start_idx, block_table=w.block_table, page_size=w.page_size,
             kv_rows=w.kv_rows, pairs=pairs, scale_kind=w.scale_kind, k_scales=w.k_scales,
-            v_scales=w.v_scales, q_len=w.q_len)
+            v_scales=w.v_scales, q_len=w.q_len, nthreads=nthreads)
         elapsed += time.perf_counter() - t0
         T = int(w.seq_len[b])
         idx = (4 + 4 * (-(-T // w.page_size))) if w.paged else 8
@@ -268,12 +284,16 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def source_digest() -> str:
+# sources that make up each split kernel (its traffic changes only with them)
+KERNEL_SOURCES = {"mma": ("fd_common.cuh", "fd_split_mma.cu"),
+                  "simt": ("fd_common.cuh", "fd_split_simt.cu")}
+
+
+def source_digest(kernel_name: str = "mma") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "flash_decoding_attention_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES.get(kernel_name, ()):
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -301,7 +321,7 @@ def recorded_traffic(kernel_name: str, config: int):
     except ValueError:
         return None
     e = d.get(f"{kernel_name}/config{config}")
-    if not e or e.get("source_digest") != source_digest():
+    if not e or e.get("source_digest") != source_digest(kernel_name):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -417,7 +437,17 @@ def run_gpu(args):
         fda.fd_set_split_events(None, None)
         if (i + 1) % SYNC_EVERY == 0:
             torch.cuda.synchronize()
+    # diagnostic only: back-to-back steps without the L2 flush (inputs partly
+    # L2-resident from the previous step), events around the whole run
+    n_hot = min(K, 200)
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    h0.record(stream)
+    for i in range(n_hot):
+        step()
+    h1.record(stream)
+    torch.cuda.synchronize()
+    hot_us = h0.elapsed_time(h1) / n_hot * 1e3
     if pg:
         pg.barrier()
     clk = clocks.stop()
@@ -504,7 +534,11 @@ def run_gpu(args):
                    "l2": "flushed between steps (write then read of 2x L2 buffers, outside the "
                          "timed events)",
                    "parallelism": f"replicas x{world}"},
-        "gpu_launches": 4 * K,
+        # split + combine (+ append) per step: the headline loop, the
+        # roofline loop and the unflushed diagnostic
+        "gpu_launches": (3 if args.append else 2) * (2 * K + n_hot),
+        "diagnostic_unflushed_us_per_step": round(hot_us, 2),
+        "env": device_env(dev),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if (args.shared_prefix or args.scales != "tensor")
@@ -515,8 +549,10 @@ def run_gpu(args):
     }
     if not args.no_cpu_baseline and args.gpus == 1:
         gbs, threads, desc, _ = oracle_sample(w, budget_s=15.0)
+        gbs1, _, desc1, _ = oracle_sample(w, budget_s=3.0, nthreads=1)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
-                                "kind": "oracle", "sample": desc}
+                                "kind": "oracle", "sample": desc,
+                                "value_1thread": round(gbs1, 4), "sample_1thread": desc1}
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
