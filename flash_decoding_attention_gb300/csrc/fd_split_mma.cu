@@ -73,6 +73,7 @@ struct Shape {
   int stages;
   int merge_bytes;
   int qfrag_bytes;
+  int qrows;         // Q rows kept per head tile: 16, or 8 when no tile has more (see make_shape)
   int scale_bytes;   // per stage with per-token scales: K then V scales, each [tile][hc] fp32
   int smem_bytes;
 };
@@ -108,7 +109,11 @@ Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int pa
   s.scale_tma = 0;   // decided at launch (needs a tensor map over the scale arrays)
   s.kv_bytes = s.hc * s.nx * s.region_bytes;
   s.merge_bytes = s.wph > 1 ? kConsumerWarps * (16 * (head_dim + head_dim / 8) + 32) * 4 : 0;
-  s.qfrag_bytes = s.mt * s.hc * (head_dim / 16) * 512;   // one Q fragment set per head tile
+  // One Q fragment set per head tile.  With per-token scales and at most 8
+  // query heads per KV head, rows 8..15 of every tile are zero: only rows
+  // 0..7 are kept, which leaves room for a third stage on those shapes.
+  s.qrows = token_scales && group <= 8 ? 8 : 16;
+  s.qfrag_bytes = s.mt * s.hc * (head_dim / 16) * (s.qrows == 8 ? 256 : 512);
   s.scale_bytes = token_scales ? 2 * s.hc * s.tile * 4 : 0;
   int st = (kSmemBudget - 1024 - s.merge_bytes - s.qfrag_bytes) / (2 * s.kv_bytes + s.scale_bytes);
   if (st > kMaxStages) st = kMaxStages;
@@ -248,10 +253,28 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
+}
+
+// A fragment of k-step kk of this lane's head tile: rows r and r + 8 (QROWS
+// 16), or row r with zeros for the absent rows 8..15 (QROWS 8).
+template <int QROWS>
+__device__ __forceinline__ uint4 load_qfrag(uint32_t qf, int kk) {
+  if constexpr (QROWS == 16) {
+    return lds128(qf + kk * 512);
+  } else {
+    const uint2 h = lds64(qf + kk * 256);
+    return make_uint4(h.x, 0u, h.y, 0u);
+  }
 }
 
 // Two e4m3 codes (low byte first) -> two f16 (or bf16) in one register, exact.
@@ -374,7 +397,7 @@ struct Shared {
 // consumer multiplies each score by its token's K scale and each probability
 // by its token's V scale before the P V product (the softmax sum keeps the
 // unscaled probabilities).
-template <int KVT, typename QT, int D, bool TOK>
+template <int KVT, typename QT, int D, bool TOK, int QROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     mma_split_kernel(const Params p, const Shape sh, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv,
@@ -575,12 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // local query heads (within the stream) of rows r and r + 8
     const int h0 = mtile * 16 + r, h1 = h0 + 8;
     const bool v0 = h0 < G, v1 = h1 < G;
-    // multi-token queries: rows r and r + 8 stop this many keys before the
-    // sequence's end (0 for one query token per sequence)
-    const int cut0 = p.q_len - 1 - h0 % p.q_len, cut1 = p.q_len - 1 - h1 % p.q_len;
     const int li0 = kvl * G + h0, li1 = kvl * G + h1;   // slot rows
     // this head tile's Q fragments in shared memory: [kk][lane] x 16 bytes
-    const uint32_t qf = qfrag0 + (uint32_t)ht * KSTEPS * 512 + lane * 16;
+    const uint32_t qf = qfrag0 + (uint32_t)ht * KSTEPS * (QROWS * 32) + lane * (QROWS);
 
     SegmentIter it;
     it.init(p, plan);
@@ -619,9 +639,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint2 x0 = make_uint2(0, 0), x1 = make_uint2(0, 0);
         if (v0) x0 = __ldg(reinterpret_cast<const uint2*>(qg + (qrow0 + li0) * D + dd));
         if (v1) x1 = __ldg(reinterpret_cast<const uint2*>(qg + (qrow0 + li1) * D + dd));
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qf + kk * 512), "r"(x0.x),
-                     "r"(x1.x), "r"(x0.y), "r"(x1.y)
-                     : "memory");
+        if constexpr (QROWS == 8)
+          asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(qf + kk * 256), "r"(x0.x), "r"(x0.y)
+                       : "memory");
+        else
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qf + kk * 512), "r"(x0.x),
+                       "r"(x1.x), "r"(x0.y), "r"(x1.y)
+                       : "memory");
       }
       __syncwarp();
       float o[NT][4];
@@ -650,10 +674,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // valid keys of rows r and r + 8 from the sub-tile start: the
             // segment's end, and for multi-token queries the causal limit
             int left0 = left, left1 = left;
-            if (p.q_len > 1) {
+            if (p.q_len > 1) {   // rows r and r + 8 stop q_len - 1 - j keys before the end
               const int tail = seg.T - (t0 + sub);
-              left0 = min(left, tail - cut0);
-              left1 = min(left, tail - cut1);
+              left0 = min(left, tail - (p.q_len - 1 - h0 % p.q_len));
+              left1 = min(left, tail - (p.q_len - 1 - h1 % p.q_len));
             }
             const bool edge = min(left0, left1) < SUB;
             // ---- S = Q K^T over NJ n-tiles of 8 tokens.  Each Q fragment is
@@ -673,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
-                const uint4 a = lds128(qf + kk * 512);
+                const uint4 a = load_qfrag<QROWS>(qf, kk);
 #pragma unroll
                 for (int jn = 0; jn < NJ; ++jn) {
                   const uint2 kb = widen8x4<KVT, BF16>(w[jn][kk]);
@@ -689,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint4 a = lds128(qf + kk * 512);
+                const uint4 a = load_qfrag<QROWS>(qf, kk);
 #pragma unroll
                 for (int jn = 0; jn < NJ; ++jn) {
                   const uint2 kb = widen8x4<KVT, BF16>(w[jn][kk]);
@@ -708,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
-                  const uint4 a = lds128(qf + (x2 * 4 + k4) * 512);
+                  const uint4 a = load_qfrag<QROWS>(qf, x2 * 4 + k4);
 #pragma unroll
                   for (int jn = 0; jn < NJ; ++jn) {
                     const uint4 pp = c[jn][k4 >> 1];
@@ -724,14 +748,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             float mx0 = -INFINITY, mx1 = -INFINITY;
             // per-token scales of this warp's KV head in the stage (TOK):
             // token tt of the tile at [tt * hc + kvl]
-            const float* tsk = scl + (size_t)stg * (sh.scale_bytes / 4) + sub * sh.hc + kvl;
-            const float* tsv = tsk + sh.hc * sh.tile;
+            // (32-bit shared-memory addresses: fewer registers than pointers)
+            const uint32_t tsk =
+                smem_u32(scl) + 4u * (uint32_t)(stg * (sh.scale_bytes / 4) + sub * sh.hc + kvl);
+            const uint32_t tsv = tsk + 4u * (uint32_t)(sh.hc * sh.tile);
 #pragma unroll
             for (int jn = 0; jn < NJ; ++jn) {
               float2 kk2 = make_float2(1.f, 1.f);
               if constexpr (TOK) {
-                kk2.x = tsk[(8 * jn + 2 * q) * sh.hc];
-                kk2.y = tsk[(8 * jn + 2 * q + 1) * sh.hc];
+                kk2.x = lds_f32(tsk + 4u * (uint32_t)((8 * jn + 2 * q) * sh.hc));
+                kk2.y = lds_f32(tsk + 4u * (uint32_t)((8 * jn + 2 * q + 1) * sh.hc));
               }
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -771,8 +797,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int jn = 0; jn < NJ; ++jn) {
                 // tokens past the end: their scale slot may hold anything
                 const int tk = 8 * jn + 2 * q;
-                const float vx = tk < left ? tsv[tk * sh.hc] : 0.f;
-                const float vy = tk + 1 < left ? tsv[(tk + 1) * sh.hc] : 0.f;
+                const float vx = tk < left ? lds_f32(tsv + 4u * (uint32_t)(tk * sh.hc)) : 0.f;
+                const float vy = tk + 1 < left ? lds_f32(tsv + 4u * (uint32_t)((tk + 1) * sh.hc)) : 0.f;
                 pr[jn][0] *= vx;
                 pr[jn][1] *= vy;
                 pr[jn][2] *= vx;
@@ -1101,9 +1127,9 @@ struct Maps {
   CUtensorMap k, v, ks, vs;   // caches; per-token scale arrays (when sh.scale_tma)
 };
 
-template <int KVT, typename QT, int D, bool TOK>
+template <int KVT, typename QT, int D, bool TOK, int QROWS = 16>
 cudaError_t launch_t(const Params& p, const Shape& sh, const Maps& m, cudaStream_t stream) {
-  auto kern = mma_split_kernel<KVT, QT, D, TOK>;
+  auto kern = mma_split_kernel<KVT, QT, D, TOK, QROWS>;
   static int configured = 0;
   if (configured < sh.smem_bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1115,14 +1141,21 @@ cudaError_t launch_t(const Params& p, const Shape& sh, const Maps& m, cudaStream
                       m.v, m.ks, m.vs);
 }
 
+// 8-bit caches with per-token scales: all 16 Q rows, or 8.
+template <int KVT, typename QT, int D>
+cudaError_t launch_tok(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st) {
+  return sh.qrows == 8 ? launch_t<KVT, QT, D, true, 8>(p, sh, m, st)
+                       : launch_t<KVT, QT, D, true, 16>(p, sh, m, st);
+}
+
 // 8-bit caches: q dtype x per-token scales or not.
 template <int KVT, int D>
 cudaError_t launch_8bit(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st) {
   const bool tok = p.scale_kind == FD_SCALE_TOKEN;
   if (p.q_dtype == FD_F16)
-    return tok ? launch_t<KVT, __half, D, true>(p, sh, m, st)
+    return tok ? launch_tok<KVT, __half, D>(p, sh, m, st)
                : launch_t<KVT, __half, D, false>(p, sh, m, st);
-  return tok ? launch_t<KVT, __nv_bfloat16, D, true>(p, sh, m, st)
+  return tok ? launch_tok<KVT, __nv_bfloat16, D>(p, sh, m, st)
              : launch_t<KVT, __nv_bfloat16, D, false>(p, sh, m, st);
 }
 
