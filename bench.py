@@ -140,9 +140,9 @@ def make_workload(args) -> fw.Workload:
     if args.kv != "e4m3":
         if args.config < 3:
             raise SystemExit("--kv needs an 8-bit workload (configs 3-5)")
-        w = fw.CONFIGS[args.config](kv_dtype=args.kv)
+        w = fw.WORKLOADS[args.config](kv_dtype=args.kv)
     else:
-        w = fw.CONFIGS[args.config]()
+        w = fw.WORKLOADS[args.config]()
     if args.q_len > 1:
         if args.append:
             raise SystemExit("--append takes one query token per sequence")
@@ -160,7 +160,7 @@ def make_workload(args) -> fw.Workload:
 
 
 def workload_config(args) -> dict:
-    c = {"workload": fw.CONFIG_NAMES[args.config]}
+    c = {"workload": fw.WORKLOAD_NAMES[args.config]}
     if args.shared_prefix:
         c["shared_prefix_tokens"] = args.shared_prefix
     if args.kv != "e4m3":

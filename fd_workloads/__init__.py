@@ -397,7 +397,7 @@ def with_q_len(w: Workload, q_len: int, seed: int) -> Workload:
     return dataclasses.replace(w, name=w.name + f"-q{q_len}", q=q, q_len=q_len)
 
 
-CONFIGS = {
+WORKLOADS = {
     1: tiny_mqa,
     2: gqa_bf16,
     3: fp8_ragged,
@@ -405,7 +405,7 @@ CONFIGS = {
     5: long_mqa,
 }
 
-CONFIG_NAMES = {
+WORKLOAD_NAMES = {
     1: "tiny MQA decode fp16: B=2, seq_len {7,33}, 4/1 heads, D=64, contiguous",
     2: "GQA decode bf16: B=16, seq_len 4096, 32/8 heads, D=128, contiguous",
     3: "FP8 ragged decode: B=32, seq_len U[512,32768], 32/8 heads, D=128, e4m3 KV, contiguous",

@@ -147,7 +147,7 @@ def test_decode_with_append_matches_oracle(i, kernel):
                                     (4, fw.SCALE_TOKEN)])
 def test_config_full_size_with_append(n, kind):
     """The decode workloads' last token written by the step itself."""
-    w = fw.CONFIGS[n]()
+    w = fw.WORKLOADS[n]()
     if kind:
         w = fw.with_scales(w, kind, 84 + n)
     exp, t, out, lse = _fused(w, 400 + n)

@@ -73,12 +73,12 @@ def test_multi_token_finer_scales(kind):
 
 @functools.lru_cache(maxsize=None)
 def verify_workload(n, q_len):
-    return fw.with_q_len(fw.CONFIGS[n](), q_len, 540 + n)
+    return fw.with_q_len(fw.WORKLOADS[n](), q_len, 540 + n)
 
 
 @pytest.mark.parametrize("n,q_len", [(4, 2), (4, 4), (5, 4), (5, 8), (3, 2)])
 def test_config_full_size_multi_token(n, q_len):
-    """The decode workloads as verify steps: config 4 with 2 tokens fills the
-    16-row MMA tile (8 query heads x 2 tokens per KV head)."""
+    """The decode workloads as verify steps: on the FP8 paged one, 2 tokens fill
+    the 16-row MMA tile (8 query heads x 2 tokens per KV head)."""
     w = verify_workload(n, q_len)
     check(w, label=f"config{n}-q{q_len}")

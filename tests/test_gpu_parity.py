@@ -35,7 +35,7 @@ def kernels_for(w):
 
 @functools.lru_cache(maxsize=None)
 def config(n):
-    return fw.CONFIGS[n]()
+    return fw.WORKLOADS[n]()
 
 
 @functools.lru_cache(maxsize=None)
@@ -147,7 +147,7 @@ def test_config_full_size_finer_scales(n, kind):
                                     (5, fw.SCALE_TOKEN)])
 def test_config_full_size_int8(n, kind):
     """The 8-bit workloads with the same draws quantised to INT8."""
-    w = fw.CONFIGS[n](kv_dtype="i8")
+    w = fw.WORKLOADS[n](kv_dtype="i8")
     assert w.k_cache.dtype == np.int8
     if kind:
         w = fw.with_scales(w, kind, 74 + n)
