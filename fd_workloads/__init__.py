@@ -302,32 +302,34 @@ def share_prefix(w: Workload, shared_tokens: int) -> Workload:
     return dataclasses.replace(w, name=w.name + f"-shared{int(shared_tokens)}", block_table=table)
 
 
-def new_tokens(w: Workload, seed: int, std: float = 1.0):
-    """K and V of one new token per sequence, [B, KVH, D] 16-bit patterns of
-    the workload's q dtype (the projection's output dtype): N(0, std^2) draws,
-    K then V."""
+def new_tokens(w: Workload, seed: int, std: float = 1.0, n_new: int = 1):
+    """K and V of the new tokens of every sequence, [B, KVH, D] (one token) or
+    [B, n_new, KVH, D] 16-bit patterns of the workload's q dtype (the
+    projection's output dtype): N(0, std^2) draws, K then V."""
     rng = np.random.Generator(np.random.PCG64(seed))
-    shape = (w.batch, w.num_kv_heads, w.head_dim)
+    shape = ((w.batch, w.num_kv_heads, w.head_dim) if n_new == 1
+             else (w.batch, n_new, w.num_kv_heads, w.head_dim))
     k = rng.standard_normal(shape, dtype=np.float32) * np.float32(std)
     v = rng.standard_normal(shape, dtype=np.float32) * np.float32(std)
     return _cast16(k, w.q_dtype), _cast16(v, w.q_dtype)
 
 
-def append_bytes(w: Workload) -> int:
-    """Bytes the KV append of one new token per sequence must move: the new
+def append_bytes(w: Workload, n_new: int = 1) -> int:
+    """Bytes the KV append of n_new new tokens per sequence must move: the new
     K/V rows read (q dtype), the same rows written to the cache, the
     positions, and per-token scales written."""
-    rows = w.batch * w.num_kv_heads * w.head_dim
+    rows = w.batch * n_new * w.num_kv_heads * w.head_dim
     b = 2 * rows * 2 + 2 * rows * w.kv_elem_bytes + 4 * w.batch
     if w.scale_kind == SCALE_TOKEN:
-        b += 2 * 4 * w.batch * w.num_kv_heads
+        b += 2 * 4 * w.batch * n_new * w.num_kv_heads
     return b
 
 
-def last_positions(w: Workload) -> np.ndarray:
-    """Index of each sequence's last token (the slot a decode step appends
-    into when seq_len already counts the new token); -1 for empty ones."""
-    return np.where(w.seq_len > 0, w.seq_len - 1, -1).astype(np.int32)
+def last_positions(w: Workload, n_new: int = 1) -> np.ndarray:
+    """Index of the first of each sequence's last n_new tokens (the slots a
+    decode or verify step appends into when seq_len already counts its new
+    tokens); -1 for sequences shorter than n_new."""
+    return np.where(w.seq_len >= n_new, w.seq_len - n_new, -1).astype(np.int32)
 
 
 # ----------------------------------------------------------------------------

@@ -83,7 +83,7 @@ class Oracle:
         lib.fdo_append_kv.restype = ctypes.c_int
         lib.fdo_append_kv.argtypes = [
             vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int64,
-            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
             ctypes.c_float, ctypes.c_int, vp, vp]
         self.lib = lib
         self.path = lib_path
@@ -102,12 +102,14 @@ class Oracle:
 
     def append_kv(self, w, k_new, v_new, positions):
         """The KV append on copies of the workload's caches (and per-token
-        scale arrays).  k_new, v_new: [B, KVH, D] 16-bit patterns of the
-        workload's q dtype; positions: int32 [B] (< 0: no append).  Returns
+        scale arrays).  k_new, v_new: [B, KVH, D] (one new token) or
+        [B, n_new, KVH, D] 16-bit patterns of the workload's q dtype;
+        positions: int32 [B], the first new token's index (< 0: no append).  Returns
         (k_cache, v_cache, k_scales, v_scales); the scale arrays are None for
         per-tensor scales."""
         k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
         v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+        n_new = int(k_new.shape[1]) if k_new.ndim == 4 else 1
         positions = np.ascontiguousarray(positions, dtype=np.int32)
         kc = np.ascontiguousarray(w.k_cache).copy()
         vc = np.ascontiguousarray(w.v_cache).copy()
@@ -119,9 +121,9 @@ class Oracle:
         bt_stride = int(w.block_table.shape[1]) if w.block_table is not None else 0
         rc = self.lib.fdo_append_kv(
             _ptr(k_new), _ptr(v_new), _DTYPES[w.q_dtype], _ptr(kc), _ptr(vc), _DTYPES[w.kv_dtype],
-            _ptr(w.kv_start_idx), _ptr(w.block_table), bt_stride, _ptr(positions), int(w.kv_rows), int(w.batch), int(w.num_kv_heads),
-            int(w.head_dim), int(w.page_size), float(w.k_scale), float(w.v_scale), int(kind),
-            _ptr(ks), _ptr(vs))
+            _ptr(w.kv_start_idx), _ptr(w.block_table), bt_stride, _ptr(positions),
+            int(w.kv_rows), int(w.batch), n_new, int(w.num_kv_heads), int(w.head_dim),
+            int(w.page_size), float(w.k_scale), float(w.v_scale), int(kind), _ptr(ks), _ptr(vs))
         if rc != 0:
             raise OracleError(_ERRORS.get(rc, f"status {rc}"))
         return kc, vc, ks, vs

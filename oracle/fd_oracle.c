@@ -64,10 +64,12 @@
  * cache before the attention read ("Learn CUDA from scratch, chapter 15",
  * section 15.9: contiguous and paged cache write layouts, and its exercise on
  * a single-token decode append; quantisation with scales as in section
- * 15.11).  For each sequence b with positions[b] >= 0 and each KV head h:
+ * 15.11).  For each sequence b with positions[b] >= 0, each of its n_new new
+ * tokens i (n_new > 1: the drafted tokens of a speculative verify step) and
+ * each KV head h:
  *
- *   row       = row(b, positions[b])            (as above)
- *   x_d       = new[b][h][d]                     (f16 or bf16, exact in fp32)
+ *   row       = row(b, positions[b] + i)        (as above)
+ *   x_d       = new[b][i][h][d]                  (f16 or bf16, exact in fp32)
  *   16-bit cache: the element is stored as it is (the cache has new's dtype);
  *   8-bit cache, with QMAX = 448 (e4m3) or 127 (int8):
  *     s = k_scale                                (per tensor)
@@ -362,39 +364,41 @@ static float elem16_to_f32(const uint16_t *base, int dtype, size_t idx) {
 static int append_one(const uint16_t *x_new, int new_dtype, void *cache, int kv_dtype,
                       const int32_t *kv_start_idx, const int32_t *block_table,
                       int block_table_stride, const int32_t *positions, int64_t kv_rows,
-                      int batch, int num_kv_heads, int head_dim, int page_size, float scale,
-                      int scale_kind, float *scales) {
+                      int batch, int n_new, int num_kv_heads, int head_dim, int page_size,
+                      float scale, int scale_kind, float *scales) {
   int status = FDO_OK;
   const float qmax = kv_dtype == FDO_I8 ? 127.0f : 448.0f;
   for (int b = 0; b < batch; ++b) {
     if (positions[b] < 0) continue;
-    int64_t row = cache_row(kv_start_idx, block_table, block_table_stride, page_size, b,
-                            positions[b], kv_rows);
-    if (row < 0) { status = FDO_ROW_OUT_OF_RANGE; continue; }
-    for (int h = 0; h < num_kv_heads; ++h) {
-      const size_t src = ((size_t)b * num_kv_heads + h) * head_dim;
-      const size_t dst = ((size_t)row * num_kv_heads + h) * head_dim;
-      if (kv_dtype == FDO_F16 || kv_dtype == FDO_BF16) {
-        for (int d = 0; d < head_dim; ++d) ((uint16_t *)cache)[dst + d] = x_new[src + d];
-        continue;
-      }
-      float s = scale;
-      if (scale_kind == FDO_SCALE_HEAD) {
-        s = scale * scales[h];
-      } else if (scale_kind == FDO_SCALE_TOKEN) {
-        float amax = 0.0f;
-        for (int d = 0; d < head_dim; ++d) {
-          float a = fabsf(elem16_to_f32(x_new, new_dtype, src + d));
-          if (a > amax) amax = a;
+    for (int i = 0; i < n_new; ++i) {
+      int64_t row = cache_row(kv_start_idx, block_table, block_table_stride, page_size, b,
+                              positions[b] + i, kv_rows);
+      if (row < 0) { status = FDO_ROW_OUT_OF_RANGE; continue; }
+      for (int h = 0; h < num_kv_heads; ++h) {
+        const size_t src = (((size_t)b * n_new + i) * num_kv_heads + h) * head_dim;
+        const size_t dst = ((size_t)row * num_kv_heads + h) * head_dim;
+        if (kv_dtype == FDO_F16 || kv_dtype == FDO_BF16) {
+          for (int d = 0; d < head_dim; ++d) ((uint16_t *)cache)[dst + d] = x_new[src + d];
+          continue;
         }
-        const float denom = qmax * scale;
-        const float ks = amax > 0.0f ? amax / denom : 1.0f;
-        scales[(size_t)row * num_kv_heads + h] = ks;
-        s = scale * ks;
-      }
-      for (int d = 0; d < head_dim; ++d) {
-        const float q = elem16_to_f32(x_new, new_dtype, src + d) / s;
-        ((uint8_t *)cache)[dst + d] = kv_dtype == FDO_I8 ? fdo_i8_encode(q) : fdo_e4m3_encode(q);
+        float s = scale;
+        if (scale_kind == FDO_SCALE_HEAD) {
+          s = scale * scales[h];
+        } else if (scale_kind == FDO_SCALE_TOKEN) {
+          float amax = 0.0f;
+          for (int d = 0; d < head_dim; ++d) {
+            float a = fabsf(elem16_to_f32(x_new, new_dtype, src + d));
+            if (a > amax) amax = a;
+          }
+          const float denom = qmax * scale;
+          const float ks = amax > 0.0f ? amax / denom : 1.0f;
+          scales[(size_t)row * num_kv_heads + h] = ks;
+          s = scale * ks;
+        }
+        for (int d = 0; d < head_dim; ++d) {
+          const float q = elem16_to_f32(x_new, new_dtype, src + d) / s;
+          ((uint8_t *)cache)[dst + d] = kv_dtype == FDO_I8 ? fdo_i8_encode(q) : fdo_e4m3_encode(q);
+        }
       }
     }
   }
@@ -402,16 +406,19 @@ static int append_one(const uint16_t *x_new, int new_dtype, void *cache, int kv_
 }
 
 /*
- * Writes the new token of every sequence into k_cache / v_cache (see the file
- * comment).  k_new, v_new: [batch][KVH][D] 16-bit patterns of new_dtype.
- * positions: [batch] token index of the new token (< 0: no append).
+ * Writes the n_new new tokens of every sequence into k_cache / v_cache (see
+ * the file comment).  k_new, v_new: [batch][n_new][KVH][D] 16-bit patterns
+ * of new_dtype.  positions: [batch] token index of the first new token (< 0:
+ * no append).
  * k_scales / v_scales: read (per KV head) or written (per token).
  */
 int fdo_append_kv(const void *k_new, const void *v_new, int new_dtype, void *k_cache,
                   void *v_cache, int kv_dtype, const int32_t *kv_start_idx,
                   const int32_t *block_table, int block_table_stride, const int32_t *positions,
-                  int64_t kv_rows, int batch, int num_kv_heads, int head_dim, int page_size,
-                  float k_scale, float v_scale, int scale_kind, float *k_scales, float *v_scales) {
+                  int64_t kv_rows, int batch, int n_new, int num_kv_heads, int head_dim,
+                  int page_size, float k_scale, float v_scale, int scale_kind, float *k_scales,
+                  float *v_scales) {
+  if (n_new < 1) return FDO_BAD_ARG;
   if (!k_new || !v_new || !k_cache || !v_cache || !positions) return FDO_BAD_ARG;
   if ((kv_start_idx == NULL) == (block_table == NULL)) return FDO_BAD_ARG;
   if (new_dtype != FDO_F16 && new_dtype != FDO_BF16) return FDO_BAD_ARG;
@@ -421,10 +428,10 @@ int fdo_append_kv(const void *k_new, const void *v_new, int new_dtype, void *k_c
   if (scale_kind != FDO_SCALE_TENSOR && (!k_scales || !v_scales)) return FDO_BAD_ARG;
   if (block_table && page_size <= 0) return FDO_BAD_ARG;
   int a = append_one((const uint16_t *)k_new, new_dtype, k_cache, kv_dtype, kv_start_idx,
-                     block_table, block_table_stride, positions, kv_rows, batch, num_kv_heads,
-                     head_dim, page_size, k_scale, scale_kind, k_scales);
+                     block_table, block_table_stride, positions, kv_rows, batch, n_new,
+                     num_kv_heads, head_dim, page_size, k_scale, scale_kind, k_scales);
   int b = append_one((const uint16_t *)v_new, new_dtype, v_cache, kv_dtype, kv_start_idx,
-                     block_table, block_table_stride, positions, kv_rows, batch, num_kv_heads,
-                     head_dim, page_size, v_scale, scale_kind, v_scales);
+                     block_table, block_table_stride, positions, kv_rows, batch, n_new,
+                     num_kv_heads, head_dim, page_size, v_scale, scale_kind, v_scales);
   return a != FDO_OK ? a : b;
 }

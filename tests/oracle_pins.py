@@ -572,30 +572,32 @@ def _appended_rows(w, positions):
     return rows
 
 
-def _check_append(orc, w, seed):
-    k_new, v_new = fw.new_tokens(w, seed, std=3.0)
-    pos = fw.last_positions(w)
+def _check_append(orc, w, seed, n_new=1):
+    k_new, v_new = fw.new_tokens(w, seed, std=3.0, n_new=n_new)
+    pos = fw.last_positions(w, n_new)
     pos[0] = -1   # the first sequence gets no append
     kc, vc, ks, vs = orc.append_kv(w, k_new, v_new, pos)
     KVH, D = w.num_kv_heads, w.head_dim
-    rows = _appended_rows(w, pos)
+    if n_new == 1:
+        k_new, v_new = k_new[:, None], v_new[:, None]
+    rows = [_appended_rows(w, np.where(pos >= 0, pos + i, -1)) for i in range(n_new)]
     for cache, old, new, scale, sarr, sarr_old in (
             (kc, w.k_cache, k_new, w.k_scale, ks, w.k_scales),
             (vc, w.v_cache, v_new, w.v_scale, vs, w.v_scales)):
         c2 = cache.reshape(-1, KVH, D)
         o2 = np.asarray(old).reshape(-1, KVH, D)
         touched = np.zeros(c2.shape[0], bool)
-        touched[[r for r in rows if r >= 0]] = True
+        touched[[r for ri in rows for r in ri if r >= 0]] = True
         assert np.array_equal(c2[~touched], o2[~touched]), f"{w.name}: rows outside the append changed"
         if sarr is not None and w.scale_kind == fw.SCALE_TOKEN:
             s2 = sarr.reshape(-1, KVH)
             assert np.array_equal(s2[~touched], np.asarray(sarr_old).reshape(-1, KVH)[~touched])
-        x = lib_decode(new, w.q_dtype).astype(np.float32)      # [B, KVH, D], exact
-        for b, r in enumerate(rows):
+        x = lib_decode(new, w.q_dtype).astype(np.float32)      # [B, n_new, KVH, D], exact
+        for b, i, r in ((b, i, rows[i][b]) for i in range(n_new) for b in range(w.batch)):
             if r < 0:
                 continue
             if w.kv_dtype in ("f16", "bf16"):
-                assert np.array_equal(c2[r], new[b]), "16-bit append must store the bits"
+                assert np.array_equal(c2[r], new[b, i]), "16-bit append must store the bits"
                 continue
             qmax = 448.0 if w.kv_dtype == "e4m3" else 127.0
             for h in range(KVH):
@@ -605,7 +607,7 @@ def _check_append(orc, w, seed):
                     seff = np.float32(scale) * np.float32(sarr[h])
                 else:
                     seff = np.float32(scale)
-                q = x[b, h] / seff                                   # numpy fp32 IEEE division
+                q = x[b, i, h] / seff                                # numpy fp32 IEEE division
                 enc = lib_e4m3_encode(q) if w.kv_dtype == "e4m3" else lib_i8_encode(q)
                 assert np.array_equal(c2[r, h].view(np.uint8), enc), f"{w.name} row {r} head {h}"
                 if w.scale_kind == fw.SCALE_TOKEN:
@@ -636,6 +638,9 @@ def pin_append_kv(orc):
                              4, 56))
     for i, w in enumerate(cases):
         _check_append(orc, w, 60 + i)
+    # several new tokens per sequence (a verify step's drafted tokens)
+    _check_append(orc, cases[2], 70, n_new=3)
+    _check_append(orc, cases[3], 71, n_new=2)
 
 
 # ----------------------------------------------------------------------------

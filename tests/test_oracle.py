@@ -57,10 +57,11 @@ MUTATIONS = [
     ("if (f > 0.5 || (f == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;",
      "if (f >= 0.5) r += 1.0;", "int8 encoder ties away from zero"),
     ("if (r > 127.0) r = 127.0;", "if (r > 128.0) r = 128.0;", "int8 encoder clamps at 128"),
-    ("positions[b], kv_rows);\n    if (row < 0) { status = FDO_ROW_OUT_OF_RANGE; continue; }",
-     "positions[b] + 1, kv_rows);\n    if (row < 0) { status = FDO_ROW_OUT_OF_RANGE; continue; }",
-     "append one token late"),
-    ("        s = scale * scales[h];\n", "        s = scale;\n", "append ignores head scales"),
+    ("positions[b] + i, kv_rows);", "positions[b] + i + 1, kv_rows);", "append one token late"),
+    ("          s = scale * scales[h];\n", "          s = scale;\n", "append ignores head scales"),
+    ("(((size_t)b * n_new + i) * num_kv_heads + h) * head_dim;",
+     "(((size_t)b * n_new + 0) * num_kv_heads + h) * head_dim;",
+     "every new token takes the first token's rows"),
     ("          if (a > amax) amax = a;", "          if (a > amax && d == 0) amax = a;",
      "token scale from the first element"),
     ("        const float denom = qmax * scale;", "        const float denom = qmax;",
