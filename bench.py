@@ -53,8 +53,9 @@ def parse():
                     help="query tokens per sequence (a speculative-decoding verify step: the "
                          "last q_len cached tokens, causal among themselves)")
     ap.add_argument("--append", action="store_true",
-                    help="the step also writes each sequence's last token (its K/V rows, "
-                         "quantised for 8-bit caches) before attending, in one call")
+                    help="the step also writes each sequence's last token (with --q-len, its "
+                         "last q_len tokens: K/V rows, quantised for 8-bit caches) before "
+                         "attending, in one call")
     ap.add_argument("--shared-prefix", type=int, default=0,
                     help="paged workloads: every sequence's first pages alias those of "
                          "sequence 0 up to this many tokens (prefix-cache hits)")
@@ -144,8 +145,6 @@ def make_workload(args) -> fw.Workload:
     else:
         w = fw.WORKLOADS[args.config]()
     if args.q_len > 1:
-        if args.append:
-            raise SystemExit("--append takes one query token per sequence")
         w = fw.with_q_len(w, args.q_len, 540 + args.config)
     if args.shared_prefix:
         if not w.paged:
@@ -168,9 +167,9 @@ def workload_config(args) -> dict:
     if args.q_len > 1:
         c["q_len"] = args.q_len
     if args.append:
-        c["append"] = ("each step first writes every sequence's last token (K/V rows of the "
-                       "projection dtype, quantised for 8-bit caches) into the cache, then "
-                       "attends over it: fd_decode_attention_append")
+        c["append"] = ("each step first writes every sequence's last q_len tokens (K/V rows of "
+                       "the projection dtype, quantised for 8-bit caches) into the cache, then "
+                       "attends over them: fd_decode_attention_append")
     if args.scales != "tensor":
         c["kv_scales"] = f"per {args.scales} (fp32, on top of the per-tensor scales)"
     return c
@@ -190,16 +189,17 @@ def run_reference(args):
             # the oracle's append of the whole batch, then the attention sample
             import dataclasses
             import oracle
-            k_new, v_new = fw.new_tokens(w, 500 + args.config)
+            k_new, v_new = fw.new_tokens(w, 500 + args.config, n_new=w.q_len)
             t0 = time.perf_counter()
-            kc, vc, ks, vs = oracle.default().append_kv(w, k_new, v_new, fw.last_positions(w))
+            kc, vc, ks, vs = oracle.default().append_kv(w, k_new, v_new,
+                                                        fw.last_positions(w, w.q_len))
             t_app = time.perf_counter() - t0
             wa = dataclasses.replace(w, k_cache=kc, v_cache=vc)
             if w.scale_kind == fw.SCALE_TOKEN:
                 wa = dataclasses.replace(wa, k_scales=ks, v_scales=vs)
             gbs, threads, desc, el = oracle_sample(wa, budget_s=2.0)
             el_all = el + t_app
-            gbs = (gbs * el + fw.append_bytes(w) / 1e9) / el_all
+            gbs = (gbs * el + fw.append_bytes(w, w.q_len) / 1e9) / el_all
             el = el_all
             desc += f"; plus the append of all {w.batch} new tokens ({t_app:.3f} s)"
         else:
@@ -356,14 +356,14 @@ def run_gpu(args):
     kname = {1: "simt", 2: "mma"}.get(sel, "none")
 
     if args.append:
-        k_new, v_new = fw.new_tokens(w, 500 + args.config)
+        k_new, v_new = fw.new_tokens(w, 500 + args.config, n_new=w.q_len)
         qd, _ = fw.torch_dtypes(w)
         t["k_new"] = torch.from_numpy(k_new.view(np.int16)).view(qd).to(dev)
         t["v_new"] = torch.from_numpy(v_new.view(np.int16)).view(qd).to(dev)
-        t["positions"] = torch.from_numpy(fw.last_positions(w)).to(dev)
+        t["positions"] = torch.from_numpy(fw.last_positions(w, w.q_len)).to(dev)
 
     def step():
-        if w.q_len > 1:
+        if w.q_len > 1 and not args.append:
             fda.fd_decode_attention_multi(
                 t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
                 w.kv_rows, QH, KVH, D, w.page_size, float(w.softmax_scale), float(w.k_scale),
@@ -457,7 +457,7 @@ def run_gpu(args):
     if pg:
         total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / K
-    alg = w.algorithmic_bytes() + (fw.append_bytes(w) if args.append else 0)
+    alg = w.algorithmic_bytes() + (fw.append_bytes(w, w.q_len) if args.append else 0)
     value = whole_job_throughput(alg, world, ms_per_step * 1e-3) / 1e9
 
     # end to end through the public API: pinned host inputs in, result out

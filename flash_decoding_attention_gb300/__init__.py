@@ -93,12 +93,12 @@ def load_library(path: Optional[str] = None):
                                                   i32, i32, i32, f32, f32, f32, i32, vp, vp, i32,
                                                   i32, vp, vp, vp, sz, vp]
         lib.fd_append_kv.restype = i32
-        lib.fd_append_kv.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, i32, f32,
-                                     f32, i32, vp, vp, i32, i32, vp, sz, vp]
+        lib.fd_append_kv.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, i32, i32,
+                                     f32, f32, i32, vp, vp, i32, i32, vp, sz, vp]
         lib.fd_decode_attention_append.restype = i32
         lib.fd_decode_attention_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i64,
-                                                   i32, i32, i32, i32, i32, f32, f32, f32, i32,
-                                                   vp, vp, i32, i32, vp, vp, vp, sz, vp]
+                                                   i32, i32, i32, i32, i32, i32, f32, f32, f32,
+                                                   i32, vp, vp, i32, i32, vp, vp, vp, sz, vp]
         lib.fd_decode_attention_noalloc.restype = i32
         lib.fd_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, i32, i32,
                                                     i32, i32, i32, f32, f32, f32, i32, i32, vp,
@@ -250,16 +250,18 @@ def fd_append_kv(k_new, v_new, k_cache, v_cache, kv_start_idx, block_table, posi
                  v_scale: float, scale_kind: int, k_scales, v_scales, workspace, stream=None,
                  new_dtype: Optional[int] = None, kv_dtype: Optional[int] = None,
                  check: bool = True) -> int:
-    """Writes one new token per sequence (k_new, v_new: [B, KVH, D]) into the
-    caches at ``positions`` (int32 [B], < 0: none), quantising for 8-bit
+    """Writes the new tokens of every sequence (k_new, v_new: [B, KVH, D] for
+    one, [B, n_new, KVH, D] for n_new) into the caches from ``positions``
+    (int32 [B], the first new token's index, < 0: none), quantising for 8-bit
     caches; per-token scales are written into ``k_scales`` / ``v_scales``."""
     lib = load_library()
     batch = int(positions.shape[0])
+    n_new = int(k_new.shape[1]) if k_new.dim() == 4 else 1
     stride = int(block_table.shape[1]) if block_table is not None else 0
     st = lib.fd_append_kv(
         _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(kv_start_idx),
-        _ptr(block_table), stride, _ptr(positions), int(kv_rows), batch, int(num_kv_heads),
-        int(head_dim), int(page_size), float(k_scale), float(v_scale), int(scale_kind),
+        _ptr(block_table), stride, _ptr(positions), int(kv_rows), batch, n_new,
+        int(num_kv_heads), int(head_dim), int(page_size), float(k_scale), float(v_scale), int(scale_kind),
         _ptr(k_scales), _ptr(v_scales),
         _q_dtype(k_new) if new_dtype is None else int(new_dtype),
         _kv_dtype(k_cache) if kv_dtype is None else int(kv_dtype),
@@ -276,14 +278,17 @@ def fd_decode_attention_append(q, k_new, v_new, k_cache, v_cache, kv_start_idx, 
                                scale_kind: int, k_scales, v_scales, out, lse, workspace,
                                stream=None, q_dtype: Optional[int] = None,
                                kv_dtype: Optional[int] = None, check: bool = True) -> int:
-    """fd_append_kv of the step's new token, then the attention over the
-    caches holding it (``seq_len`` counts the new token), in one call."""
+    """fd_append_kv of the step's new tokens, then the attention over the
+    caches holding them (``seq_len`` counts them), in one call.  One new token
+    per sequence with q [B, QH, D] and k_new [B, KVH, D]; q_len of them with
+    q [B, QH, q_len, D] and k_new [B, q_len, KVH, D]."""
     lib = load_library()
     batch = int(seq_len.shape[0])
+    q_len = int(q.shape[2]) if q.dim() == 4 else 1
     stride = int(block_table.shape[1]) if block_table is not None else 0
     st = lib.fd_decode_attention_append(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(kv_start_idx),
-        _ptr(block_table), stride, _ptr(positions), _ptr(seq_len), int(kv_rows), batch,
+        _ptr(block_table), stride, _ptr(positions), _ptr(seq_len), int(kv_rows), batch, q_len,
         int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size), float(softmax_scale),
         float(k_scale), float(v_scale), int(scale_kind), _ptr(k_scales), _ptr(v_scales),
         _q_dtype(q) if q_dtype is None else int(q_dtype),
@@ -399,7 +404,8 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     8-bit caches, per-token scales written), and ``seq_len`` counts it.  A 4-d
     ``q`` ([B, QH, q_len, D]) asks for q_len query tokens per sequence, the
     last q_len cached tokens, causal among themselves (out and lse carry the
-    q_len axis too)."""
+    q_len axis too); with it, k_new / v_new are [B, q_len, KVH, D] and
+    ``positions`` holds the first new token's index."""
     multi = q.dim() == 4              # [B, QH, q_len, D]: multi-token queries
     B, QH, D = q.shape[0], q.shape[1], q.shape[-1]
     q_len = q.shape[2] if multi else 1
@@ -418,9 +424,7 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = alloc_workspace(B, QH * q_len, KVH, D, q.device)
-    if multi:
-        if k_new is not None:
-            raise ValueError("the KV append takes one query token per sequence")
+    if multi and k_new is None:
         kind = FD_SCALE_TENSOR if k_scales is None else (
             FD_SCALE_HEAD if k_scales.dim() == 1 else FD_SCALE_TOKEN)
         fd_decode_attention_multi(q, k_cache, v_cache, kv_start_idx, block_table, seq_len,

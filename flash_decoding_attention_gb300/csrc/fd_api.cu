@@ -109,7 +109,8 @@ fd_status check_append(const AppendArgs& a, int kv_dtype, float k_scale, float v
   return FD_OK;
 }
 
-void set_append(Params& p, const AppendArgs& a, float k_scale, float v_scale) {
+void set_append(Params& p, const AppendArgs& a, int n_new, float k_scale, float v_scale) {
+  p.n_new = n_new;
   p.k_new = a.k_new;
   p.v_new = a.v_new;
   p.positions = a.positions;
@@ -238,7 +239,7 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
                              float* lse, void* workspace, size_t workspace_bytes,
                              fd_stream_t stream, const AppendArgs* app, int q_len = 1) {
   // q_len query tokens per sequence run as q_len virtual query heads per head
-  if (q_len < 1 || q_len > 16 || (app && q_len != 1)) return FD_ERR_INVALID_ARG;
+  if (q_len < 1 || q_len > 16) return FD_ERR_INVALID_ARG;
   if (num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
       (num_q_heads / num_kv_heads) * q_len > 128)
     return FD_ERR_UNSUPPORTED;
@@ -329,7 +330,7 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (app) {
-    set_append(p, *app, k_scale, v_scale);
+    set_append(p, *app, q_len, k_scale, v_scale);
     if (launch_append(p, st) != cudaSuccess) return FD_ERR_CUDA;
     p.pdl = 1;
   }
@@ -379,7 +380,7 @@ fd_status fd_decode_attention_append(const void* q, const void* k_new, const voi
                                      void* k_cache, void* v_cache, const int32_t* kv_start_idx,
                                      const int32_t* block_table, int block_table_stride,
                                      const int32_t* positions, const int32_t* seq_len,
-                                     int64_t kv_rows, int batch, int num_q_heads,
+                                     int64_t kv_rows, int batch, int q_len, int num_q_heads,
                                      int num_kv_heads, int head_dim, int page_size,
                                      float softmax_scale, float k_scale, float v_scale,
                                      fd_scale_kind scale_kind, float* k_scales, float* v_scales,
@@ -389,14 +390,15 @@ fd_status fd_decode_attention_append(const void* q, const void* k_new, const voi
   return decode_impl(q, k_cache, v_cache, kv_start_idx, block_table, block_table_stride, seq_len,
                      kv_rows, batch, num_q_heads, num_kv_heads, head_dim, page_size,
                      softmax_scale, k_scale, v_scale, scale_kind, k_scales, v_scales, q_dtype,
-                     kv_dtype, out, lse, workspace, workspace_bytes, stream, &app);
+                     kv_dtype, out, lse, workspace, workspace_bytes, stream, &app, q_len);
 }
 
 fd_status fd_append_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                        const int32_t* kv_start_idx, const int32_t* block_table,
                        int block_table_stride, const int32_t* positions, int64_t kv_rows,
-                       int batch, int num_kv_heads, int head_dim, int page_size, float k_scale,
-                       float v_scale, fd_scale_kind scale_kind, float* k_scales, float* v_scales,
+                       int batch, int n_new, int num_kv_heads, int head_dim, int page_size,
+                       float k_scale, float v_scale, fd_scale_kind scale_kind, float* k_scales,
+                       float* v_scales,
                        fd_dtype new_dtype, fd_dtype kv_dtype, void* workspace,
                        size_t workspace_bytes, fd_stream_t stream) {
   if (scale_kind != FD_SCALE_TENSOR && scale_kind != FD_SCALE_HEAD &&
@@ -412,6 +414,7 @@ fd_status fd_append_kv(const void* k_new, const void* v_new, void* k_cache, void
   if ((kv_start_idx == nullptr) == (block_table == nullptr)) return FD_ERR_INVALID_ARG;
   if (batch <= 0 || batch > (1 << 24) || num_kv_heads <= 0 || num_kv_heads > 4096)
     return FD_ERR_INVALID_ARG;
+  if (n_new < 1 || n_new > 16) return FD_ERR_INVALID_ARG;
   if (kv_rows <= 0 || kv_rows > (int64_t(1) << 40)) return FD_ERR_INVALID_ARG;
   const int paged = block_table != nullptr;
   if (paged) {
@@ -448,7 +451,7 @@ fd_status fd_append_kv(const void* k_new, const void* v_new, void* k_cache, void
   p.scale_kind = scale_kind;
   p.k_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : k_scales;
   p.v_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : v_scales;
-  set_append(p, app, k_scale, v_scale);
+  set_append(p, app, n_new, k_scale, v_scale);
   return launch_append(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FD_OK
                                                                                 : FD_ERR_CUDA;
 }

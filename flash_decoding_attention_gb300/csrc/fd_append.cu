@@ -3,7 +3,9 @@
 // A decode step first writes the new token's K and V rows (the projection's
 // output, in the query dtype) into the cache, then attends over the cache
 // including them ("Learn CUDA from scratch, chapter 15", section 15.9: cache
-// write layouts, contiguous and paged, and its single-token decode append).
+// write layouts, contiguous and paged, and its single-token decode append);
+// a speculative verify step (section 15.21) writes its n_new drafted tokens,
+// token i of sequence b at position positions[b] + i.
 // For 8-bit caches the rows are quantised on the way in, with the scales of
 // section 15.11 of the same chapter:
 //   s = k_scale                          per tensor
@@ -16,7 +18,7 @@
 // operation (explicit round-to-nearest intrinsics, so no contraction), which
 // makes the codes reproducible off the device.
 //
-// One warp per (sequence, KV head): each lane holds head_dim / 32 elements,
+// One warp per (sequence, new token, KV head): each lane holds head_dim / 32 elements,
 // so a row is one coalesced 256- or 128-byte load per tensor and the row's
 // amax one warp reduction.
 #include <type_traits>
@@ -111,14 +113,15 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const Params 
   constexpr int DPL = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long item = (long long)blockIdx.x * kAppendWarps + warp;
-  if (item >= (long long)p.batch * p.num_kv_heads) return;
-  const int b = (int)(item / p.num_kv_heads);
-  const int h = (int)(item - (long long)b * p.num_kv_heads);
-  const int t = __ldg(p.positions + b);
-  if (t < 0) return;
-  const long long row = cache_row(p, b, t);   // records out-of-range rows itself
+  if (item >= (long long)p.batch * p.n_new * p.num_kv_heads) return;
+  const long long bi = item / p.num_kv_heads;            // b * n_new + i
+  const int h = (int)(item - bi * p.num_kv_heads);
+  const int b = (int)(bi / p.n_new), i = (int)(bi - (long long)b * p.n_new);
+  const int t0 = __ldg(p.positions + b);
+  if (t0 < 0) return;
+  const long long row = cache_row(p, b, t0 + i);   // records out-of-range rows itself
   if (row < 0) return;
-  const long long src = ((long long)b * p.num_kv_heads + h) * D + lane * DPL;
+  const long long src = (bi * p.num_kv_heads + h) * D + lane * DPL;
   const long long dst = (row * p.num_kv_heads + h) * D + lane * DPL;
   const long long srow = row * p.num_kv_heads + h;
   append_row<XT, KVT, DPL>(static_cast<const XT*>(p.k_new) + src, p.k_dst, dst, p.k_scale_raw,
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const Params 
 
 template <typename XT, int KVT>
 cudaError_t launch_t(const Params& p, cudaStream_t stream) {
-  const long long items = (long long)p.batch * p.num_kv_heads;
+  const long long items = (long long)p.batch * p.n_new * p.num_kv_heads;
   const unsigned blocks = (unsigned)((items + kAppendWarps - 1) / kAppendWarps);
   if (p.head_dim == 128)
     append_kernel<XT, KVT, 128><<<blocks, kAppendWarps * 32, 0, stream>>>(p);

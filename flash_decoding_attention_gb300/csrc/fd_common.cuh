@@ -101,9 +101,10 @@ struct Params {
   // it attends to the first T - (q_len - 1 - j) keys of its sequence.
   int q_len;
   // KV append (fd_append.cu); q_dtype is the dtype of k_new / v_new
-  const void* k_new;         // [batch][KVH][D]
+  const void* k_new;         // [batch][n_new][KVH][D]
   const void* v_new;
-  const int32_t* positions;  // [batch] token index of the new token, < 0: none
+  const int32_t* positions;  // [batch] token index of the first new token, < 0: none
+  int n_new;                 // new tokens per sequence
   void* k_dst;               // the caches, written
   void* v_dst;
   float* k_scales_dst;       // FD_SCALE_TOKEN: per-token scales, written

@@ -212,27 +212,31 @@ fd_status fd_decode_attention_multi(const void *q, const void *k_cache, const vo
  * KV-cache append of one new token per sequence ("Learn CUDA from scratch,
  * chapter 15", section 15.9: cache write layouts, contiguous and paged, and
  * the single-token decode append; quantisation with the scales of section
- * 15.11).  For every sequence b with positions[b] >= 0 and every KV head h,
- * the row r = kv_start_idx[b] + positions[b] (contiguous) or
- * block_table[b][positions[b] / page_size] * page_size + positions[b] % page_size
- * (paged) of K receives k_new[b][h][0 .. head_dim), and V likewise:
+ * 15.11; n_new > 1: the drafted tokens of a speculative verify step,
+ * section 15.21).  For every sequence b with positions[b] >= 0, every new
+ * token i < n_new and every KV head h, with t = positions[b] + i, the row
+ * r = kv_start_idx[b] + t (contiguous) or
+ * block_table[b][t / page_size] * page_size + t % page_size (paged) of K
+ * receives k_new[b][i][h][0 .. head_dim), and V likewise:
  *   16-bit cache (kv_dtype == new_dtype): the elements as they are;
  *   8-bit cache (FD_E4M3 or FD_I8), QMAX = 448 or 127, s the element's scale:
  *     s = k_scale                                  FD_SCALE_TENSOR
  *       = k_scale * k_scales[h]                    FD_SCALE_HEAD
  *       = k_scale * ks,  ks = amax / (QMAX * k_scale), stored to
- *         k_scales[r * num_kv_heads + h], amax = max_d |k_new[b][h][d]|
+ *         k_scales[r * num_kv_heads + h], amax = max_d |k_new[b][i][h][d]|
  *         (ks = 1 when amax = 0)                   FD_SCALE_TOKEN
  *     code = e4m3: nearest to x / s, ties to even, |x / s| > 448 -> 448;
  *            int8: nearest integer to x / s, ties to even, clamped to +-127.
  *   Each product and quotient above is one IEEE fp32 operation.
  *
- * k_new, v_new  [batch, num_kv_heads, head_dim] of new_dtype (FD_F16 or
- *               FD_BF16), 16-byte aligned, device.
+ * k_new, v_new  [batch, n_new, num_kv_heads, head_dim] of new_dtype (FD_F16
+ *               or FD_BF16), 16-byte aligned, device.
+ * n_new         new tokens per sequence, 1 .. 16.
  * k_cache, v_cache, kv_start_idx, block_table, block_table_stride, kv_rows,
  * page_size     as for fd_decode_attention; the caches are written.
- * positions     int32 [batch] device: the new token's index in its sequence;
- *               < 0 leaves the sequence alone.  Rows outside [0, kv_rows) or
+ * positions     int32 [batch] device: the first new token's index in its
+ *               sequence; < 0 leaves the sequence alone.  The block table
+ *               must cover positions[b] + n_new - 1.  Rows outside [0, kv_rows) or
  *               negative page ids are not written and are recorded as
  *               FD_ERR_DEVICE_BOUNDS (fd_check_device_error).
  * k_scale, v_scale  finite; > 0 for 8-bit caches.
@@ -246,16 +250,18 @@ fd_status fd_decode_attention_multi(const void *q, const void *k_cache, const vo
 fd_status fd_append_kv(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                        const int32_t *kv_start_idx, const int32_t *block_table,
                        int block_table_stride, const int32_t *positions, int64_t kv_rows,
-                       int batch, int num_kv_heads, int head_dim, int page_size, float k_scale,
-                       float v_scale, fd_scale_kind scale_kind, float *k_scales, float *v_scales,
-                       fd_dtype new_dtype, fd_dtype kv_dtype, void *workspace,
+                       int batch, int n_new, int num_kv_heads, int head_dim, int page_size,
+                       float k_scale, float v_scale, fd_scale_kind scale_kind, float *k_scales,
+                       float *v_scales, fd_dtype new_dtype, fd_dtype kv_dtype, void *workspace,
                        size_t workspace_bytes, fd_stream_t stream);
 
 /*
- * One decode step with its KV append: fd_append_kv of the step's new token
- * (k_new, v_new of q_dtype, at `positions`), then fd_decode_attention_scaled
- * over the caches that now hold it, in one call.  seq_len counts the new
- * token (typically positions[b] + 1).  The split kernel of the attention is
+ * One decode (q_len = 1) or verify (q_len > 1) step with its KV append:
+ * fd_append_kv of the step's q_len new tokens (k_new, v_new
+ * [batch, q_len, num_kv_heads, head_dim] of q_dtype, the first at
+ * `positions`), then fd_decode_attention_multi over the caches that now hold
+ * them, in one call.  seq_len counts the new tokens (typically
+ * positions[b] + q_len).  The split kernel of the attention is
  * launched as a programmatic dependent of the append: its plan overlaps the
  * append, and it waits for the append's writes before reading K/V.
  * Arguments and errors are those of the two functions; nothing is launched
@@ -265,7 +271,7 @@ fd_status fd_decode_attention_append(const void *q, const void *k_new, const voi
                                      void *k_cache, void *v_cache, const int32_t *kv_start_idx,
                                      const int32_t *block_table, int block_table_stride,
                                      const int32_t *positions, const int32_t *seq_len,
-                                     int64_t kv_rows, int batch, int num_q_heads,
+                                     int64_t kv_rows, int batch, int q_len, int num_q_heads,
                                      int num_kv_heads, int head_dim, int page_size,
                                      float softmax_scale, float k_scale, float v_scale,
                                      fd_scale_kind scale_kind, float *k_scales, float *v_scales,

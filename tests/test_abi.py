@@ -111,13 +111,13 @@ def test_scaled_host_validation(fda, kind, ks, vs, kvdt, status):
 def _call_append(fda, **over):
     """fd_append_kv with fake pointers; only argument errors are asked for."""
     a = dict(kn=0x1000, vn=0x2000, k=0x3000, v=0x4000, kv_start=0x5000, bt=None, bt_stride=0,
-             pos=0x6000, kv_rows=100, batch=2, kvh=2, d=128, page=0, ks=1.0, vs=1.0, kind=0,
-             kss=None, vss=None, ndt=0, kvdt=2, ws=0x8000, wsb=256)
+             pos=0x6000, kv_rows=100, batch=2, n_new=1, kvh=2, d=128, page=0, ks=1.0, vs=1.0,
+             kind=0, kss=None, vss=None, ndt=0, kvdt=2, ws=0x8000, wsb=256)
     a.update(over)
     return fda.load_library().fd_append_kv(
         a["kn"], a["vn"], a["k"], a["v"], a["kv_start"], a["bt"], a["bt_stride"], a["pos"],
-        a["kv_rows"], a["batch"], a["kvh"], a["d"], a["page"], a["ks"], a["vs"], a["kind"],
-        a["kss"], a["vss"], a["ndt"], a["kvdt"], a["ws"], a["wsb"], None)
+        a["kv_rows"], a["batch"], a["n_new"], a["kvh"], a["d"], a["page"], a["ks"], a["vs"],
+        a["kind"], a["kss"], a["vss"], a["ndt"], a["kvdt"], a["ws"], a["wsb"], None)
 
 
 @pytest.mark.parametrize("over,status", [
@@ -138,6 +138,8 @@ def _call_append(fda, **over):
     (dict(kind=1), 1),                                     # head scales missing
     (dict(wsb=128), 3),                                    # workspace below the header
     (dict(batch=0), 1),
+    (dict(n_new=0), 1),
+    (dict(n_new=17), 1),
 ])
 def test_append_host_validation(fda, over, status):
     assert _call_append(fda, **over) == status
@@ -147,8 +149,8 @@ def test_decode_with_append_validates_the_append(fda):
     """fd_decode_attention_append refuses a missing new row before any launch."""
     lib = fda.load_library()
     st = lib.fd_decode_attention_append(0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, None, 0,
-                                        0x6000, 0x7000, 100, 2, 8, 2, 128, 0, 0.125, 1.0, 1.0, 0,
-                                        None, None, 0, 2, 0x8000, 0x9000, 0xA000, 1 << 20, None)
+                                        0x6000, 0x7000, 100, 2, 1, 8, 2, 128, 0, 0.125, 1.0, 1.0,
+                                        0, None, None, 0, 2, 0x8000, 0x9000, 0xA000, 1 << 20, None)
     assert st == 1
 
 

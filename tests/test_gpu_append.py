@@ -98,15 +98,16 @@ def test_append_matches_oracle(i):
 
 
 def _fused(w, seed, kernel=0):
-    """fd_decode_attention_append on device copies; returns (exp, t, out, lse)."""
+    """fd_decode_attention_append on device copies (w.q_len new tokens per
+    sequence); returns (exp, t, out, lse)."""
     fda = lib()
-    k_new, v_new = fw.new_tokens(w, seed, std=2.0)
-    pos = fw.last_positions(w)
+    k_new, v_new = fw.new_tokens(w, seed, std=2.0, n_new=w.q_len)
+    pos = fw.last_positions(w, w.q_len)
     exp = _expected(w, k_new, v_new, pos)
     t = _device_inputs(w, k_new, v_new, pos)
     out = torch.full(t["q"].shape, float("nan"), dtype=t["q"].dtype, device="cuda")
-    lse = torch.full(t["q"].shape[:2], float("nan"), dtype=torch.float32, device="cuda")
-    ws = fda.alloc_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim)
+    lse = torch.full(t["q"].shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
+    ws = fda.alloc_workspace(w.batch, w.num_q_heads * w.q_len, w.num_kv_heads, w.head_dim)
     fda.fd_set_kernel(kernel)
     try:
         fda.fd_decode_attention_append(
@@ -175,3 +176,28 @@ def test_append_out_of_range_is_reported_and_not_written():
     _check_caches(w, exp, t)
     st, info = fda.fd_check_device_error(ws)
     assert st == fda.FD_ERR_DEVICE_BOUNDS, (fda.fd_status_string(st), info)
+
+
+@pytest.mark.parametrize("q_len", [2, 4])
+@pytest.mark.parametrize("i", [0, 2, 5, 6], ids=[CASES[i].name for i in (0, 2, 5, 6)])
+def test_verify_step_with_append(i, q_len):
+    """A speculative verify step in one call: its q_len drafted tokens are
+    appended (token j at position seq_len - q_len + j) and attended to
+    causally; caches as the oracle's append, outputs as its attention."""
+    w = fw.with_q_len(CASES[i], q_len, 600 + i)
+    exp, t, out, lse = _fused(w, 610 + i)
+    _check_caches(w, exp, t)
+    ref_out, ref_lse = oracle.decode_attention(exp)
+    parity(exp, out.float().cpu().numpy().astype(np.float64),
+           lse.cpu().numpy().astype(np.float64), ref_out, ref_lse, label=f"{w.name} verify")
+
+
+@pytest.mark.parametrize("n,q_len", [(4, 2), (5, 4)])
+def test_config_full_size_verify_with_append(n, q_len):
+    w = fw.with_q_len(fw.WORKLOADS[n](), q_len, 620 + n)
+    exp, t, out, lse = _fused(w, 630 + n)
+    _check_caches(w, exp, t)
+    ref_out, ref_lse = oracle.decode_attention(exp)
+    parity(exp, out.float().cpu().numpy().astype(np.float64),
+           lse.cpu().numpy().astype(np.float64), ref_out, ref_lse,
+           label=f"config{n}-q{q_len} verify")
