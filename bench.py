@@ -103,20 +103,27 @@ def whole_job_throughput(units_per_rank: float, world: int, max_seconds: float) 
 # CPU baseline: the oracle as it stands, on the host cores
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w: fw.Workload, budget_s: float, nthreads: int = 0):
-    """Times the oracle on whole sequences (all query heads) of the workload,
-    taken in order until about `budget_s` seconds of wall time; returns
-    (GB/s by the algorithmic-bytes formula, threads used, description)."""
+def oracle_sample(w: fw.Workload, budget_s: float, nthreads: int = 0, start: int = 0):
+    """Times the oracle on the workload's (sequence, KV head) units -- the
+    query heads of one KV head of one sequence; with a budget of a second or
+    more, whole sequences per call -- taken in order from unit `start`
+    (wrapping) until about `budget_s` seconds of wall time; returns (GB/s by
+    the algorithmic-bytes formula, threads used, description, seconds)."""
     import oracle
     orc = oracle.default()
+    g = w.num_q_heads // w.num_kv_heads
+    per_call = w.num_kv_heads if budget_s >= 1.0 else 1     # KV heads per oracle call
+    calls_per_seq = w.num_kv_heads // per_call
+    n_calls = w.batch * calls_per_seq
     done_bytes = 0
     elapsed = 0.0
     threads = 0
-    nseq = 0
-    heads = w.num_q_heads
-    per_seq_qo = 2 * heads * w.q_len * w.head_dim * 2
-    for b in range(w.batch):
-        pairs = [(b, h) for h in range(heads)]
+    calls = 0
+    for c in range(n_calls):
+        u = (start + c) % n_calls
+        b, h0 = u // calls_per_seq, (u % calls_per_seq) * per_call
+        T = int(w.seq_len[b])
+        pairs = [(b, h) for h in range(h0 * g, (h0 + per_call) * g)]
         t0 = time.perf_counter()
         _, _, _, threads = orc.decode_attention_raw(
             w.q, w.q_dtype, w.k_cache, w.v_cache, w.kv_dtype, w.seq_len, w.num_q_heads,
@@ -125,14 +132,17 @@ def oracle_sample(w: fw.Workload, budget_s: float, nthreads: int = 0):
             kv_rows=w.kv_rows, pairs=pairs, scale_kind=w.scale_kind, k_scales=w.k_scales,
             v_scales=w.v_scales, q_len=w.q_len, nthreads=nthreads)
         elapsed += time.perf_counter() - t0
-        T = int(w.seq_len[b])
-        idx = (4 + 4 * (-(-T // w.page_size))) if w.paged else 8
-        done_bytes += T * w.num_kv_heads * w.head_dim * w.kv_elem_bytes * 2 + per_seq_qo + idx
-        nseq += 1
+        done_bytes += per_call * (T * w.head_dim * w.kv_elem_bytes * 2
+                                  + 2 * g * w.q_len * w.head_dim * 2)
+        if h0 == 0:   # index bytes, once per sequence
+            done_bytes += (4 + 4 * (-(-T // w.page_size))) if w.paged else 8
+        calls += 1
         if elapsed >= budget_s:
             break
     gbs = done_bytes / elapsed / 1e9 if elapsed > 0 else 0.0
-    desc = (f"{nseq} of {w.batch} sequences (all {heads} query heads each), "
+    what = "sequences (all query heads)" if per_call == w.num_kv_heads else \
+        f"(sequence, KV head) units ({g} query heads each)"
+    desc = (f"{calls} of {n_calls} {what} from unit {start % n_calls}, "
             f"{done_bytes / 1e6:.1f} MB algorithmic, {elapsed:.2f} s")
     return gbs, threads, desc, elapsed
 
@@ -184,6 +194,9 @@ def run_reference(args):
     gbs_all = []
     threads = 0
     desc = ""
+    # each step samples the oracle for a bounded time, so that the whole
+    # --steps / --warmup run stays within about two minutes
+    budget = min(2.0, max(0.02, 120.0 / max(1, args.warmup + args.steps)))
     for i in range(args.warmup + args.steps):
         if args.append:
             # the oracle's append of the whole batch, then the attention sample
@@ -197,13 +210,13 @@ def run_reference(args):
             wa = dataclasses.replace(w, k_cache=kc, v_cache=vc)
             if w.scale_kind == fw.SCALE_TOKEN:
                 wa = dataclasses.replace(wa, k_scales=ks, v_scales=vs)
-            gbs, threads, desc, el = oracle_sample(wa, budget_s=2.0)
+            gbs, threads, desc, el = oracle_sample(wa, budget_s=budget, start=i)
             el_all = el + t_app
             gbs = (gbs * el + fw.append_bytes(w, w.q_len) / 1e9) / el_all
             el = el_all
             desc += f"; plus the append of all {w.batch} new tokens ({t_app:.3f} s)"
         else:
-            gbs, threads, desc, el = oracle_sample(w, budget_s=2.0)
+            gbs, threads, desc, el = oracle_sample(w, budget_s=budget, start=i)
         if i >= args.warmup:
             per_step.append(el)
             gbs_all.append(gbs)
