@@ -98,3 +98,25 @@ def test_mutated_oracle_fails_a_pin(tmp_path, mutation):
             caught.append(pin.__name__)
             break
     assert caught, f"no pin catches the mutation: {what}"
+
+
+def test_golden_fixtures(orc):
+    """The oracle reproduces its frozen fixtures (tests/golden) to 1e-12
+    relative: guards against silent changes of its arithmetic and against a
+    host whose libm rounds differently."""
+    import importlib.util
+    import json
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    spec = importlib.util.spec_from_file_location("make_golden", os.path.join(here, "make_golden.py"))
+    mg = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mg)
+    for name, w, _ in mg.cases():
+        doc = json.load(open(os.path.join(here, name)))
+        ref_out = np.array([float.fromhex(x) for x in doc["out"]]).reshape(doc["out_shape"])
+        ref_lse = np.array([float.fromhex(x) for x in doc["lse"]]).reshape(doc["lse_shape"])
+        out, lse = orc.decode_attention(w)
+        assert out.shape == ref_out.shape and lse.shape == ref_lse.shape, name
+        assert np.allclose(out, ref_out, rtol=1e-12, atol=1e-14), name
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(fin, np.isfinite(lse)) and np.array_equal(lse[~fin], ref_lse[~fin])
+        assert np.allclose(lse[fin], ref_lse[fin], rtol=1e-12, atol=1e-14), name
