@@ -21,11 +21,13 @@ def _plan_cases():
         fw.make_contiguous("p2", 2, list(rng.integers(0, 5000, 40)), 32, 8, 128, "bf16", "bf16"),
         fw.make_contiguous("p3", 3, [40000, 3], 64, 8, 64, "f16", "e4m3"),
         fw.make_contiguous("p4", 4, [131072], 16, 1, 128, "f16", "e4m3"),
+        # more streams than threads per CTA (the plan's multi-pass branch)
+        fw.make_contiguous("p5", 6, list(rng.integers(0, 300, 700)), 8, 8, 64, "f16", "e4m3"),
     ]
 
 
 @pytest.mark.parametrize("kernel", [1, 2])
-@pytest.mark.parametrize("case", range(5))
+@pytest.mark.parametrize("case", range(6))
 def test_device_plan_matches_restatement(kernel, case):
     fda = lib()
     w = _plan_cases()[case]
