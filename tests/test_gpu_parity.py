@@ -229,3 +229,63 @@ def test_nondefault_stream():
     s = torch.cuda.Stream()
     out, lse, _, _ = run(w, 0, stream=s)
     parity(w, out, lse, ref[0], ref[1], label="side stream")
+
+
+def test_cache_offsets_beyond_int32_elements():
+    """Sequences whose rows lie past 2^31 cache elements (8 KV heads x 128
+    dims = 1024 elements per row, rows from 2.1 M on): every element offset
+    the kernels form must be 64-bit.  Contiguous and paged (page ids above
+    2^31 / (16 x 1024))."""
+    import dataclasses
+    lead = 2_100_000
+    w = fw.make_contiguous("beyond-int32", 90, [5, 300, 1000], 64, 8, 128, "f16", "e4m3", lead=lead)
+    assert w.kv_rows * 8 * 128 > 2 ** 31
+    check_workload(w)
+    # paged: the same rows at page ids from 135,000 on in a 140,000-page pool
+    P, pool, base = 16, 140_000, 135_000
+    assert base * P * 8 * 128 > 2 ** 31
+    k = np.full((pool, P, 8, 128), fw.POISON_E4M3, np.uint8)
+    v = np.full((pool, P, 8, 128), fw.POISON_E4M3, np.uint8)
+    npages = [-(-int(t) // P) for t in w.seq_len]
+    table = np.full((w.batch, max(npages)), -1, np.int32)
+    nxt = base
+    for b in range(w.batch):
+        s0, T = int(w.kv_start_idx[b]), int(w.seq_len[b])
+        for j in range(npages[b]):
+            lo, hi = j * P, min(T, (j + 1) * P)
+            k[nxt, : hi - lo] = w.k_cache[s0 + lo:s0 + hi]
+            v[nxt, : hi - lo] = w.v_cache[s0 + lo:s0 + hi]
+            table[b, j] = nxt
+            nxt += 1
+    wp = dataclasses.replace(w, name="beyond-int32-paged16", k_cache=k, v_cache=v, page_size=P,
+                             kv_start_idx=None, block_table=table)
+    check_workload(wp)
+
+
+@pytest.mark.parametrize("qh,kvh", [(64, 8), (16, 16)])
+def test_multi_token_max_q_len(qh, kvh):
+    """q_len 16, the largest: with 8 query heads per KV head that is 128 rows
+    per KV head (8 MMA row tiles)."""
+    w = fw.make_contiguous(f"q16-{qh}-{kvh}", 91, [1, 16, 17, 500], qh, kvh, 128, "f16", "e4m3",
+                           gap=1, q_len=16)
+    ref = oracle.decode_attention(w)
+    fda = lib()
+    ks = []
+    for k in (SIMT, MMA):
+        fda.fd_set_kernel(k)
+        if fda.fd_selected_kernel(qh * 16, kvh, 128, 0, 2, 0, 1) == k:
+            ks.append(k)
+        fda.fd_set_kernel(0)
+    assert ks
+    for k in ks:
+        out, lse, _, _ = run(w, k)
+        parity(w, out, lse, ref[0], ref[1], label=f"{w.name} kernel={k}")
+
+
+def test_many_sequences():
+    """4,000 short sequences: thousands of streams for the plan's multi-pass
+    branch and the combine."""
+    rng = np.random.default_rng(92)
+    lens = rng.integers(0, 70, size=4000)
+    w = fw.make_contiguous("many-4000", 93, lens, 16, 2, 128, "f16", "e4m3", gap=1)
+    check_workload(w)
