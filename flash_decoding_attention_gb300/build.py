@@ -23,6 +23,9 @@ LIB_PATH = os.path.join(OUT_DIR, "libfdattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
+# FD_NVTX=1: NVTX ranges around each phase's launch (see fd_api.cu)
+if os.environ.get("FD_NVTX") == "1":
+    NVCC_FLAGS.append("-DFD_NVTX")
 
 
 def nvcc() -> str:

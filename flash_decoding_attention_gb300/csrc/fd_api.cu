@@ -7,6 +7,20 @@
 
 #include "fd_common.cuh"
 
+// Optional NVTX ranges around the host-side launch of each phase (append,
+// split, combine), for timeline tools; built with -DFD_NVTX (FD_NVTX=1 in
+// the build environment), absent otherwise.
+#ifdef FD_NVTX
+#include <nvtx3/nvToolsExt.h>
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+#define FD_RANGE(name) NvtxRange fd_nvtx_range_(name)
+#else
+#define FD_RANGE(name) ((void)0)
+#endif
+
 namespace fd {
 
 // Tensor-core kernel entry points (fd_split_mma.cu).
@@ -329,18 +343,25 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
   p.v_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : v_scales;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  FD_RANGE("fd_decode_attention");
   if (app) {
+    FD_RANGE("fd.append");
     set_append(p, *app, q_len, k_scale, v_scale);
     if (launch_append(p, st) != cudaSuccess) return FD_ERR_CUDA;
     p.pdl = 1;
   }
   const bool timed = t_ev_before != nullptr;
   if (timed && cudaEventRecord(t_ev_before, st) != cudaSuccess) return FD_ERR_CUDA;
-  cudaError_t e = c.kernel == FD_KERNEL_MMA ? launch_split_mma(p, st) : launch_split_simt(p, st);
-  if (e != cudaSuccess) return FD_ERR_CUDA;
+  {
+    FD_RANGE("fd.split");
+    cudaError_t e = c.kernel == FD_KERNEL_MMA ? launch_split_mma(p, st) : launch_split_simt(p, st);
+    if (e != cudaSuccess) return FD_ERR_CUDA;
+  }
   if (timed && cudaEventRecord(t_ev_after, st) != cudaSuccess) return FD_ERR_CUDA;
-  e = launch_combine(p, st);
-  if (e != cudaSuccess) return FD_ERR_CUDA;
+  {
+    FD_RANGE("fd.combine");
+    if (launch_combine(p, st) != cudaSuccess) return FD_ERR_CUDA;
+  }
   return FD_OK;
 }
 
