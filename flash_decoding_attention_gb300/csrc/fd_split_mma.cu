@@ -397,7 +397,7 @@ struct Shared {
 // consumer multiplies each score by its token's K scale and each probability
 // by its token's V scale before the P V product (the softmax sum keeps the
 // unscaled probabilities).
-template <int KVT, typename QT, int D, bool TOK, int QROWS>
+template <int KVT, typename QT, int D, bool TOK, int QROWS, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     mma_split_kernel(const Params p, const Shape sh, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv,
@@ -671,10 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sub = ts * SUB * sh.r + SUB * rr;   // first token of the sub-tile in the tile
             const int left = seg.t_end - (t0 + sub);      // valid tokens from the sub-tile start
             if (left <= 0) break;
-            // valid keys of rows r and r + 8 from the sub-tile start: the
-            // segment's end, and for multi-token queries the causal limit
-            int left0 = left, left1 = left;
-            if (p.q_len > 1) {   // rows r and r + 8 stop q_len - 1 - j keys before the end
+            int left0 = left, left1 = left;   // valid keys of rows r and r + 8 (see below)
+            if (TOK && p.q_len > 1) {
               const int tail = seg.T - (t0 + sub);
               left0 = min(left, tail - (p.q_len - 1 - h0 % p.q_len));
               left1 = min(left, tail - (p.q_len - 1 - h1 % p.q_len));
@@ -743,7 +741,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             // ---- online softmax (rows r and r + 8; this lane holds tokens
-            //      8*jn + 2q + {0,1} of the sub-tile)
+            //      8*jn + 2q + {0,1} of the sub-tile).  Keys past the segment
+            //      end are masked; with multi-token queries rows r and r + 8
+            //      (token j of their head) also stop q_len - 1 - j keys before
+            //      the sequence's end: folded into the same test in the
+            //      per-token-scale kernels, a separate pass near the end in
+            //      the others (either way fewer registers).
             float pr[NJ][4];
             float mx0 = -INFINITY, mx1 = -INFINITY;
             // per-token scales of this warp's KV head in the stage (TOK):
@@ -764,11 +767,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tok = 8 * jn + 2 * q + (e & 1);
                 float v = s[jn][e] * sc;
                 if constexpr (TOK) v *= (e & 1) ? kk2.y : kk2.x;
-                if (edge && tok >= ((e & 2) ? left1 : left0)) v = -INFINITY;   // ragged end
+                if (edge && tok >= ((e & 2) ? left1 : left0)) v = -INFINITY;
                 pr[jn][e] = v;
               }
               mx0 = fmaxf(mx0, fmaxf(pr[jn][0], pr[jn][1]));
               mx1 = fmaxf(mx1, fmaxf(pr[jn][2], pr[jn][3]));
+            }
+            if (CAUSAL && !TOK) {
+              const int tail = seg.T - (t0 + sub);
+              const int lim0 = tail - (p.q_len - 1 - h0 % p.q_len);
+              const int lim1 = tail - (p.q_len - 1 - h1 % p.q_len);
+              if (min(lim0, lim1) < SUB) {
+                mx0 = mx1 = -INFINITY;
+#pragma unroll
+                for (int jn = 0; jn < NJ; ++jn) {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int tok = 8 * jn + 2 * q + (e & 1);
+                    if (tok >= ((e & 2) ? lim1 : lim0)) pr[jn][e] = -INFINITY;
+                  }
+                  mx0 = fmaxf(mx0, fmaxf(pr[jn][0], pr[jn][1]));
+                  mx1 = fmaxf(mx1, fmaxf(pr[jn][2], pr[jn][3]));
+                }
+              }
             }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
@@ -1127,9 +1148,11 @@ struct Maps {
   CUtensorMap k, v, ks, vs;   // caches; per-token scale arrays (when sh.scale_tma)
 };
 
-template <int KVT, typename QT, int D, bool TOK, int QROWS = 16>
+// CAUSAL: multi-token queries (q_len > 1) without per-token scales; the
+// per-token-scale kernels fold the causal limit into their ragged-end test.
+template <int KVT, typename QT, int D, bool TOK, int QROWS = 16, bool CAUSAL = false>
 cudaError_t launch_t(const Params& p, const Shape& sh, const Maps& m, cudaStream_t stream) {
-  auto kern = mma_split_kernel<KVT, QT, D, TOK, QROWS>;
+  auto kern = mma_split_kernel<KVT, QT, D, TOK, QROWS, CAUSAL>;
   static int configured = 0;
   if (configured < sh.smem_bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1139,6 +1162,13 @@ cudaError_t launch_t(const Params& p, const Shape& sh, const Maps& m, cudaStream
   }
   return launch_split(p, kern, dim3(p.grid), dim3(kThreads), sh.smem_bytes, stream, p, sh, m.k,
                       m.v, m.ks, m.vs);
+}
+
+// Without per-token scales: one query token per sequence, or several.
+template <int KVT, typename QT, int D>
+cudaError_t launch_plain(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st) {
+  return p.q_len > 1 ? launch_t<KVT, QT, D, false, 16, true>(p, sh, m, st)
+                     : launch_t<KVT, QT, D, false, 16, false>(p, sh, m, st);
 }
 
 // 8-bit caches with per-token scales: all 16 Q rows, or 8.
@@ -1154,15 +1184,15 @@ cudaError_t launch_8bit(const Params& p, const Shape& sh, const Maps& m, cudaStr
   const bool tok = p.scale_kind == FD_SCALE_TOKEN;
   if (p.q_dtype == FD_F16)
     return tok ? launch_tok<KVT, __half, D>(p, sh, m, st)
-               : launch_t<KVT, __half, D, false>(p, sh, m, st);
+               : launch_plain<KVT, __half, D>(p, sh, m, st);
   return tok ? launch_tok<KVT, __nv_bfloat16, D>(p, sh, m, st)
-             : launch_t<KVT, __nv_bfloat16, D, false>(p, sh, m, st);
+             : launch_plain<KVT, __nv_bfloat16, D>(p, sh, m, st);
 }
 
 template <int D>
 cudaError_t launch_d(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st) {
-  if (p.kv_dtype == FD_F16) return launch_t<FD_F16, __half, D, false>(p, sh, m, st);
-  if (p.kv_dtype == FD_BF16) return launch_t<FD_BF16, __nv_bfloat16, D, false>(p, sh, m, st);
+  if (p.kv_dtype == FD_F16) return launch_plain<FD_F16, __half, D>(p, sh, m, st);
+  if (p.kv_dtype == FD_BF16) return launch_plain<FD_BF16, __nv_bfloat16, D>(p, sh, m, st);
   if (p.kv_dtype == FD_I8) return launch_8bit<FD_I8, D>(p, sh, m, st);
   return launch_8bit<FD_E4M3, D>(p, sh, m, st);
 }
