@@ -598,6 +598,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // local query heads (within the stream) of rows r and r + 8
     const int h0 = mtile * 16 + r, h1 = h0 + 8;
     const bool v0 = h0 < G, v1 = h1 < G;
+    // multi-token kernels: rows r and r + 8 (token j of their head) stop
+    // q_len - 1 - j keys before the sequence's end
+    int cut0 = 0, cut1 = 0;
+    if constexpr (CAUSAL) {
+      cut0 = p.q_len - 1 - h0 % p.q_len;
+      cut1 = p.q_len - 1 - h1 % p.q_len;
+    }
     const int li0 = kvl * G + h0, li1 = kvl * G + h1;   // slot rows
     // this head tile's Q fragments in shared memory: [kk][lane] x 16 bytes
     const uint32_t qf = qfrag0 + (uint32_t)ht * KSTEPS * (QROWS * 32) + lane * (QROWS);
@@ -775,8 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (CAUSAL && !TOK) {
               const int tail = seg.T - (t0 + sub);
-              const int lim0 = tail - (p.q_len - 1 - h0 % p.q_len);
-              const int lim1 = tail - (p.q_len - 1 - h1 % p.q_len);
+              const int lim0 = tail - cut0, lim1 = tail - cut1;
               if (min(lim0, lim1) < SUB) {
                 mx0 = mx1 = -INFINITY;
 #pragma unroll
