@@ -29,7 +29,7 @@ import numpy as np  # noqa: E402
 
 import fd_workloads as fw  # noqa: E402
 
-METRIC = "decode-attention effective HBM GB/s (% of GB300 peak) and us per decode step"
+METRIC = "decode-attention effective HBM GB/s (% of GB300 peak) and \u00b5s per decode step"
 FALLBACK_HBM_GBS = 6800.0
 
 
