@@ -53,6 +53,7 @@ EXPORTED = [
     "fd_set_kernel", "fd_selected_kernel", "fd_set_split_events", "fd_debug_read_plan",
     "fd_debug_gather_kv", "fd_decode_attention_noalloc", "fd_decode_attention_scaled",
     "fd_append_kv", "fd_decode_attention_append", "fd_decode_attention_multi",
+    "fd_debug_set_wait_limit", "fd_debug_plan_segments",
 ]
 
 
@@ -118,6 +119,12 @@ def load_library(path: Optional[str] = None):
         lib.fd_debug_gather_kv.restype = i32
         lib.fd_debug_gather_kv.argtypes = [vp, vp, vp, i32, vp, i64, i32, i32, i32, i32, i32, vp,
                                            vp, vp]
+        lib.fd_debug_set_wait_limit.restype = i32
+        lib.fd_debug_set_wait_limit.argtypes = [i64, i32]
+        lib.fd_debug_plan_segments.restype = i32
+        lib.fd_debug_plan_segments.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                               vp, i64, i32, ctypes.POINTER(ctypes.c_int), vp, sz,
+                                               vp]
         if path is None:
             _lib = lib
         return lib
@@ -372,6 +379,40 @@ def fd_debug_gather_kv(cache, kv_start_idx, block_table, seq_len, kv_rows, num_k
         _stream_handle(stream))
     if st != FD_OK:
         raise FdError(st, "fd_debug_gather_kv")
+
+
+def fd_debug_set_wait_limit(wait_ns: int, starve_first_stage: bool = False) -> None:
+    st = load_library().fd_debug_set_wait_limit(int(wait_ns), int(bool(starve_first_stage)))
+    if st != FD_OK:
+        raise FdError(st, "fd_debug_set_wait_limit")
+
+
+def fd_debug_plan_segments(seq_len, q_len: int, num_q_heads: int, num_kv_heads: int,
+                           head_dim: int, paged: bool, page_size: int, q_dtype: int,
+                           kv_dtype: int, workspace, capacity_per_cta: int = 64, stream=None):
+    """Segments (stream, t_begin, t_end, complete, slot) of every CTA of the
+    split kernel for these sizes, as the device plans them: a list with one
+    list of tuples per CTA."""
+    sms = torch.cuda.get_device_properties(seq_len.device).multi_processor_count
+    rows = 1 + 5 * capacity_per_cta
+    dst = torch.full((4 * sms * rows,), -1, dtype=torch.int32, device=seq_len.device)
+    grid = ctypes.c_int(0)
+    st = load_library().fd_debug_plan_segments(
+        _ptr(seq_len), int(seq_len.shape[0]), int(q_len), int(num_q_heads), int(num_kv_heads),
+        int(head_dim), int(bool(paged)), int(page_size), int(q_dtype), int(kv_dtype), _ptr(dst),
+        dst.numel(), int(capacity_per_cta), ctypes.byref(grid), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != FD_OK:
+        raise FdError(st, "fd_debug_plan_segments")
+    torch.cuda.synchronize(seq_len.device)
+    d = dst[:grid.value * rows].view(grid.value, rows).cpu().tolist()
+    out = []
+    for r in d:
+        n = r[0]
+        if n > capacity_per_cta:
+            raise RuntimeError(f"a CTA has {n} segments, more than capacity {capacity_per_cta}")
+        out.append([tuple(r[1 + 5 * k: 6 + 5 * k]) for k in range(n)])
+    return out
 
 
 # ---------------------------------------------------------------------------

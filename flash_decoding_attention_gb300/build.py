@@ -18,7 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
-LIB_PATH = os.path.join(OUT_DIR, "libfdattn.so")
+# FD_STAMPS=1: per-CTA %globaltimer stamps of each phase in the split and
+# combine kernels, read back with fd_debug_read_stamps (a separate library)
+STAMPS = os.environ.get("FD_STAMPS") == "1"
+LIB_PATH = os.path.join(OUT_DIR, "libfdattn_stamps.so" if STAMPS else "libfdattn.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -26,6 +29,8 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompil
 # FD_NVTX=1: NVTX ranges around each phase's launch (see fd_api.cu)
 if os.environ.get("FD_NVTX") == "1":
     NVCC_FLAGS.append("-DFD_NVTX")
+if STAMPS:
+    NVCC_FLAGS.append("-DFD_STAMPS")
 
 
 def nvcc() -> str:

@@ -32,6 +32,11 @@ void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms
 namespace {
 
 std::atomic<int> g_kernel{FD_KERNEL_AUTO};
+// fd_debug_set_wait_limit: bound of the split kernel's pipeline waits (ns,
+// 0 = one second) and the switch that starves its consumers
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;
+std::atomic<long long> g_wait_ns{0};
+std::atomic<int> g_starve{0};
 thread_local cudaEvent_t t_ev_before = nullptr;
 thread_local cudaEvent_t t_ev_after = nullptr;
 
@@ -157,7 +162,85 @@ __global__ void gather_kernel(const Params p, uint8_t* dst, int row_bytes) {
   }
 }
 
+// The segments every CTA of the split kernel takes (test hook): the plan and
+// the segment walk of the split kernels, run by a grid of the same size.
+// Row c of dst: the number of segments, then per segment (stream, t_begin,
+// t_end, complete, slot), at most `cap` of them.
+__global__ void plan_segments_kernel(const Params p, int32_t* dst, int cap) {
+  __shared__ long long red[34];
+  const PlanResult plan = compute_plan(p, red);
+  if (threadIdx.x != 0) return;
+  SegmentIter it;
+  it.init(p, plan);
+  Segment seg;
+  int32_t* d = dst + (size_t)blockIdx.x * (1 + 5 * (size_t)cap);
+  int k = 0;
+  while (it.next(p, seg)) {
+    if (k < cap) {
+      int32_t* e = d + 1 + 5 * k;
+      e[0] = seg.s;
+      e[1] = seg.t_begin;
+      e[2] = seg.t_end;
+      e[3] = seg.complete ? 1 : 0;
+      e[4] = seg.slot;
+    }
+    ++k;
+  }
+  d[0] = k;
+}
+
 }  // namespace
+}  // namespace fd
+
+namespace fd {
+// Host-side checks of a decode call's arguments, in the order every entry
+// point applies them; `workspace` is only checked for presence and alignment
+// (the no-allocation entry point passes its own array).
+fd_status check_decode_args(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* kv_start_idx, const int32_t* block_table,
+                            int block_table_stride, const int32_t* seq_len, int64_t kv_rows,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int page_size, float softmax_scale, float k_scale, float v_scale,
+                            fd_scale_kind scale_kind, const float* k_scales,
+                            const float* v_scales, fd_dtype q_dtype, fd_dtype kv_dtype,
+                            const void* out, const float* lse, const void* workspace, int q_len) {
+  // q_len query tokens per sequence run as q_len virtual query heads per head
+  if (q_len < 1 || q_len > 16) return FD_ERR_INVALID_ARG;
+  if (num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
+      (num_q_heads / num_kv_heads) * q_len > 128)
+    return FD_ERR_UNSUPPORTED;
+  if (scale_kind != FD_SCALE_TENSOR && scale_kind != FD_SCALE_HEAD &&
+      scale_kind != FD_SCALE_TOKEN)
+    return FD_ERR_INVALID_ARG;
+  if (scale_kind != FD_SCALE_TENSOR) {
+    if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4))
+      return FD_ERR_INVALID_ARG;
+    if (kv_elem_bytes(kv_dtype) != 1) return FD_ERR_UNSUPPORTED;
+  }
+  if (!q || !k_cache || !v_cache || !seq_len || !out || !workspace) return FD_ERR_INVALID_ARG;
+  if ((kv_start_idx == nullptr) == (block_table == nullptr)) return FD_ERR_INVALID_ARG;
+  if (batch <= 0 || batch > (1 << 24)) return FD_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return FD_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > 128 || num_q_heads > 4096) return FD_ERR_UNSUPPORTED;
+  if (kv_rows <= 0 || kv_rows > (int64_t(1) << 40)) return FD_ERR_INVALID_ARG;
+  const int paged = block_table != nullptr;
+  if (paged) {
+    if (!is_pow2(page_size) || page_size > 256) return FD_ERR_UNSUPPORTED;
+    if (block_table_stride <= 0 || kv_rows % page_size != 0) return FD_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return FD_ERR_INVALID_ARG;
+  if (q_dtype != FD_F16 && q_dtype != FD_BF16) return FD_ERR_INVALID_ARG;
+  if (kv_dtype != FD_F16 && kv_dtype != FD_BF16 && kv_dtype != FD_E4M3 && kv_dtype != FD_I8)
+    return FD_ERR_INVALID_ARG;
+  if (!dtypes_ok(q_dtype, kv_dtype)) return FD_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return FD_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
+    return FD_ERR_INVALID_ARG;
+  return FD_OK;
+}
 }  // namespace fd
 
 using namespace fd;
@@ -240,6 +323,7 @@ fd_status fd_decode_attention(const void* q, const void* k_cache, const void* v_
                                     out, lse, workspace, workspace_bytes, stream);
 }
 
+
 // The attention of one decode step, optionally preceded by the KV append of
 // the step's new token (then the split kernel runs as a programmatic
 // dependent of the append and waits for it before reading the caches).
@@ -252,42 +336,13 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
                              const float* v_scales, fd_dtype q_dtype, fd_dtype kv_dtype, void* out,
                              float* lse, void* workspace, size_t workspace_bytes,
                              fd_stream_t stream, const AppendArgs* app, int q_len = 1) {
-  // q_len query tokens per sequence run as q_len virtual query heads per head
-  if (q_len < 1 || q_len > 16) return FD_ERR_INVALID_ARG;
-  if (num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
-      (num_q_heads / num_kv_heads) * q_len > 128)
-    return FD_ERR_UNSUPPORTED;
+  const fd_status chk = check_decode_args(
+      q, k_cache, v_cache, kv_start_idx, block_table, block_table_stride, seq_len, kv_rows, batch,
+      num_q_heads, num_kv_heads, head_dim, page_size, softmax_scale, k_scale, v_scale, scale_kind,
+      k_scales, v_scales, q_dtype, kv_dtype, out, lse, workspace, q_len);
+  if (chk != FD_OK) return chk;
   const int virt_heads = num_q_heads * q_len;
-  if (scale_kind != FD_SCALE_TENSOR && scale_kind != FD_SCALE_HEAD &&
-      scale_kind != FD_SCALE_TOKEN)
-    return FD_ERR_INVALID_ARG;
-  if (scale_kind != FD_SCALE_TENSOR) {
-    if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4))
-      return FD_ERR_INVALID_ARG;
-    if (kv_elem_bytes(kv_dtype) != 1) return FD_ERR_UNSUPPORTED;
-  }
-  if (!q || !k_cache || !v_cache || !seq_len || !out || !workspace) return FD_ERR_INVALID_ARG;
-  if ((kv_start_idx == nullptr) == (block_table == nullptr)) return FD_ERR_INVALID_ARG;
-  if (batch <= 0 || batch > (1 << 24)) return FD_ERR_INVALID_ARG;
-  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
-    return FD_ERR_INVALID_ARG;
-  if (num_q_heads / num_kv_heads > 128 || num_q_heads > 4096) return FD_ERR_UNSUPPORTED;
-  if (kv_rows <= 0 || kv_rows > (int64_t(1) << 40)) return FD_ERR_INVALID_ARG;
   const int paged = block_table != nullptr;
-  if (paged) {
-    if (!is_pow2(page_size) || page_size > 256) return FD_ERR_UNSUPPORTED;
-    if (block_table_stride <= 0 || kv_rows % page_size != 0) return FD_ERR_INVALID_ARG;
-  }
-  if (!std::isfinite(softmax_scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
-    return FD_ERR_INVALID_ARG;
-  if (q_dtype != FD_F16 && q_dtype != FD_BF16) return FD_ERR_INVALID_ARG;
-  if (kv_dtype != FD_F16 && kv_dtype != FD_BF16 && kv_dtype != FD_E4M3 && kv_dtype != FD_I8)
-    return FD_ERR_INVALID_ARG;
-  if (!dtypes_ok(q_dtype, kv_dtype)) return FD_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return FD_ERR_UNSUPPORTED;
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-      !aligned(workspace, 256) || (lse && !aligned(lse, 4)))
-    return FD_ERR_INVALID_ARG;
   if (app) {
     const fd_status st = check_append(*app, kv_dtype, k_scale, v_scale);
     if (st != FD_OK) return st;
@@ -341,6 +396,9 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
   p.scale_kind = scale_kind;
   p.k_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : k_scales;
   p.v_scales = scale_kind == FD_SCALE_TENSOR ? nullptr : v_scales;
+  const long long wns = g_wait_ns.load();
+  p.wait_ns = wns > 0 ? (unsigned long long)wns : kDefaultWaitNs;
+  p.starve = g_starve.load();
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   FD_RANGE("fd_decode_attention");
@@ -487,7 +545,7 @@ fd_status fd_check_device_error(void* workspace, fd_stream_t stream, int64_t* in
   if (cudaMemsetAsync(workspace, 0, 16, st) != cudaSuccess) return FD_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return FD_ERR_CUDA;
   if (info) *info = h.error_info ? (int64_t)(h.error_info - 1) : 0;
-  if (h.error_bits & kErrTimeout) return FD_ERR_DEVICE_TIMEOUT;
+  if (h.error_bits & (kErrTimeout | kErrDrain)) return FD_ERR_DEVICE_TIMEOUT;
   if (h.error_bits & (kErrBounds | kErrPlan)) return FD_ERR_DEVICE_BOUNDS;
   return FD_OK;
 }
@@ -508,6 +566,52 @@ fd_status fd_debug_read_plan(const void* workspace, fd_stream_t stream, int32_t*
     return FD_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return FD_ERR_CUDA;
   return FD_OK;
+}
+
+fd_status fd_debug_set_wait_limit(int64_t wait_ns, int starve_first_stage) {
+  if (wait_ns < 0 || wait_ns > (int64_t)10000000000LL) return FD_ERR_INVALID_ARG;
+  g_wait_ns.store((long long)wait_ns);
+  g_starve.store(starve_first_stage ? 1 : 0);
+  return FD_OK;
+}
+
+fd_status fd_debug_plan_segments(const int32_t* seq_len, int batch, int q_len, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int paged, int page_size,
+                                 fd_dtype q_dtype, fd_dtype kv_dtype, int32_t* dst,
+                                 int64_t dst_len, int capacity_per_cta, int* grid_out,
+                                 void* workspace,
+                                 size_t workspace_bytes, fd_stream_t stream) {
+  if (!seq_len || !dst || !workspace || !grid_out || capacity_per_cta < 1 || batch <= 0 ||
+      q_len < 1 || q_len > 16 || !aligned(workspace, 256))
+    return FD_ERR_INVALID_ARG;
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return FD_ERR_INVALID_ARG;
+  const int sms = current_sms();
+  if (sms <= 0) return FD_ERR_CUDA;
+  Config c;
+  if (!choose(g_kernel.load(), num_q_heads * q_len, num_kv_heads, head_dim, q_dtype, kv_dtype,
+              paged ? 1 : 0, paged ? page_size : 0, sms, &c))
+    return FD_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(batch * c.hg, c.grid, c.hq, head_dim);
+  if (workspace_bytes < L.total) return FD_ERR_WORKSPACE_TOO_SMALL;
+  *grid_out = c.grid;
+  if (dst_len < (int64_t)c.grid * (1 + 5 * (int64_t)capacity_per_cta)) return FD_ERR_INVALID_ARG;
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws = reinterpret_cast<WsHeader*>(ws);
+  p.prefix = reinterpret_cast<int32_t*>(ws + L.prefix_off);
+  p.seq_len = seq_len;
+  p.batch = batch;
+  p.hg = c.hg;
+  p.hq = c.hq;
+  p.tile = c.tile;
+  p.seg_units = c.seg_units;
+  p.grid = c.grid;
+  p.kernel = c.kernel;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  plan_segments_kernel<<<c.grid, 256, 0, st>>>(p, dst, capacity_per_cta);
+  return cudaGetLastError() == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
 fd_status fd_debug_gather_kv(const void* cache, const int32_t* kv_start_idx,
@@ -539,5 +643,22 @@ fd_status fd_debug_gather_kv(const void* cache, const int32_t* kv_start_idx,
   gather_kernel<<<batch, 128, 0, st>>>(p, static_cast<uint8_t*>(dst), row_bytes);
   return cudaGetLastError() == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
+
+#ifdef FD_STAMPS
+// Instrumented builds only (not in the public header): copies the phase
+// stamps of the last split (which = 0) or combine (which = 1) launch,
+// 8 per CTA, into host memory; synchronises the device.
+int fd_debug_empty_launch(int grid, int threads, int smem, fd_stream_t stream) {
+  return launch_empty(grid, threads, smem, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FD_OK
+             : FD_ERR_CUDA;
+}
+
+int fd_debug_read_stamps(int which, unsigned long long* host, int n) {
+  if (!host || n <= 0) return FD_ERR_INVALID_ARG;
+  const cudaError_t e = which == 0 ? read_split_stamps(host, n) : read_combine_stamps(host, n);
+  return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+#endif
 
 }  // extern "C"

@@ -20,6 +20,11 @@ namespace {
 
 constexpr int kCombineWarps = 8;
 
+#ifdef FD_STAMPS
+// 0 past griddepcontrol.wait, 1 merge done (warp 0), 2 stored (warp 0)
+FD_STAMP_ARRAY(g_combine_stamps);
+#endif
+
 // Segment k of a stream whose first tile is in CTA c0 -> its partial slot:
 // the first CTA's "last" slot, then each later CTA's "first" slot.
 __device__ __forceinline__ int seg_slot(int c0, int k) { return k == 0 ? 2 * c0 + 1 : 2 * (c0 + k); }
@@ -44,6 +49,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
   // wait for the split kernel (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) FD_STAMP(g_combine_stamps, 0, stamp_ns());
   const int part = warp % WPI, slot_in_cta = warp / WPI;
   const int S = p.batch * p.hg;
   const long long item = (long long)blockIdx.x * IPC + slot_in_cta;
@@ -155,6 +161,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
       acc[k] = x;
     }
   }
+  if (threadIdx.x == 0) FD_STAMP(g_combine_stamps, 1, stamp_ns());
   if (nseg == 0) return;
   // per-KV-head V scales apply here; per-token ones are inside the partials
   float vsc = p.v_scale;
@@ -183,6 +190,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Param
     for (int k = 0; k < DPL; ++k) out[lane * DPL + k] = QType<QT>::from_f32(acc[k] * r);
   }
   if (lse && lane == 0) *lse = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  if (threadIdx.x == 0) FD_STAMP(g_combine_stamps, 2, stamp_ns());
 }
 
 // Launched as a programmatic dependent of the split kernel: its CTAs may be
@@ -217,6 +225,13 @@ cudaError_t launch_t(const Params& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+#ifdef FD_STAMPS
+cudaError_t read_combine_stamps(unsigned long long* host, int n) {
+  if (n > kStampCtas * kStampSlots) n = kStampCtas * kStampSlots;
+  return cudaMemcpyFromSymbol(host, g_combine_stamps, sizeof(unsigned long long) * n);
+}
+#endif
 
 cudaError_t launch_combine(const Params& p, cudaStream_t stream) {
   if (p.q_dtype == FD_F16)

@@ -19,6 +19,7 @@ enum : uint32_t {
   kErrBounds = 1u,   // cache row or page id outside the cache
   kErrTimeout = 2u,  // a bounded wait expired
   kErrPlan = 4u,     // plan does not fit the workspace (more tiles than int32)
+  kErrDrain = 8u,    // copies still in flight when a CTA gave up waiting for them
 };
 
 struct WsHeader {
@@ -110,7 +111,35 @@ struct Params {
   float* k_scales_dst;       // FD_SCALE_TOKEN: per-token scales, written
   float* v_scales_dst;
   float k_scale_raw, v_scale_raw;   // the per-tensor scales as given
+  // Bound of every pipeline wait of the tensor-core split kernel, in ns
+  // (one second unless a test shortens it), and a test switch under which
+  // its producer issues no copy at all, so that the consumers' first wait
+  // runs out with nothing in flight (fd_debug_set_wait_limit).
+  unsigned long long wait_ns;
+  int starve;
 };
+
+// Optional phase timestamps (built with -DFD_STAMPS, a separate library):
+// slot i of CTA c in a kernel's stamp array holds %globaltimer (ns) when the
+// CTA passed phase i; fd_debug_read_stamps copies them out.
+#ifdef FD_STAMPS
+constexpr int kStampCtas = 4096, kStampSlots = 16;
+#define FD_STAMP_ARRAY(name) __device__ unsigned long long name[kStampCtas * kStampSlots]
+#define FD_STAMP(arr, i, v)                                                        \
+  do {                                                                             \
+    if (blockIdx.x < kStampCtas) arr[blockIdx.x * kStampSlots + (i)] = (v);        \
+  } while (0)
+__device__ __forceinline__ unsigned long long stamp_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+cudaError_t read_split_stamps(unsigned long long* host, int n);
+cudaError_t read_combine_stamps(unsigned long long* host, int n);
+cudaError_t launch_empty(int grid, int threads, int smem, cudaStream_t st);
+#else
+#define FD_STAMP(arr, i, v) ((void)0)
+#endif
 
 // ---------------------------------------------------------------------------
 // Split plan ("stream-K", balanced on cost).  A work stream is (sequence b,
@@ -148,7 +177,8 @@ struct PlanResult {
 // Block-wide; every thread gets the same result.  CTA 0 also writes the
 // prefix array and the plan words of the header.  `red` is >= 34 long longs
 // of shared memory.
-__device__ inline PlanResult compute_plan(const Params& p, long long* red) {
+__device__ inline PlanResult compute_plan(const Params& p, long long* red,
+                                          unsigned long long* stamp = nullptr) {
   const int S = p.batch * p.hg;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
@@ -161,6 +191,11 @@ __device__ inline PlanResult compute_plan(const Params& p, long long* red) {
   long long total = 0;
   for (int w = 0; w < nwarps; ++w) total += red[w];
   __syncthreads();
+#ifdef FD_STAMPS
+  if (stamp && tid == 0) *stamp = stamp_ns();
+#else
+  (void)stamp;
+#endif
   PlanResult r;
   r.total = total;
   r.per_cta = total > 0 ? (total + p.grid - 1) / p.grid : 0;
@@ -354,6 +389,16 @@ inline cudaError_t launch_split(const Params& p, Kernel kern, dim3 grid, dim3 bl
   cfg.numAttrs = p.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
+
+// Host-side argument checks shared by the decode entry points (fd_api.cu).
+fd_status check_decode_args(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* kv_start_idx, const int32_t* block_table,
+                            int block_table_stride, const int32_t* seq_len, int64_t kv_rows,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int page_size, float softmax_scale, float k_scale, float v_scale,
+                            fd_scale_kind scale_kind, const float* k_scales,
+                            const float* v_scales, fd_dtype q_dtype, fd_dtype kv_dtype,
+                            const void* out, const float* lse, const void* workspace, int q_len);
 
 // Launchers (defined in their .cu files).
 cudaError_t launch_split_simt(const Params& p, cudaStream_t stream);

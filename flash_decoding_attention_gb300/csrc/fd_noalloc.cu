@@ -13,7 +13,8 @@
 // library holds kStaticScratchBytes of it until the process exits.  Host code
 // cannot use the array's name as a device address; the device address is
 // looked up once per device with cudaGetSymbolAddress (while that device is
-// current) on the first call made on that device, and cached.
+// current) on the first call made on that device, and cached for the life of
+// the process (the entry point is not for use after cudaDeviceReset).
 #include <mutex>
 
 #include "fd_common.cuh"
@@ -50,8 +51,16 @@ extern "C" fd_status fd_decode_attention_noalloc(
     int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
     float softmax_scale, float k_scale, float v_scale, fd_dtype q_dtype, fd_dtype kv_dtype,
     void* out, float* lse, fd_stream_t stream) {
+  // the argument checks of fd_decode_attention first, so that both entry
+  // points give bad arguments the same status (the array stands in for the
+  // workspace, which is only checked for presence here)
+  const fd_status chk = fd::check_decode_args(
+      q, k_cache, v_cache, kv_start_idx, block_table, block_table_stride, seq_len, kv_rows, batch,
+      num_q_heads, num_kv_heads, head_dim, page_size, softmax_scale, k_scale, v_scale,
+      FD_SCALE_TENSOR, nullptr, nullptr, q_dtype, kv_dtype, out, lse, g_static_scratch, 1);
+  if (chk != FD_OK) return chk;
   const size_t need = fd_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim);
-  if (need == 0) return FD_ERR_INVALID_ARG;
+  if (need == 0) return FD_ERR_CUDA;   // valid sizes: only the device query can fail
   if (need > kStaticScratchBytes) return FD_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = scratch_for_current_device();
   if (scratch == nullptr) return FD_ERR_CUDA;

@@ -54,7 +54,9 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
 constexpr int kPageWindow = 256;   // block-table entries staged per window
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 225 * 1024;
-constexpr unsigned long long kWaitNs = 1000000000ull;
+// Bound of the exit drain (waits for copies already issued); unlike the
+// pipeline waits it is never shortened.
+constexpr unsigned long long kDrainNs = 1000000000ull;
 
 struct Shape {
   int mt;            // 16-row head tiles per KV head (power of two)
@@ -161,13 +163,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Bounded wait on a barrier phase; false on expiry.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait on a barrier phase bounded by limit_ns; false on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 255u) == 0 && global_ns() - t0 > kWaitNs) return false;
+    if ((n & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -380,6 +383,14 @@ __device__ __forceinline__ void zero_rows_past_end(W& w0, W& w1, W& w2, W& w3, i
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+#ifdef FD_STAMPS
+// 0 entry, 1 plan done, 2 first copy issued, 3 first stage landed (warp 0),
+// 4 last stage released (warp 0), 5 last segment stored (warp 0), 6 exit,
+// 7 stages consumed by warp 0, 8 plan total known, 9 producer has its first
+// segment, 10 producer has the segment's row data, 11 before the plan
+FD_STAMP_ARRAY(g_split_stamps);
+#endif
+
 struct Shared {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
@@ -421,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         sh.qfrag_bytes);   // per-token scales (TOK)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) FD_STAMP(g_split_stamps, 0, stamp_ns());
   if (threadIdx.x == 0) {
     for (int i = 0; i < sh.stages; ++i) {
       mbar_init(&sm.full[i], TOK && !sh.scale_tma ? 1 + 32 : 1);
@@ -436,7 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_map(&tmv);
   }
   prefetch_index_arrays(p);
+  if (threadIdx.x == 0) FD_STAMP(g_split_stamps, 11, stamp_ns());
+#ifdef FD_STAMPS
+  const PlanResult plan = compute_plan(p, sm.red, blockIdx.x < kStampCtas ? &g_split_stamps[blockIdx.x * kStampSlots + 8] : nullptr);
+#else
   const PlanResult plan = compute_plan(p, sm.red);   // contains __syncthreads
+#endif
+  if (threadIdx.x == 0) FD_STAMP(g_split_stamps, 1, stamp_ns());
   allow_dependent_launch();
   wait_prior_grid();   // a KV append launched just before may still be writing rows
 
@@ -454,11 +472,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     it.init(p, plan);
     Segment seg;
     long long n = 0;
-    bool stop = false;
+    bool stop = p.starve != 0;   // test switch: issue nothing, the consumers' waits run out
     while (!stop && it.next(p, seg)) {
+      if (n == 0 && lane == 0) FD_STAMP(g_split_stamps, 9, stamp_ns());
       const int b = seg.s / p.hg;
       const int kvh0 = (seg.s - b * p.hg) * sh.hc;
       const long long start = p.block_table ? 0 : (long long)__ldg(p.kv_start + b);
+#ifdef FD_STAMPS
+      if (n == 0 && lane == 0 && start >= 0) FD_STAMP(g_split_stamps, 10, stamp_ns());
+#endif
       int win_lo = 0, win_hi = 0;   // logical pages [win_lo, win_hi) held in sm.pages
       for (int t0 = seg.t_begin; t0 < seg.t_end; t0 += sh.tile, ++n) {
         const int valid = min(sh.tile, seg.t_end - t0);
@@ -478,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const int stg = (int)(n % S);
           const uint32_t ph = (uint32_t)((n / S) & 1);
-          if (*(volatile int*)&sm.abort_flag || !mbar_wait(&sm.empty[stg], ph ^ 1u)) {
+          if (*(volatile int*)&sm.abort_flag || !mbar_wait(&sm.empty[stg], ph ^ 1u, p.wait_ns)) {
             if (!*(volatile int*)&sm.abort_flag) {
               raise_error(p.ws, kErrTimeout, 1);
               *(volatile int*)&sm.abort_flag = 1;
@@ -520,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   continue;
                 }
                 if (!ok) continue;
+                if (n == 0 && i == 0) FD_STAMP(g_split_stamps, 2, stamp_ns());
                 if constexpr (TOK) {
                   if (sh.scale_tma) {   // the box rows' scales of the hc heads
                     float* sk = scl + (size_t)stg * (sh.scale_bytes / 4) +
@@ -584,9 +607,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if constexpr (TOK) asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0 && stop) {
-      // drain: copies of the last S issued tiles must land before the CTA exits
+      // drain: copies of the last S issued tiles must land before the CTA
+      // exits; a drain that gives up is recorded on its own
       for (long long i = n - S < 0 ? 0 : n - S; i < n; ++i)
-        mbar_wait(&sm.full[i % S], (uint32_t)((i / S) & 1));
+        if (!mbar_wait(&sm.full[i % S], (uint32_t)((i / S) & 1), kDrainNs))
+          raise_error(p.ws, kErrDrain, 3);
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -664,11 +689,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int stg = (int)(n % S);
         const uint32_t ph = (uint32_t)((n / S) & 1);
         bool ok = !*(volatile int*)&sm.abort_flag;
-        if (ok && !mbar_wait(&sm.full[stg], ph)) {
+        if (ok && !mbar_wait(&sm.full[stg], ph, p.wait_ns)) {
           raise_error(p.ws, kErrTimeout, 2);
           *(volatile int*)&sm.abort_flag = 1;
           ok = false;
         }
+        if (n == 0 && warp == 0 && lane == 0) FD_STAMP(g_split_stamps, 3, stamp_ns());
         if (ok && !sm.bad[stg]) {
           const uint32_t kreg = stage0 + stg * 2 * sh.kv_bytes + kvl * sh.region_bytes;
           const uint32_t xstride = sh.hc * sh.region_bytes;   // next head-dim slice
@@ -920,6 +946,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stg]);
+        if (warp == 0 && lane == 0) {
+          FD_STAMP(g_split_stamps, 4, stamp_ns());
+          FD_STAMP(g_split_stamps, 7, (unsigned long long)(n + 1));
+        }
       }
 
       // ---- end of segment: full row sums, merge the warps of a head tile
@@ -1034,9 +1064,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
       }
+      if (warp == 0 && lane == 0) FD_STAMP(g_split_stamps, 5, stamp_ns());
     }
   }
   __syncthreads();
+  if (threadIdx.x == 0) FD_STAMP(g_split_stamps, 6, stamp_ns());
 }
 
 
@@ -1204,6 +1236,22 @@ cudaError_t launch_d(const Params& p, const Shape& sh, const Maps& m, cudaStream
 }
 
 }  // namespace
+
+#ifdef FD_STAMPS
+cudaError_t read_split_stamps(unsigned long long* host, int n) {
+  if (n > kStampCtas * kStampSlots) n = kStampCtas * kStampSlots;
+  return cudaMemcpyFromSymbol(host, g_split_stamps, sizeof(unsigned long long) * n);
+}
+
+__global__ void empty_kernel(int) {}
+
+// An empty kernel of the given launch shape (launch-cost floor).
+cudaError_t launch_empty(int grid, int threads, int smem, cudaStream_t st) {
+  cudaFuncSetAttribute(empty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+  empty_kernel<<<grid, threads, smem, st>>>(0);
+  return cudaGetLastError();
+}
+#endif
 
 bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv_dtype, int paged,
                   int page_size) {

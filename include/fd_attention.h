@@ -295,7 +295,10 @@ fd_status fd_decode_attention_append(const void *q, const void *k_new, const voi
  * reported; use fd_decode_attention when they must be.  All calls share the
  * one array: calls that can overlap on the GPU (different streams, or
  * different host threads) race on it and must be serialised by the caller.
- * Nothing is allocated or freed.
+ * Nothing is allocated or freed.  Invalid or unsupported arguments get the
+ * same status as from fd_decode_attention.  The array's address is kept for
+ * the life of the process: do not call this entry point after
+ * cudaDeviceReset.
  */
 fd_status fd_decode_attention_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                       const int32_t *kv_start_idx, const int32_t *block_table,
@@ -364,6 +367,47 @@ fd_status fd_debug_gather_kv(const void *cache, const int32_t *kv_start_idx,
                              const int32_t *seq_len, int64_t kv_rows, int batch,
                              int num_kv_heads, int head_dim, int page_size, fd_dtype kv_dtype,
                              void *dst, void *workspace, fd_stream_t stream);
+
+/*
+ * Test hook for the bounded waits of the tensor-core split kernel.  Every
+ * wait of that kernel on its copy pipeline gives up after `wait_ns`
+ * nanoseconds (0: the default of one second), records
+ * FD_ERR_DEVICE_TIMEOUT in the workspace's error word and ends the CTA's
+ * work; the asynchronous-error reporting this follows is the one of
+ * "SGLang Prefill optimisation: dissecting FlashAttention kernel bottlenecks
+ * with GPU Trace", section 4.2 (a device error is found by a later host
+ * check, not at the launch).  With `starve_first_stage` non-zero the
+ * producer of every CTA issues no copy, so the consumers' first wait runs out
+ * with nothing in flight: the call itself returns FD_OK, its outputs are
+ * undefined, and fd_check_device_error reports FD_ERR_DEVICE_TIMEOUT.  The
+ * wait that drains copies already issued before a CTA exits keeps its own
+ * one-second bound and reports FD_ERR_DEVICE_TIMEOUT too when it gives up.
+ * Process-wide, from the next call on; wait_ns outside [0, 1e10] is
+ * FD_ERR_INVALID_ARG.  The CUDA-core split kernel has no such waits.
+ */
+fd_status fd_debug_set_wait_limit(int64_t wait_ns, int starve_first_stage);
+
+/*
+ * Test hook: the segments of the split plan that each CTA of the split
+ * kernel takes for these sizes, computed on the device by the split kernels'
+ * own plan and segment walk (the plan of "Learn CUDA from scratch, chapter
+ * 15", section 15.13: ragged batches scan their real lengths).  Arguments as
+ * in fd_decode_attention_multi (paged: a block table is used, page_size its
+ * page size).  dst is a device int32 array of dst_len values, of which the
+ * first grid * (1 + 5 * capacity_per_cta) are written: row c holds the
+ * number of segments of CTA c, then (stream, t_begin, t_end, complete, slot)
+ * for each of its first capacity_per_cta segments.  *grid_out (host) always
+ * receives the grid; a dst_len too small for it returns FD_ERR_INVALID_ARG
+ * before any launch.  A workspace of fd_workspace_bytes for these sizes is
+ * needed (its plan words are written as by a decode call).  Asynchronous on
+ * `stream`.
+ */
+fd_status fd_debug_plan_segments(const int32_t *seq_len, int batch, int q_len, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int paged, int page_size,
+                                 fd_dtype q_dtype, fd_dtype kv_dtype, int32_t *dst,
+                                 int64_t dst_len, int capacity_per_cta, int *grid_out,
+                                 void *workspace,
+                                 size_t workspace_bytes, fd_stream_t stream);
 
 #ifdef __cplusplus
 }

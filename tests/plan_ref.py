@@ -77,3 +77,46 @@ def merge_slots(prefix, total, grid, s, seg_units: int = 0):
     if c0 == c1:
         return []
     return [2 * c0 + 1] + [2 * c for c in range(c0 + 1, c1 + 1)]
+
+
+def _next_pow2(x: int) -> int:
+    p = 1
+    while p < x:
+        p <<= 1
+    return p
+
+
+def host_shape(kernel: int, num_q_heads: int, num_kv_heads: int, head_dim: int, kv_elem: int,
+               sms: int, q_len: int = 1):
+    """The host's choice of plan shape for a call, restated: returns
+    (streams_per_sequence hg, tile tokens, grid, seg_units).
+
+    kernel 2 (tensor cores): a 16-row head tile holds 16 query heads of one
+    KV head; mt = next power of two of ceil(group / 16) tiles per KV head; a
+    stream carries hc = 8 / mt KV heads (halved until it divides the KV
+    heads), so that 8 consumer warps cover its mt * hc head tiles with
+    wph = 8 / (mt * hc) warps each; a warp takes r sub-tiles of SUB tokens
+    (32 for 8-bit caches, 16 for 16-bit ones) per stage, r = 65536 bytes of
+    K+V over one r-step's bytes, clamped to [1, 4] and halved while a box
+    would exceed 256 rows; tile = SUB * wph * r; a segment start costs
+    ceil(128 KiB / stage bytes) tiles; grid = one CTA per SM.
+    kernel 1 (CUDA cores): streams of min(group, 16) query heads of one KV
+    head, 32-token tiles, one CTA per SM, no start cost.
+    """
+    group = num_q_heads * q_len // num_kv_heads
+    if kernel == 1:
+        hq = min(group, 16)
+        return num_q_heads * q_len // hq, 32, sms, 0
+    mt = _next_pow2(-(-group // 16))
+    hc = 8 // mt
+    while hc > 1 and num_kv_heads % hc:
+        hc //= 2
+    wph = 8 // (mt * hc)
+    row = head_dim * kv_elem
+    sub = 32 if kv_elem == 1 else 16
+    r = max(1, min(4, 65536 // (sub * wph * hc * row * 2)))
+    while r > 1 and sub * wph * r > 256:
+        r //= 2
+    tile = sub * wph * r
+    stage = 2 * hc * tile * row
+    return num_kv_heads // hc, tile, sms, -(-131072 // stage)

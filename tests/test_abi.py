@@ -168,3 +168,36 @@ def test_header_enums_match_the_binding(fda):
                  "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
                  "FD_ERR_CUDA", "FD_ERR_DEVICE_BOUNDS", "FD_ERR_DEVICE_TIMEOUT"):
         assert enums[name] == getattr(fda, name), name
+
+
+def test_noalloc_classifies_bad_arguments_like_the_workspace_entry(fda):
+    """Both entry points give the same status to the same bad arguments
+    (checked on the host, before any device work)."""
+    lib = fda.load_library()
+    fake = 0x1000
+    for d, want in ((96, 2), (128, None)):
+        st_ws = _call(fda, d=d, qh=8, kvh=2, batch=4)
+        st_na = lib.fd_decode_attention_noalloc(fake, fake, fake, fake, None, 0, fake, 100, 4, 8,
+                                                2, d, 0, 0.1, 1.0, 1.0, 0, 0, fake, fake, None)
+        if want is not None:
+            assert st_ws == want and st_na == want, (d, st_ws, st_na)
+    for over in (dict(q=None), dict(batch=0), dict(qh=6, kvh=4), dict(kvdt=4)):
+        a = dict(q=fake, batch=4, qh=8, kvh=2, kvdt=0)
+        a.update(over)
+        st_ws = _call(fda, **over)
+        st_na = lib.fd_decode_attention_noalloc(a["q"], fake, fake, fake, None, 0, fake, 100,
+                                                a["batch"], a["qh"], a["kvh"], 128, 0, 0.1, 1.0,
+                                                1.0, 0, a["kvdt"], fake, fake, None)
+        assert st_na == st_ws, (over, st_ws, st_na)
+
+
+def test_debug_hook_arguments_are_checked_on_the_host(fda):
+    lib = fda.load_library()
+    assert lib.fd_debug_set_wait_limit(-5, 0) == 1
+    assert lib.fd_debug_set_wait_limit(0, 0) == 0
+    grid = ctypes.c_int(0)
+    # no dst, no workspace, bad q_len: refused before any device work
+    assert lib.fd_debug_plan_segments(0x1000, 2, 1, 8, 2, 128, 0, 0, 0, 0, None, 0, 4,
+                                      ctypes.byref(grid), 0x2000, 1 << 20, None) == 1
+    assert lib.fd_debug_plan_segments(0x1000, 2, 0, 8, 2, 128, 0, 0, 0, 0, 0x3000, 1 << 20, 4,
+                                      ctypes.byref(grid), 0x2000, 1 << 20, None) == 1

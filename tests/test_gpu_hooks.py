@@ -49,11 +49,47 @@ def test_device_plan_matches_restatement(kernel, case):
     assert hq % group == 0 or group % hq == 0      # a stream never splits a KV head's reads
     assert S == w.batch * hg
     assert seg_units >= 0 and (kernel == 2 or seg_units == 0)
+    # the host's choice of shape, restated
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    elem = 1 if w.kv_dtype in ("e4m3", "i8") else 2
+    assert (hg, tile, grid, seg_units) == plan_ref.host_shape(
+        kernel, w.num_q_heads, w.num_kv_heads, w.head_dim, elem, sms, w.q_len)
     p_prefix, p_total, p_per_cta, _ = plan_ref.plan(w.seq_len, hg, tile, grid, seg_units)
     assert prefix == p_prefix
     assert (total, per_cta) == (p_total, p_per_cta)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert grid % sms == 0
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("case", range(6))
+def test_device_segments_match_restatement(kernel, case):
+    """Every CTA's segments (stream, token range, complete, partial slot), as
+    the split kernels' own plan and segment walk produce them on the device,
+    equal the restatement's bit for bit."""
+    fda = lib()
+    w = _plan_cases()[case]
+    fda.fd_set_kernel(kernel)
+    try:
+        qd = 0 if w.q_dtype == "f16" else 1
+        kd = fda.DTYPE_CODES[w.kv_dtype]
+        if fda.fd_selected_kernel(w.num_q_heads, w.num_kv_heads, w.head_dim, qd, kd, w.paged,
+                                  1) != kernel:
+            pytest.skip("kernel does not support this shape")
+        ws = fda.alloc_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim)
+        seq = torch.from_numpy(w.seq_len).cuda()
+        got = fda.fd_debug_plan_segments(seq, w.q_len, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                         w.paged, max(w.page_size, 1), qd, kd, ws,
+                                         capacity_per_cta=1024)
+    finally:
+        fda.fd_set_kernel(0)
+    head, prefix = fda.fd_debug_read_plan(ws)
+    S, hg, tile, grid, total, per_cta, k, seg_units = head
+    assert k == kernel and len(got) == grid
+    p_prefix, _, _, segs = plan_ref.plan(w.seq_len, hg, tile, grid, seg_units)
+    assert prefix == p_prefix
+    want = [[] for _ in range(grid)]
+    for sg in segs:
+        want[sg.cta].append((sg.stream, sg.t_begin, sg.t_end, int(sg.complete), sg.slot))
+    assert got == want
 
 
 def _cpu_gather(w, which):

@@ -4,10 +4,12 @@ cannot reach, or code bound to a fixed memory budget).
 
 fd_decode_attention_noalloc takes its scratch memory from a fixed array inside
 the library instead of a caller workspace.  These checks call it through the C
-ABI twice in a row and compare each result with fd_decode_attention's on the
-same inputs, at the parity tolerances; they also check that sizes needing more
-scratch than the array holds are refused before any launch.  The file is named
-so that pytest collects it after every other test file.
+ABI twice in a row and compare each result with the CPU oracle at the parity
+bar, and with fd_decode_attention's on the same inputs bit for bit (the same
+kernels run the same plan, so leftover scratch from an earlier call must not
+change a single bit); they also check that sizes needing more scratch than the
+array holds are refused before any launch.  The file is named so that pytest
+collects it after every other test file.
 """
 import ctypes
 
@@ -16,7 +18,7 @@ import pytest
 import torch
 
 import fd_workloads as fw
-from gpu_util import TOL, LSE_REL, lib
+from gpu_util import lib, parity
 
 pytestmark = pytest.mark.gpu
 
@@ -56,21 +58,19 @@ def _noalloc(fda, w, t):
 
 
 @pytest.mark.parametrize("case", range(4))
-def test_noalloc_matches_workspace_entry_twice(case):
+def test_noalloc_matches_oracle_and_workspace_entry_twice(case, orc):
     fda = lib()
     w = _cases()[case]
     t = fw.to_torch(w, "cuda")
-    ref_out, ref_lse = _with_workspace(fda, w, t)
-    tol = TOL[w.q_dtype]
+    ws_out, ws_lse = _with_workspace(fda, w, t)
+    ref_out, ref_lse = orc.decode_attention(w)
     for call in range(2):
         out, lse = _noalloc(fda, w, t)
-        assert np.all(np.isfinite(out)), f"call {call}"
-        d = np.abs(out.astype(np.float64) - ref_out)
-        assert d.max() <= tol["max_abs"], f"call {call}: max_abs {d.max():.3e}"
-        fin = np.isfinite(ref_lse)
-        assert np.array_equal(fin, np.isfinite(lse))
-        rel = np.abs(lse[fin] - ref_lse[fin]) / np.maximum(np.abs(ref_lse[fin]), 1.0)
-        assert rel.max() <= LSE_REL, f"call {call}: lse {rel.max():.3e}"
+        parity(w, out.astype(np.float64), lse.astype(np.float64), ref_out, ref_lse,
+               label=f"{w.name} call {call}")
+        # same kernels, same plan: identical bits, NaN nowhere
+        assert np.array_equal(out, ws_out, equal_nan=False), f"call {call}: output bits differ"
+        assert np.array_equal(lse, ws_lse), f"call {call}: lse bits differ"
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
