@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--shared-prefix", type=int, default=0,
                     help="paged workloads: every sequence's first pages alias those of "
                          "sequence 0 up to this many tokens (prefix-cache hits)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config timings of the other workloads and variants")
     return ap.parse_args()
 
 
@@ -342,6 +344,139 @@ def recorded_traffic(kernel_name: str, config: int):
 SYNC_EVERY = 64   # timed steps between host waits (keeps the launch queue short)
 
 
+def timed_steps(step, flush, stream, K, split_events: bool = False):
+    """Times K steps, each after an L2 flush (outside the events), with CUDA
+    events on the launching stream: around the whole step, or (split_events)
+    around the split kernel's launch inside it.  The host waits for the GPU
+    every SYNC_EVERY steps, between two timed steps, so the launch queue
+    never fills (a host thread blocked on a full queue can wake up late and
+    leave the GPU idle inside a timed step).  Returns milliseconds per step."""
+    import torch
+    import flash_decoding_attention_gb300 as fda
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    if split_events:
+        for a, b in ev:           # torch creates the CUDA events on first record
+            a.record(stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush()
+        if split_events:
+            fda.fd_set_split_events(*ev[i])
+            step()
+            fda.fd_set_split_events(None, None)
+        else:
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        if (i + 1) % SYNC_EVERY == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def make_step(fda, w, t, out, lse, ws, stream, append: bool = False):
+    """One decode step of workload w through the C ABI (the entry point its
+    options call for)."""
+    QH, KVH, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+
+    def step():
+        if w.q_len > 1 and not append:
+            fda.fd_decode_attention_multi(
+                t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
+                w.kv_rows, QH, KVH, D, w.page_size, float(w.softmax_scale), float(w.k_scale),
+                float(w.v_scale), w.scale_kind, t["k_scales"], t["v_scales"], out, lse, ws, stream)
+            return
+        if append:
+            fda.fd_decode_attention_append(
+                t["q"], t["k_new"], t["v_new"], t["k"], t["v"], t["kv_start_idx"],
+                t["block_table"], t["positions"], t["seq_len"], w.kv_rows, QH, KVH, D,
+                w.page_size, float(w.softmax_scale), float(w.k_scale), float(w.v_scale),
+                w.scale_kind, t["k_scales"], t["v_scales"], out, lse, ws, stream)
+            return
+        if w.scale_kind:
+            fda.fd_decode_attention_scaled(
+                t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
+                w.kv_rows, QH, KVH, D, w.page_size, float(w.softmax_scale), float(w.k_scale),
+                float(w.v_scale), w.scale_kind, t["k_scales"], t["v_scales"], out, lse, ws, stream)
+            return
+        fda.fd_decode_attention(t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"],
+                                t["seq_len"], w.kv_rows, QH, KVH, D, w.page_size,
+                                float(w.softmax_scale), float(w.k_scale), float(w.v_scale), out,
+                                lse, ws, stream)
+    return step
+
+
+def pct(xs, q):
+    return round(float(np.percentile(xs, q)) * 1e3, 2)
+
+
+# Workloads timed next to the headline one (same protocol): the other
+# configurations, and the per-token-scale, INT8 and verify-step variants of
+# the headline workloads.  name -> (config, kv format, scale kind, q_len)
+PER_CONFIG = {
+    "config1": (1, "e4m3", "tensor", 1), "config2": (2, "e4m3", "tensor", 1),
+    "config3": (3, "e4m3", "tensor", 1), "config4": (4, "e4m3", "tensor", 1),
+    "config5": (5, "e4m3", "tensor", 1),
+    "config4_token_scales": (4, "e4m3", "token", 1), "config4_int8": (4, "i8", "tensor", 1),
+    "config5_q_len4": (5, "e4m3", "tensor", 4),
+}
+
+
+def per_config_timings(args, dev, stream, flush, peak, kernel_name):
+    """µs per step (mean, p10/p50/p90), effective GB/s and its fraction of the
+    peak, and the split kernel's own µs, for every PER_CONFIG entry except
+    the headline's own."""
+    import torch
+    import flash_decoding_attention_gb300 as fda
+    K = max(100, min(args.steps, 400))
+    res = {}
+    for name, (cfg, kv, scales, q_len) in PER_CONFIG.items():
+        if (cfg, kv, scales, q_len) == (args.config, args.kv, args.scales, args.q_len):
+            continue
+        a = argparse.Namespace(**vars(args))
+        a.config, a.kv, a.scales, a.q_len, a.shared_prefix = cfg, kv, scales, q_len, 0
+        w = make_workload(a)
+        t = fw.to_torch(w, dev)
+        out = torch.empty_like(t["q"])
+        lse = torch.empty(t["q"].shape[:-1], dtype=torch.float32, device=dev)
+        ws = fda.alloc_workspace(w.batch, w.num_q_heads * w.q_len, w.num_kv_heads, w.head_dim,
+                                 dev)
+        step = make_step(fda, w, t, out, lse, ws, stream)
+        for _ in range(5):
+            flush()
+            step()
+        torch.cuda.synchronize()
+        st, info = fda.fd_check_device_error(ws)
+        if st != 0:
+            raise RuntimeError(f"{name}: device error {fda.fd_status_string(st)} info={info}")
+        ms = timed_steps(step, flush, stream, K)
+        alg = w.algorithmic_bytes()
+        mean_ms = sum(ms) / K
+        e = {"workload": fw.WORKLOAD_NAMES[cfg], "steps": K, "us_per_step": round(mean_ms * 1e3, 2),
+             "us_per_step_p10_p50_p90": [pct(ms, 10), pct(ms, 50), pct(ms, 90)]}
+        if kv != "e4m3":
+            e["kv_dtype"] = kv
+        if scales != "tensor":
+            e["kv_scales"] = f"per {scales}"
+        if q_len > 1:
+            e["q_len"] = q_len
+        if cfg == 1:
+            e["note"] = "latency-bound (12 KB per step): time only"
+        else:
+            sms = timed_steps(step, flush, stream, K, split_events=True)
+            split_ms = sum(sms) / K
+            gbs = alg / (mean_ms * 1e-3) / 1e9
+            e.update({"algorithmic_bytes_per_step": alg, "gbs": round(gbs, 1),
+                      "frac": round(gbs / peak, 4), "split_us": round(split_ms * 1e3, 2),
+                      "split_frac": round(alg / (split_ms * 1e-3) / 1e9 / peak, 4)})
+        res[name] = e
+        del t, out, lse, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args):
     import torch
     import flash_decoding_attention_gb300 as fda
@@ -375,30 +510,7 @@ def run_gpu(args):
         t["v_new"] = torch.from_numpy(v_new.view(np.int16)).view(qd).to(dev)
         t["positions"] = torch.from_numpy(fw.last_positions(w, w.q_len)).to(dev)
 
-    def step():
-        if w.q_len > 1 and not args.append:
-            fda.fd_decode_attention_multi(
-                t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
-                w.kv_rows, QH, KVH, D, w.page_size, float(w.softmax_scale), float(w.k_scale),
-                float(w.v_scale), w.scale_kind, t["k_scales"], t["v_scales"], out, lse, ws, stream)
-            return
-        if args.append:
-            fda.fd_decode_attention_append(
-                t["q"], t["k_new"], t["v_new"], t["k"], t["v"], t["kv_start_idx"],
-                t["block_table"], t["positions"], t["seq_len"], w.kv_rows, QH, KVH, D,
-                w.page_size, float(w.softmax_scale), float(w.k_scale), float(w.v_scale),
-                w.scale_kind, t["k_scales"], t["v_scales"], out, lse, ws, stream)
-            return
-        if w.scale_kind:
-            fda.fd_decode_attention_scaled(
-                t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"], t["seq_len"],
-                w.kv_rows, QH, KVH, D, w.page_size, float(w.softmax_scale), float(w.k_scale),
-                float(w.v_scale), w.scale_kind, t["k_scales"], t["v_scales"], out, lse, ws, stream)
-            return
-        fda.fd_decode_attention(t["q"], t["k"], t["v"], t["kv_start_idx"], t["block_table"],
-                                t["seq_len"], w.kv_rows, QH, KVH, D, w.page_size,
-                                float(w.softmax_scale), float(w.k_scale), float(w.v_scale), out,
-                                lse, ws, stream)
+    step = make_step(fda, w, t, out, lse, ws, stream, append=args.append)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(2 * l2 // 4, dtype=torch.int32, device=dev)
@@ -417,39 +529,17 @@ def run_gpu(args):
         raise RuntimeError(f"device error {fda.fd_status_string(st)} info={info}")
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
-    for a, b in sev:           # torch creates the CUDA events on first record
-        a.record(stream)
-        b.record(stream)
     clocks = ClockSampler(local, not args.no_clocks)
     time.sleep(0.3)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    # headline: whole decode steps (split + combine, launched back to back).
-    # The host waits for the GPU every SYNC_EVERY steps, between two timed
-    # steps, so the launch queue never fills: a host thread blocked on a full
-    # queue can wake up late and leave the GPU idle inside a timed step.
-    for i in range(K):
-        flush()
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-        if (i + 1) % SYNC_EVERY == 0:
-            torch.cuda.synchronize()
+    # headline: whole decode steps, L2 flushed before each
+    step_ms = timed_steps(step, flush, stream, K)
     # roofline: the same steps again with events around the split kernel alone
-    # (an event between the two launches stops the combine from overlapping
-    # the split kernel's tail, so these steps are not used for the headline)
-    for i in range(K):
-        flush()
-        fda.fd_set_split_events(*sev[i])
-        step()
-        fda.fd_set_split_events(None, None)
-        if (i + 1) % SYNC_EVERY == 0:
-            torch.cuda.synchronize()
+    # (an event between two launches of a step stops them from overlapping,
+    # so these steps are not used for the headline)
+    split_ms = timed_steps(step, flush, stream, K, split_events=True)
     # diagnostic only: back-to-back steps without the L2 flush (inputs partly
     # L2-resident from the previous step), events around the whole run
     n_hot = min(K, 200)
@@ -464,8 +554,6 @@ def run_gpu(args):
     if pg:
         pg.barrier()
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    split_ms = [a.elapsed_time(b) for a, b in sev]
     total_ms = sum(step_ms)
     if pg:
         total_ms = max_over_ranks(total_ms, dev)
@@ -530,36 +618,49 @@ def run_gpu(args):
     split_avg = sum(split_ms) / K
     achieved = alg / (split_avg * 1e-3) / 1e9
     peak, peak_src = measured_peak()
+    fused = kname == "mma"   # the tensor-core kernel merges split streams itself
+    per_config = None
+    if not args.no_per_config and world == 1:
+        clocks2 = ClockSampler(local, not args.no_clocks)
+        per_config = per_config_timings(args, dev, stream, flush, peak, kname)
+        clk2 = clocks2.stop()
+        if clk2:
+            per_config["clocks"] = clk2
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "us_per_step": round(ms_per_step * 1e3, 2),
-        "us_per_step_p10_p50_p90": [round(float(np.percentile(step_ms, q)) * 1e3, 2)
-                                    for q in (10, 50, 90)],
+        "us_per_step_p10_p50_p90": [pct(step_ms, q) for q in (10, 50, 90)],
         "us_per_step_max": round(max(step_ms) * 1e3, 2),
         "slow_steps": int(sum(1 for x in step_ms if x > 1.5 * float(np.median(step_ms)))),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": (f"{w.kv_dtype}->{w.q_dtype} mma, f32 acc" if w.kv_dtype in ("e4m3", "i8")
-                  else f"{w.kv_dtype} mma, f32 acc"),
+        "dtype": (f"{w.kv_dtype}->{w.q_dtype} {'mma' if kname == 'mma' else 'fma'}, f32 acc"
+                  if w.kv_dtype in ("e4m3", "i8")
+                  else f"{w.kv_dtype} {'mma' if kname == 'mma' else 'fma'}, f32 acc"),
         "data": "synthetic",
         "config": {**workload_config(args), "kernel": kname,
                    "algorithmic_bytes_per_step": alg, "sum_seq_len": int(w.seq_len.sum()),
                    "l2": "flushed between steps (write then read of 2x L2 buffers, outside the "
                          "timed events)",
                    "parallelism": f"replicas x{world}"},
-        # split + combine (+ append) per step: the headline loop, the
-        # roofline loop and the unflushed diagnostic
-        "gpu_launches": (3 if args.append else 2) * (2 * K + n_hot),
+        # per step: the split kernel (which also merges split streams on the
+        # tensor-core path; else a combine kernel follows) and the append;
+        # the headline loop, the roofline loop and the unflushed diagnostic
+        "gpu_launches": ((1 if fused else 2) + (1 if args.append else 0)) * (2 * K + n_hot),
         "diagnostic_unflushed_us_per_step": round(hot_us, 2),
         "env": device_env(dev),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if (args.shared_prefix or args.scales != "tensor")
                      else recorded_traffic(kname, args.config),
-                     "kernel": f"split ({kname})", "split_us": round(split_avg * 1e3, 2)},
+                     "kernel": (f"split ({kname}), merging split streams in the same launch"
+                                if fused else f"split ({kname})"),
+                     "split_us": round(split_avg * 1e3, 2)},
         "e2e": e2e,
         "clocks": clk,
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     if not args.no_cpu_baseline and args.gpus == 1:
         gbs, threads, desc, _ = oracle_sample(w, budget_s=15.0)
         gbs1, _, desc1, _ = oracle_sample(w, budget_s=3.0, nthreads=1)

@@ -122,7 +122,7 @@ def load_library(path: Optional[str] = None):
         lib.fd_debug_set_wait_limit.restype = i32
         lib.fd_debug_set_wait_limit.argtypes = [i64, i32]
         lib.fd_debug_plan_segments.restype = i32
-        lib.fd_debug_plan_segments.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+        lib.fd_debug_plan_segments.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                                vp, i64, i32, ctypes.POINTER(ctypes.c_int), vp, sz,
                                                vp]
         if path is None:
@@ -389,7 +389,8 @@ def fd_debug_set_wait_limit(wait_ns: int, starve_first_stage: bool = False) -> N
 
 def fd_debug_plan_segments(seq_len, q_len: int, num_q_heads: int, num_kv_heads: int,
                            head_dim: int, paged: bool, page_size: int, q_dtype: int,
-                           kv_dtype: int, workspace, capacity_per_cta: int = 64, stream=None):
+                           kv_dtype: int, workspace, capacity_per_cta: int = 64, stream=None,
+                           kv_start_idx=None):
     """Segments (stream, t_begin, t_end, complete, slot) of every CTA of the
     split kernel for these sizes, as the device plans them: a list with one
     list of tuples per CTA."""
@@ -398,7 +399,7 @@ def fd_debug_plan_segments(seq_len, q_len: int, num_q_heads: int, num_kv_heads: 
     dst = torch.full((4 * sms * rows,), -1, dtype=torch.int32, device=seq_len.device)
     grid = ctypes.c_int(0)
     st = load_library().fd_debug_plan_segments(
-        _ptr(seq_len), int(seq_len.shape[0]), int(q_len), int(num_q_heads), int(num_kv_heads),
+        _ptr(seq_len), _ptr(kv_start_idx), int(seq_len.shape[0]), int(q_len), int(num_q_heads), int(num_kv_heads),
         int(head_dim), int(bool(paged)), int(page_size), int(q_dtype), int(kv_dtype), _ptr(dst),
         dst.numel(), int(capacity_per_cta), ctypes.byref(grid), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream_handle(stream))

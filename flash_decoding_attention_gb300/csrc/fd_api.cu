@@ -167,8 +167,8 @@ __global__ void gather_kernel(const Params p, uint8_t* dst, int row_bytes) {
 // Row c of dst: the number of segments, then per segment (stream, t_begin,
 // t_end, complete, slot), at most `cap` of them.
 __global__ void plan_segments_kernel(const Params p, int32_t* dst, int cap) {
-  __shared__ long long red[34];
-  const PlanResult plan = compute_plan(p, red);
+  __shared__ long long red[35];
+  const PlanResult plan = compute_plan(p, red, blockDim.x, 0);
   if (threadIdx.x != 0) return;
   SegmentIter it;
   it.init(p, plan);
@@ -575,7 +575,8 @@ fd_status fd_debug_set_wait_limit(int64_t wait_ns, int starve_first_stage) {
   return FD_OK;
 }
 
-fd_status fd_debug_plan_segments(const int32_t* seq_len, int batch, int q_len, int num_q_heads,
+fd_status fd_debug_plan_segments(const int32_t* seq_len, const int32_t* kv_start_idx, int batch,
+                                 int q_len, int num_q_heads,
                                  int num_kv_heads, int head_dim, int paged, int page_size,
                                  fd_dtype q_dtype, fd_dtype kv_dtype, int32_t* dst,
                                  int64_t dst_len, int capacity_per_cta, int* grid_out,
@@ -602,6 +603,7 @@ fd_status fd_debug_plan_segments(const int32_t* seq_len, int batch, int q_len, i
   p.ws = reinterpret_cast<WsHeader*>(ws);
   p.prefix = reinterpret_cast<int32_t*>(ws + L.prefix_off);
   p.seq_len = seq_len;
+  p.kv_start = kv_start_idx;
   p.batch = batch;
   p.hg = c.hg;
   p.hq = c.hq;

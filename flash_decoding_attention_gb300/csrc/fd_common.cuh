@@ -123,7 +123,7 @@ struct Params {
 // slot i of CTA c in a kernel's stamp array holds %globaltimer (ns) when the
 // CTA passed phase i; fd_debug_read_stamps copies them out.
 #ifdef FD_STAMPS
-constexpr int kStampCtas = 4096, kStampSlots = 16;
+constexpr int kStampCtas = 4096, kStampSlots = 24;
 #define FD_STAMP_ARRAY(name) __device__ unsigned long long name[kStampCtas * kStampSlots]
 #define FD_STAMP(arr, i, v)                                                        \
   do {                                                                             \
@@ -172,25 +172,93 @@ struct PlanResult {
   long long per_cta;    // L
   int s_first;          // stream holding this CTA's first unit (or num_streams)
   long long p_first;    // prefix (in units) of s_first
+  long long first_start;   // kv_start of s_first's sequence (contiguous caches), or -1
 };
 
-// Block-wide; every thread gets the same result.  CTA 0 also writes the
-// prefix array and the plan words of the header.  `red` is >= 34 long longs
-// of shared memory.
-__device__ inline PlanResult compute_plan(const Params& p, long long* red,
+__device__ inline void write_plan_words(const Params& p, long long total, long long per_cta) {
+  p.ws->plan[0] = p.batch * p.hg;
+  p.ws->plan[1] = p.hg;
+  p.ws->plan[2] = p.tile;
+  p.ws->plan[3] = p.grid;
+  p.ws->plan[4] = (int32_t)total;
+  p.ws->plan[5] = (int32_t)per_cta;
+  p.ws->plan[6] = p.kernel;
+  p.ws->plan[7] = p.seg_units;
+  if (total > 0x7fffffffLL) raise_error(p.ws, kErrPlan, total);
+}
+
+// Barrier `id` over the first `nthreads` threads of the CTA (id 0 with
+// every thread is __syncthreads).
+__device__ __forceinline__ void plan_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// The plan over threads [0, nthreads) of the CTA (barrier `bar`); every one
+// of them gets the same result.  CTA 0 also writes the prefix array and the
+// plan words of the header.  `red` is >= 35 long longs of shared memory.
+// With at most one stream per thread it is one pass (one read of seq_len,
+// and of kv_start alongside it); else two.
+__device__ inline PlanResult compute_plan(const Params& p, long long* red, int nthreads, int bar,
                                           unsigned long long* stamp = nullptr) {
   const int S = p.batch * p.hg;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
+  const int nwarps = nthreads >> 5;
+  if (S <= nthreads) {
+    const long long v = tid < S ? stream_units(p, tid) : 0;
+    const long long kvs = tid < S && p.kv_start ? (long long)__ldg(p.kv_start + tid / p.hg) : -1;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) red[warp] = x;
+    if (tid == 0) red[32] = S;
+    plan_sync(bar, nthreads);
+    long long woff = 0, total = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      if (w < warp) woff += red[w];
+      total += red[w];
+    }
+#ifdef FD_STAMPS
+    if (stamp && tid == 0) *stamp = stamp_ns();
+#else
+    (void)stamp;
+#endif
+    PlanResult r;
+    r.total = total;
+    r.per_cta = total > 0 ? (total + p.grid - 1) / p.grid : 0;
+    const long long target = (long long)blockIdx.x * r.per_cta;
+    const bool has_work = target < total;
+    const long long excl = woff + x - v;
+    if (tid < S) {
+      if (blockIdx.x == 0) p.prefix[tid] = (int32_t)excl;
+      if (has_work && v > 0 && excl <= target && target < excl + v) {
+        red[32] = tid;
+        red[33] = excl;
+        red[34] = kvs;
+      }
+    }
+    if (blockIdx.x == 0 && tid == 0) {
+      p.prefix[S] = (int32_t)total;
+      write_plan_words(p, total, r.per_cta);
+    }
+    plan_sync(bar, nthreads);
+    r.s_first = has_work ? (int)red[32] : S;
+    r.p_first = has_work ? red[33] : total;
+    r.first_start = has_work ? red[34] : -1;
+    plan_sync(bar, nthreads);
+    return r;
+  }
   // pass 1: total units
   long long acc = 0;
-  for (int s = tid; s < S; s += blockDim.x) acc += stream_units(p, s);
+  for (int s = tid; s < S; s += nthreads) acc += stream_units(p, s);
   for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) red[warp] = acc;
-  __syncthreads();
+  plan_sync(bar, nthreads);
   long long total = 0;
   for (int w = 0; w < nwarps; ++w) total += red[w];
-  __syncthreads();
+  plan_sync(bar, nthreads);
 #ifdef FD_STAMPS
   if (stamp && tid == 0) *stamp = stamp_ns();
 #else
@@ -204,7 +272,7 @@ __device__ inline PlanResult compute_plan(const Params& p, long long* red,
   // pass 2: exclusive prefix, position of this CTA's first tile
   if (tid == 0) { red[32] = S; }
   long long carry = 0;
-  for (int base = 0; base < S; base += blockDim.x) {
+  for (int base = 0; base < S; base += nthreads) {
     int s = base + tid;
     long long v = s < S ? stream_units(p, s) : 0;
     long long x = v;
@@ -213,7 +281,7 @@ __device__ inline PlanResult compute_plan(const Params& p, long long* red,
       if (lane >= o) x += y;
     }
     if (lane == 31) red[warp] = x;
-    __syncthreads();
+    plan_sync(bar, nthreads);
     long long woff = 0, ctot = 0;
     for (int w = 0; w < nwarps; ++w) {
       if (w < warp) woff += red[w];
@@ -228,23 +296,16 @@ __device__ inline PlanResult compute_plan(const Params& p, long long* red,
       }
     }
     carry += ctot;
-    __syncthreads();
+    plan_sync(bar, nthreads);
   }
   if (blockIdx.x == 0 && tid == 0) {
     p.prefix[S] = (int32_t)total;
-    p.ws->plan[0] = S;
-    p.ws->plan[1] = p.hg;
-    p.ws->plan[2] = p.tile;
-    p.ws->plan[3] = p.grid;
-    p.ws->plan[4] = (int32_t)total;
-    p.ws->plan[5] = (int32_t)r.per_cta;
-    p.ws->plan[6] = p.kernel;
-    p.ws->plan[7] = p.seg_units;
-    if (total > 0x7fffffffLL) raise_error(p.ws, kErrPlan, total);
+    write_plan_words(p, total, r.per_cta);
   }
   r.s_first = has_work ? (int)red[32] : S;
   r.p_first = has_work ? red[33] : total;
-  __syncthreads();
+  r.first_start = -1;
+  plan_sync(bar, nthreads);
   return r;
 }
 

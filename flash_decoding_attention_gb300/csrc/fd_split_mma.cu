@@ -73,7 +73,8 @@ struct Shape {
   int heads_box;     // 1: one TMA box covers all hc heads of a tile
   int scale_tma;     // 1: per-token scales come by TMA (else by 4-byte cp.async)
   int stages;
-  int merge_bytes;
+  int merge_in_stage;   // 1: the warps of a head tile merge in the stage of the segment's last tile
+  int merge_bytes;      // a dedicated merge area (wph > 1 and no stage is large enough)
   int qfrag_bytes;
   int qrows;         // Q rows kept per head tile: 16, or 8 when no tile has more (see make_shape)
   int scale_bytes;   // per stage with per-token scales: K then V scales, each [tile][hc] fp32
@@ -110,7 +111,13 @@ Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype, int pa
   s.heads_box = 0;   // decided at launch (needs a tensor map over {dims, rows, heads})
   s.scale_tma = 0;   // decided at launch (needs a tensor map over the scale arrays)
   s.kv_bytes = s.hc * s.nx * s.region_bytes;
-  s.merge_bytes = s.wph > 1 ? kConsumerWarps * (16 * (head_dim + head_dim / 8) + 32) * 4 : 0;
+  // the segment-end merge of a head tile's warps stages 16 rows of every
+  // consumer warp's output state: in the stage holding the segment's last
+  // tile when it is large enough (its release is held until the merge is
+  // done), else in an area of its own
+  const int merge_need = kConsumerWarps * 16 * head_dim * 4;
+  s.merge_in_stage = s.wph > 1 && 2 * s.kv_bytes >= merge_need ? 1 : 0;
+  s.merge_bytes = s.wph > 1 && !s.merge_in_stage ? merge_need : 0;
   // One Q fragment set per head tile.  With per-token scales and at most 8
   // query heads per KV head, rows 8..15 of every tile are zero: only rows
   // 0..7 are kept, which leaves room for a third stage on those shapes.
@@ -380,23 +387,34 @@ __device__ __forceinline__ void zero_rows_past_end(W& w0, W& w1, W& w2, W& w3, i
   if (tk + 9 >= left) w3 = W{};
 }
 
-// ---------------------------------------------------------------------------
-// The kernel
-// ---------------------------------------------------------------------------
 #ifdef FD_STAMPS
 // 0 entry, 1 plan done, 2 first copy issued, 3 first stage landed (warp 0),
 // 4 last stage released (warp 0), 5 last segment stored (warp 0), 6 exit,
 // 7 stages consumed by warp 0, 8 plan total known, 9 producer has its first
-// segment, 10 producer has the segment's row data, 11 before the plan
+// segment, 10 producer has the segment's row data, 11 before the plan,
+// 13-15 segment-end merge of a head tile's warps (stage read, states
+// staged, merged), 20 the SM's id
 FD_STAMP_ARRAY(g_split_stamps);
 #endif
+
+// Float4 chunk c of row x of a warp's area in the segment-end merge: an XOR
+// swizzle within each group of 8 chunks, so that the 8 lanes of a quarter
+// warp storing their fragments (rows r, r + 1; chunks 8q + const) and a warp
+// reading one row both hit 8 different 16-byte bank groups.
+__device__ __forceinline__ uint32_t merge_chunk(int x, int c) {
+  return (uint32_t)(c ^ (((x & 1) << 2) | ((c >> 3) & 3)));
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
 
 struct Shared {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   int bad[kMaxStages];
   int abort_flag;
-  long long red[34];
+  long long red[35];
   int pages[kPageWindow];   // producer's window of the current sequence's block table
 };
 
@@ -426,13 +444,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const uint32_t stage0 = smem_u32(base);
-  float* merge = reinterpret_cast<float*>(base + sh.stages * 2 * sh.kv_bytes);
   const uint32_t qfrag0 = stage0 + sh.stages * 2 * sh.kv_bytes + sh.merge_bytes;
   float* scl = reinterpret_cast<float*>(base + sh.stages * 2 * sh.kv_bytes + sh.merge_bytes +
                                         sh.qfrag_bytes);   // per-token scales (TOK)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) FD_STAMP(g_split_stamps, 0, stamp_ns());
+#ifdef FD_STAMPS
+  if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    FD_STAMP(g_split_stamps, 20, (unsigned long long)smid);
+  }
+#endif
   if (threadIdx.x == 0) {
     for (int i = 0; i < sh.stages; ++i) {
       mbar_init(&sm.full[i], TOK && !sh.scale_tma ? 1 + 32 : 1);
@@ -450,9 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   prefetch_index_arrays(p);
   if (threadIdx.x == 0) FD_STAMP(g_split_stamps, 11, stamp_ns());
 #ifdef FD_STAMPS
-  const PlanResult plan = compute_plan(p, sm.red, blockIdx.x < kStampCtas ? &g_split_stamps[blockIdx.x * kStampSlots + 8] : nullptr);
+  const PlanResult plan = compute_plan(
+      p, sm.red, kThreads, 0,
+      blockIdx.x < kStampCtas ? &g_split_stamps[blockIdx.x * kStampSlots + 8] : nullptr);
 #else
-  const PlanResult plan = compute_plan(p, sm.red);   // contains __syncthreads
+  const PlanResult plan = compute_plan(p, sm.red, kThreads, 0);
 #endif
   if (threadIdx.x == 0) FD_STAMP(g_split_stamps, 1, stamp_ns());
   allow_dependent_launch();
@@ -471,13 +497,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     SegmentIter it;
     it.init(p, plan);
     Segment seg;
-    long long n = 0;
+    int n = 0;
     bool stop = p.starve != 0;   // test switch: issue nothing, the consumers' waits run out
+    long long next_start = -1;   // kv_start of the next segment's sequence, read ahead
     while (!stop && it.next(p, seg)) {
       if (n == 0 && lane == 0) FD_STAMP(g_split_stamps, 9, stamp_ns());
       const int b = seg.s / p.hg;
       const int kvh0 = (seg.s - b * p.hg) * sh.hc;
-      const long long start = p.block_table ? 0 : (long long)__ldg(p.kv_start + b);
+      // the plan already read the first segment's kv_start, and each
+      // segment reads the next one's once its own copies fill the pipeline
+      const long long start = p.block_table ? 0
+                              : n == 0 && seg.s == plan.s_first && plan.first_start >= 0
+                                  ? plan.first_start
+                              : next_start >= 0 ? next_start
+                                                : (long long)__ldg(p.kv_start + b);
+      next_start = -1;
+      const int n_seg0 = n;
 #ifdef FD_STAMPS
       if (n == 0 && lane == 0 && start >= 0) FD_STAMP(g_split_stamps, 10, stamp_ns());
 #endif
@@ -578,6 +613,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         stop = __shfl_sync(0xffffffffu, stop, 0);
         if (stop) break;
+        if (n == n_seg0 + S - 1) {   // the next copy waits for a released stage anyway
+          // the next segment's row data ahead: its kv_start into a register,
+          // or its first window of block-table entries into L2
+          SegmentIter ahead = it;
+          Segment sn;
+          if (ahead.next(p, sn)) {
+            const int bn = sn.s / p.hg;
+            if (!p.block_table) {
+              next_start = __ldg(p.kv_start + bn);
+            } else {
+              const int pg0 = sn.t_begin >> p.page_shift, pg1 = (sn.t_end - 1) >> p.page_shift;
+              if (lane < kPageWindow / 32 && pg0 + 32 * lane <= pg1)
+                prefetch_l2(p.block_table + (long long)bn * p.bt_stride + pg0 + 32 * lane);
+            }
+          }
+        }
         if (TOK && !sh.scale_tma) {
           // the tile's per-token scales of its hc heads, element by element
           // (rows past the end, or outside the cache, read as zero)
@@ -609,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && stop) {
       // drain: copies of the last S issued tiles must land before the CTA
       // exits; a drain that gives up is recorded on its own
-      for (long long i = n - S < 0 ? 0 : n - S; i < n; ++i)
+      for (int i = n - S < 0 ? 0 : n - S; i < n; ++i)
         if (!mbar_wait(&sm.full[i % S], (uint32_t)((i / S) & 1), kDrainNs))
           raise_error(p.ws, kErrDrain, 3);
     }
@@ -651,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     Segment seg;
-    long long n = 0;
+    int n = 0;
     while (it.next(p, seg)) {
       const int b = seg.s / p.hg;
       const int j = seg.s - b * p.hg;
@@ -684,6 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
       float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      int last_stg = 0;
 
       for (int t0 = seg.t_begin; t0 < seg.t_end; t0 += sh.tile, ++n) {
         const int stg = (int)(n % S);
@@ -945,7 +997,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[stg]);
+        // the segment's last stage stays held when the head tile's warps
+        // merge in it (released after the merge)
+        last_stg = stg;
+        if (lane == 0 && !(sh.merge_in_stage && t0 + sh.tile >= seg.t_end))
+          mbar_arrive(&sm.empty[stg]);
         if (warp == 0 && lane == 0) {
           FD_STAMP(g_split_stamps, 4, stamp_ns());
           FD_STAMP(g_split_stamps, 7, (unsigned long long)(n + 1));
@@ -1001,12 +1057,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // Stage every warp's state in shared memory, then the wph warps of a
-        // head tile merge its 16 x D outputs together.  A staged row has 4
-        // floats of padding after every 32 dims, which spreads the float4
-        // stores of the 4 lanes of a row over different banks.
-        constexpr int RS = D + D / 8;                 // padded row stride (floats)
-        constexpr int WS = 16 * RS + 32;              // one warp's area (+ m, l)
-        float* mine = merge + warp * WS;
+        // head tile merge its 16 x D outputs together.  The area is the
+        // stage of the segment's last tile (held back from the producer) or
+        // a dedicated one: warp w's 16 rows of D floats at w * 16 * D,
+        // float4 chunk c of row x at chunk swz(x, c) (see merge_chunk), its
+        // row maxima and sums in the Q-fragment area (free at a segment end).
+        const uint32_t marea =
+            sh.merge_in_stage ? stage0 + (uint32_t)last_stg * 2u * sh.kv_bytes
+                              : stage0 + (uint32_t)(sh.stages * 2 * sh.kv_bytes);
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");   // stage read
+        if (warp == 0 && lane == 0) FD_STAMP(g_split_stamps, 13, stamp_ns());
+        const uint32_t mine = marea + (uint32_t)warp * (16u * D * 4u);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -1014,40 +1075,62 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t4 = 0; t4 < NT / 4; ++t4) {
               const int d = vdim<D, ELEM>(4 * t4, 2 * q + e);
-              *reinterpret_cast<float4*>(mine + (r + 8 * hh) * RS + d + 4 * (d >> 5)) =
-                  make_float4(o[4 * t4][2 * hh + e], o[4 * t4 + 1][2 * hh + e],
-                              o[4 * t4 + 2][2 * hh + e], o[4 * t4 + 3][2 * hh + e]);
+              const int row = r + 8 * hh;
+              asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(
+                               mine + (uint32_t)row * (D * 4) + merge_chunk(row, d >> 2) * 16u),
+                           "f"(o[4 * t4][2 * hh + e]), "f"(o[4 * t4 + 1][2 * hh + e]),
+                           "f"(o[4 * t4 + 2][2 * hh + e]), "f"(o[4 * t4 + 3][2 * hh + e])
+                           : "memory");
             }
           }
         }
+        float* mstat = reinterpret_cast<float*>(base + (size_t)(qfrag0 - stage0));   // [warp][m 16 | l 16]
         if (q == 0) {
-          mine[16 * RS + r] = m0;
-          mine[16 * RS + r + 8] = m1;
-          mine[16 * RS + 16 + r] = l0;
-          mine[16 * RS + 16 + r + 8] = l1;
+          mstat[warp * 32 + r] = m0;
+          mstat[warp * 32 + r + 8] = m1;
+          mstat[warp * 32 + 16 + r] = l0;
+          mstat[warp * 32 + 16 + r + 8] = l1;
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        if (warp == 0 && lane == 0) FD_STAMP(g_split_stamps, 14, stamp_ns());
         // each warp of the head tile merges whole rows, a lane 4 dims of one
         // row; the row's weights come from broadcast reads of m and l
-        const float* grp = merge + (ht * sh.wph) * WS;
+        const uint32_t grp = marea + (uint32_t)(ht * sh.wph) * (16u * D * 4u);
+        const float* gstat = mstat + ht * sh.wph * 32;
         for (int idx = ts * 32 + lane; idx < 16 * (D / 4); idx += sh.wph * 32) {
-          const int row = idx / (D / 4), d = 4 * (idx - row * (D / 4));
+          const int row = idx / (D / 4), c = idx - row * (D / 4), d = 4 * c;
           const int lh = mtile * 16 + row;
           if (lh >= G) continue;
+          // (at most 8 warps per head tile: a fixed bound, predicated, so
+          // that all loads issue before the first use)
+          float mw[kConsumerWarps], lw[kConsumerWarps];
+          uint4 vb[kConsumerWarps];
+          const uint32_t cofs = (uint32_t)row * (D * 4) + merge_chunk(row, c) * 16u;
+#pragma unroll
+          for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+            if (w2 < sh.wph) {
+              mw[w2] = gstat[w2 * 32 + row];
+              lw[w2] = gstat[w2 * 32 + 16 + row];
+              vb[w2] = lds128(grp + (uint32_t)w2 * (16u * D * 4u) + cofs);
+            } else {
+              mw[w2] = -INFINITY;
+              lw[w2] = 0.f;
+              vb[w2] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
           float M = -INFINITY;
-          for (int w2 = 0; w2 < sh.wph; ++w2) M = fmaxf(M, grp[w2 * WS + 16 * RS + row]);
+#pragma unroll
+          for (int w2 = 0; w2 < kConsumerWarps; ++w2) M = fmaxf(M, mw[w2]);
           float L = 0.f;
           float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int w2 = 0; w2 < sh.wph; ++w2) {
-            const float* g2 = grp + w2 * WS;
-            const float mw = g2[16 * RS + row];
-            const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-            L = fmaf(g2[16 * RS + 16 + row], f, L);
-            const float4 v = *reinterpret_cast<const float4*>(g2 + row * RS + d + 4 * (d >> 5));
-            A.x = fmaf(v.x, f, A.x);
-            A.y = fmaf(v.y, f, A.y);
-            A.z = fmaf(v.z, f, A.z);
-            A.w = fmaf(v.w, f, A.w);
+#pragma unroll
+          for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+            const float f = mw[w2] == -INFINITY ? 0.f : fast_exp2(mw[w2] - M);
+            L = fmaf(lw[w2], f, L);
+            A.x = fmaf(__uint_as_float(vb[w2].x), f, A.x);
+            A.y = fmaf(__uint_as_float(vb[w2].y), f, A.y);
+            A.z = fmaf(__uint_as_float(vb[w2].z), f, A.z);
+            A.w = fmaf(__uint_as_float(vb[w2].w), f, A.w);
           }
           const int li = kvl * G + lh;
           if (seg.complete) {
@@ -1063,6 +1146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        if (warp == 0 && lane == 0) FD_STAMP(g_split_stamps, 15, stamp_ns());
+        if (sh.merge_in_stage && lane == 0) mbar_arrive(&sm.empty[last_stg]);
       }
       if (warp == 0 && lane == 0) FD_STAMP(g_split_stamps, 5, stamp_ns());
     }
@@ -1244,10 +1329,32 @@ cudaError_t read_split_stamps(unsigned long long* host, int n) {
 }
 
 __global__ void empty_kernel(int) {}
+struct BigParams { unsigned char b[1024]; };
+__global__ void empty_kernel_big(const __grid_constant__ BigParams) {}
 
-// An empty kernel of the given launch shape (launch-cost floor).
+// An empty kernel of the given launch shape (launch-cost floor); smem < 0:
+// 1 KB of parameters; threads < 0: cooperative launch.
 cudaError_t launch_empty(int grid, int threads, int smem, cudaStream_t st) {
   cudaFuncSetAttribute(empty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+  if (smem < 0) {
+    BigParams bp;
+    memset(&bp, 0, sizeof(bp));
+    empty_kernel_big<<<grid, threads, 0, st>>>(bp);
+    return cudaGetLastError();
+  }
+  if (threads < 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(-threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, empty_kernel, 0);
+  }
   empty_kernel<<<grid, threads, smem, st>>>(0);
   return cudaGetLastError();
 }
@@ -1279,7 +1386,10 @@ void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms
   *tile = s.tile;
   *grid = sms;
   const int stage = 2 * s.kv_bytes;
-  *seg_units = (131072 + stage - 1) / stage;
+  // when the warps of a head tile merge at every segment end (wph > 1), a
+  // segment start also waits for that merge and for a refill of the
+  // pipeline behind it: twice the cost
+  *seg_units = (s.wph > 1 ? 2 : 1) * ((131072 + stage - 1) / stage);
 }
 
 cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {

@@ -98,9 +98,9 @@ template <int KVT, typename QT, int D>
 __global__ void __launch_bounds__(kSimtThreads) simt_split_kernel(const Params p) {
   constexpr int DPL = D / 32;
   extern __shared__ float sm[];
-  __shared__ long long red[34];
+  __shared__ long long red[35];
 
-  const PlanResult plan = compute_plan(p, red);
+  const PlanResult plan = compute_plan(p, red, blockDim.x, 0);
   allow_dependent_launch();
   wait_prior_grid();   // a KV append launched just before may still be writing rows
   SegmentIter it;

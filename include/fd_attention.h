@@ -393,7 +393,8 @@ fd_status fd_debug_set_wait_limit(int64_t wait_ns, int starve_first_stage);
  * own plan and segment walk (the plan of "Learn CUDA from scratch, chapter
  * 15", section 15.13: ragged batches scan their real lengths).  Arguments as
  * in fd_decode_attention_multi (paged: a block table is used, page_size its
- * page size).  dst is a device int32 array of dst_len values, of which the
+ * page size; kv_start_idx, which the plan reads ahead for the first
+ * segment of every CTA, may be NULL).  dst is a device int32 array of dst_len values, of which the
  * first grid * (1 + 5 * capacity_per_cta) are written: row c holds the
  * number of segments of CTA c, then (stream, t_begin, t_end, complete, slot)
  * for each of its first capacity_per_cta segments.  *grid_out (host) always
@@ -402,7 +403,8 @@ fd_status fd_debug_set_wait_limit(int64_t wait_ns, int starve_first_stage);
  * needed (its plan words are written as by a decode call).  Asynchronous on
  * `stream`.
  */
-fd_status fd_debug_plan_segments(const int32_t *seq_len, int batch, int q_len, int num_q_heads,
+fd_status fd_debug_plan_segments(const int32_t *seq_len, const int32_t *kv_start_idx, int batch,
+                                 int q_len, int num_q_heads,
                                  int num_kv_heads, int head_dim, int paged, int page_size,
                                  fd_dtype q_dtype, fd_dtype kv_dtype, int32_t *dst,
                                  int64_t dst_len, int capacity_per_cta, int *grid_out,

@@ -99,7 +99,8 @@ def host_shape(kernel: int, num_q_heads: int, num_kv_heads: int, head_dim: int, 
     (32 for 8-bit caches, 16 for 16-bit ones) per stage, r = 65536 bytes of
     K+V over one r-step's bytes, clamped to [1, 4] and halved while a box
     would exceed 256 rows; tile = SUB * wph * r; a segment start costs
-    ceil(128 KiB / stage bytes) tiles; grid = one CTA per SM.
+    ceil(128 KiB / stage bytes) tiles, twice that when wph > 1 (the warps of
+    a head tile merge at every segment end); grid = one CTA per SM.
     kernel 1 (CUDA cores): streams of min(group, 16) query heads of one KV
     head, 32-token tiles, one CTA per SM, no start cost.
     """
@@ -119,4 +120,4 @@ def host_shape(kernel: int, num_q_heads: int, num_kv_heads: int, head_dim: int, 
         r //= 2
     tile = sub * wph * r
     stage = 2 * hc * tile * row
-    return num_kv_heads // hc, tile, sms, -(-131072 // stage)
+    return num_kv_heads // hc, tile, sms, (2 if wph > 1 else 1) * -(-131072 // stage)

@@ -197,7 +197,7 @@ def test_debug_hook_arguments_are_checked_on_the_host(fda):
     assert lib.fd_debug_set_wait_limit(0, 0) == 0
     grid = ctypes.c_int(0)
     # no dst, no workspace, bad q_len: refused before any device work
-    assert lib.fd_debug_plan_segments(0x1000, 2, 1, 8, 2, 128, 0, 0, 0, 0, None, 0, 4,
+    assert lib.fd_debug_plan_segments(0x1000, None, 2, 1, 8, 2, 128, 0, 0, 0, 0, None, 0, 4,
                                       ctypes.byref(grid), 0x2000, 1 << 20, None) == 1
-    assert lib.fd_debug_plan_segments(0x1000, 2, 0, 8, 2, 128, 0, 0, 0, 0, 0x3000, 1 << 20, 4,
-                                      ctypes.byref(grid), 0x2000, 1 << 20, None) == 1
+    assert lib.fd_debug_plan_segments(0x1000, None, 2, 0, 8, 2, 128, 0, 0, 0, 0, 0x3000, 1 << 20,
+                                      4, ctypes.byref(grid), 0x2000, 1 << 20, None) == 1

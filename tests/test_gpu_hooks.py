@@ -23,11 +23,13 @@ def _plan_cases():
         fw.make_contiguous("p4", 4, [131072], 16, 1, 128, "f16", "e4m3"),
         # more streams than threads per CTA (the plan's multi-pass branch)
         fw.make_contiguous("p5", 6, list(rng.integers(0, 300, 700)), 8, 8, 64, "f16", "e4m3"),
+        # 250 streams: one pass of the plan, most threads busy
+        fw.make_contiguous("p6", 7, list(rng.integers(0, 900, 250)), 64, 8, 128, "f16", "e4m3"),
     ]
 
 
 @pytest.mark.parametrize("kernel", [1, 2])
-@pytest.mark.parametrize("case", range(6))
+@pytest.mark.parametrize("case", range(7))
 def test_device_plan_matches_restatement(kernel, case):
     fda = lib()
     w = _plan_cases()[case]
@@ -60,7 +62,7 @@ def test_device_plan_matches_restatement(kernel, case):
 
 
 @pytest.mark.parametrize("kernel", [1, 2])
-@pytest.mark.parametrize("case", range(6))
+@pytest.mark.parametrize("case", range(7))
 def test_device_segments_match_restatement(kernel, case):
     """Every CTA's segments (stream, token range, complete, partial slot), as
     the split kernels' own plan and segment walk produce them on the device,
@@ -76,9 +78,11 @@ def test_device_segments_match_restatement(kernel, case):
             pytest.skip("kernel does not support this shape")
         ws = fda.alloc_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim)
         seq = torch.from_numpy(w.seq_len).cuda()
+        kvs = None if w.paged else torch.from_numpy(w.kv_start_idx).cuda()
         got = fda.fd_debug_plan_segments(seq, w.q_len, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                          w.paged, max(w.page_size, 1), qd, kd, ws,
-                                         capacity_per_cta=1024)
+                                         capacity_per_cta=1024, kv_start_idx=kvs)
+        assert fda.fd_check_device_error(ws)[0] == fda.FD_OK
     finally:
         fda.fd_set_kernel(0)
     head, prefix = fda.fd_debug_read_plan(ws)
