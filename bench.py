@@ -618,7 +618,6 @@ def run_gpu(args):
     split_avg = sum(split_ms) / K
     achieved = alg / (split_avg * 1e-3) / 1e9
     peak, peak_src = measured_peak()
-    fused = kname == "mma"   # the tensor-core kernel merges split streams itself
     per_config = None
     if not args.no_per_config and world == 1:
         clocks2 = ClockSampler(local, not args.no_clocks)
@@ -643,18 +642,16 @@ def run_gpu(args):
                    "l2": "flushed between steps (write then read of 2x L2 buffers, outside the "
                          "timed events)",
                    "parallelism": f"replicas x{world}"},
-        # per step: the split kernel (which also merges split streams on the
-        # tensor-core path; else a combine kernel follows) and the append;
-        # the headline loop, the roofline loop and the unflushed diagnostic
-        "gpu_launches": ((1 if fused else 2) + (1 if args.append else 0)) * (2 * K + n_hot),
+        # split + combine (+ append) per step: the headline loop, the
+        # roofline loop and the unflushed diagnostic
+        "gpu_launches": (3 if args.append else 2) * (2 * K + n_hot),
         "diagnostic_unflushed_us_per_step": round(hot_us, 2),
         "env": device_env(dev),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if (args.shared_prefix or args.scales != "tensor")
                      else recorded_traffic(kname, args.config),
-                     "kernel": (f"split ({kname}), merging split streams in the same launch"
-                                if fused else f"split ({kname})"),
+                     "kernel": f"split ({kname})",
                      "split_us": round(split_avg * 1e3, 2)},
         "e2e": e2e,
         "clocks": clk,
