@@ -456,6 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         sh.qfrag_bytes);   // per-token scales (TOK)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // K/V lines are read once: they leave L2 first (policy made before the plan)
+  uint64_t kv_policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(kv_policy));
   if (threadIdx.x == 0) FD_STAMP(g_split_stamps, 0, stamp_ns());
 #ifdef FD_STAMPS
   if (threadIdx.x == 0) {
@@ -501,8 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA copies of each tile as soon as its stage is free.
     // K/V lines are read once: they leave L2 first, before Q rows, index
     // data and partial states
-    uint64_t kv_policy;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(kv_policy));
+
     SegmentIter it;
     it.init(p, plan);
     Segment seg;
