@@ -167,11 +167,8 @@ bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv
   if (head_dim != 64 && head_dim != 128) return false;
   if (group < 1 || group > 128 || num_kv_heads < 1) return false;
   if (paged && (page_size < 1 || page_size > 256)) return false;
-  if (paged) {
-    // every TMA box must start on a 1024-byte swizzle atom of shared memory
-    const Shape s = make_shape(group, num_kv_heads, head_dim, kv_dtype, page_size, false);
-    if ((s.box_rows * s.row_bytes) % 1024 != 0) return false;
-  }
+  // (pages too small for a TMA box to start on a 1024-byte swizzle atom of
+  // shared memory are gathered by the producer warp instead)
   if (!encode_fn()) return false;
   return true;
 }
@@ -203,8 +200,10 @@ cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {
   CUtensorMap& mv = maps.v;
   // Prefer one box per tile covering all hc heads (fewer, larger TMA copies);
   // fall back to one box per head when the tile spans several pages or the
-  // driver refuses the head-minor view.
-  if (sh.hc > 1 && sh.box_rows == sh.tile &&
+  // driver refuses the head-minor view.  Gathered rows need no tensor map.
+  if (sh.gather) {
+    // no maps
+  } else if (sh.hc > 1 && sh.box_rows == sh.tile &&
       get_map(p.k, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
               sh.hc, &mk) &&
       get_map(p.v, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
@@ -216,7 +215,7 @@ cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {
                       sh.row_bytes, 0, &mv)) {
     return cudaErrorInvalidValue;
   }
-  if (p.scale_kind == FD_SCALE_TOKEN &&
+  if (p.scale_kind == FD_SCALE_TOKEN && !sh.gather &&
       get_scale_map(p.k_scales, p.kv_rows, p.num_kv_heads, sh.hc, sh.box_rows, &maps.ks) &&
       get_scale_map(p.v_scales, p.kv_rows, p.num_kv_heads, sh.hc, sh.box_rows, &maps.vs))
     sh.scale_tma = 1;

@@ -74,6 +74,8 @@ struct Shape {
   int kv_bytes;      // K (or V) bytes of one stage = hc * nx * region_bytes
   int heads_box;     // 1: one TMA box covers all hc heads of a tile
   int scale_tma;     // 1: per-token scales come by TMA (else by 4-byte cp.async)
+  int gather;        // 1: K/V rows gathered by the producer warp with 16-byte cp.async
+                     // (pages too small for a TMA box to start on a swizzle atom)
   int stages;
   int merge_in_stage;   // 1: the warps of a head tile merge in the stage of the segment's last tile
   int merge_bytes;      // a dedicated merge area (wph > 1 and no stage is large enough)
@@ -110,6 +112,8 @@ inline Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype,
   s.tile = sub * s.wph * s.r;
   s.box_rows = page_size > 0 && page_size < s.tile ? page_size : s.tile;
   s.region_bytes = s.tile * s.row_bytes;
+  // a TMA box must land on a whole swizzle atom (1024 bytes) of shared memory
+  s.gather = page_size > 0 && (s.box_rows * s.row_bytes) % 1024 != 0 ? 1 : 0;
   s.heads_box = 0;   // decided at launch (needs a tensor map over {dims, rows, heads})
   s.scale_tma = 0;   // decided at launch (needs a tensor map over the scale arrays)
   s.kv_bytes = s.hc * s.nx * s.region_bytes;
@@ -205,6 +209,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 16-byte asynchronous global -> shared copy, cached in L2 only.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
 }
 
 // 4-byte asynchronous global -> shared copy; src_bytes 0 writes zero.
@@ -469,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
   if (threadIdx.x == 0) {
     for (int i = 0; i < sh.stages; ++i) {
-      mbar_init(&sm.full[i], TOK && !sh.scale_tma ? 1 + 32 : 1);
+      // producer lane 0, plus every producer lane when it copies with cp.async
+      mbar_init(&sm.full[i], sh.gather || (TOK && !sh.scale_tma) ? 1 + 32 : 1);
       mbar_init(&sm.empty[i], kConsumerWarps);
     }
     sm.abort_flag = 0;
@@ -477,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // work that does not need the plan: the tensor-map descriptors and the
   // index array the producer reads first
-  if (threadIdx.x == kConsumerWarps * 32) {
+  if (threadIdx.x == kConsumerWarps * 32 && !sh.gather) {
     prefetch_map(&tmk);
     prefetch_map(&tmv);
   }
@@ -554,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               *(volatile int*)&sm.abort_flag = 1;
             }
             stop = true;
-          } else {
+          } else if (!sh.gather) {
             const int nbox = sh.tile / sh.box_rows;
             uint8_t* kst = base + (size_t)stg * 2 * sh.kv_bytes;
             uint8_t* vst = kst + sh.kv_bytes;
@@ -626,6 +637,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         stop = __shfl_sync(0xffffffffu, stop, 0);
         if (stop) break;
+        if (sh.gather) {
+          // every lane copies 16-byte chunks of the tile's rows into the
+          // layout the TMA boxes would have written (regions [nx][hc], rows
+          // of row_bytes, chunks swizzled); rows outside the cache are
+          // recorded and leave the stage marked bad
+          const int stg = (int)(n % S);
+          uint8_t* kst = base + (size_t)stg * 2 * sh.kv_bytes;
+          uint8_t* vst = kst + sh.kv_bytes;
+          const int cpr = sh.row_bytes >> 4;              // chunks per row of a region
+          const int per_row = sh.hc * sh.nx * cpr;         // chunks of one token, one tensor
+          const int lpr = per_row < 32 ? per_row : 32;     // lanes per token
+          const int rstep = 32 / lpr;
+          const size_t row_stride = (size_t)p.num_kv_heads * D * ELEM;
+          bool badrow = false;
+          for (int j = lane % lpr; j < per_row; j += lpr) {
+            const int c = j % cpr, hx = j / cpr, x = hx % sh.nx, h = hx / sh.nx;
+            const size_t col = ((size_t)(kvh0 + h) * D) * ELEM + (size_t)x * sh.row_bytes + (c << 4);
+            const size_t dcol = (size_t)(x * sh.hc + h) * sh.region_bytes;
+            for (int tt = lane / lpr; tt < valid; tt += rstep) {
+              const int t = t0 + tt;
+              long long row;
+              if (p.block_table) {
+                const int page = sm.pages[(t >> p.page_shift) - win_lo];
+                row = ((long long)page << p.page_shift) + (t & (p.page_size - 1));
+                if (page < 0 || row >= p.kv_rows) {
+                  if (!badrow) raise_error(p.ws, kErrBounds, page);
+                  badrow = true;
+                  continue;
+                }
+              } else {
+                row = start + t;
+                if (row < 0 || row >= p.kv_rows) {
+                  if (!badrow) raise_error(p.ws, kErrBounds, row);
+                  badrow = true;
+                  continue;
+                }
+              }
+              const uint32_t swz = sh.row_bytes == 128 ? (tt & 7) : ((tt >> 1) & 3);
+              const size_t src = (size_t)row * row_stride + col;
+              const size_t dst = dcol + (size_t)tt * sh.row_bytes + ((c ^ swz) << 4);
+              const uint8_t* ks = static_cast<const uint8_t*>(p.k) + src;
+              const uint8_t* vs = static_cast<const uint8_t*>(p.v) + src;
+              // (self-check: 16-byte aligned, inside the stage and the cache)
+              if (((reinterpret_cast<uintptr_t>(ks) | reinterpret_cast<uintptr_t>(vs) |
+                    reinterpret_cast<uintptr_t>(kst + dst)) & 15u) != 0 ||
+                  dst + 16 > (size_t)sh.kv_bytes || src + 16 > (size_t)p.kv_rows * row_stride) {
+                if (!badrow) raise_error(p.ws, kErrBounds, (long long)dst);
+                badrow = true;
+                continue;
+              }
+              cp_async16(kst + dst, ks);
+              cp_async16(vst + dst, vs);
+            }
+          }
+          const bool anybad = __any_sync(0xffffffffu, badrow);
+          if (lane == 0) {
+            sm.bad[stg] = anybad ? 1 : 0;
+            mbar_arrive(&sm.full[stg]);
+          }
+        }
         if (n == n_seg0 + S - 1) {   // the next copy waits for a released stage anyway
           // the next segment's row data ahead: its kv_start into a register,
           // or its first window of block-table entries into L2
@@ -642,13 +713,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (TOK && !sh.scale_tma) {
+        if (sh.gather || (TOK && !sh.scale_tma)) {
           // the tile's per-token scales of its hc heads, element by element
-          // (rows past the end, or outside the cache, read as zero)
+          // (rows past the end, or outside the cache, read as zero); then
+          // every lane's copies complete on the stage's "full" barrier
           const int stg = (int)(n % S);
           float* dk = scl + (size_t)stg * (sh.scale_bytes / 4);
           float* dv = dk + sh.hc * sh.tile;
-          for (int idx = lane; idx < sh.hc * sh.tile; idx += 32) {
+          for (int idx = lane; TOK && !sh.scale_tma && idx < sh.hc * sh.tile; idx += 32) {
             const int tt = idx / sh.hc, h = idx - tt * sh.hc;
             const int t = t0 + tt;
             long long row = -1;
@@ -669,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if constexpr (TOK) asm volatile("cp.async.wait_all;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0 && stop) {
       // drain: copies of the last S issued tiles must land before the CTA
       // exits; a drain that gives up is recorded on its own

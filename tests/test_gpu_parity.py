@@ -96,7 +96,7 @@ def _fill_unowned_rows_with_nan(w):
 
 
 @pytest.mark.parametrize("kv_dtype,P", [("e4m3", 0), ("e4m3", 16), ("e4m3", 64), ("f16", 0),
-                                        ("f16", 16), ("bf16", 32)])
+                                        ("f16", 16), ("bf16", 32), ("e4m3", 4), ("f16", 2)])
 @pytest.mark.parametrize("qh,kvh", [(16, 2), (8, 8), (16, 1)])
 def test_nan_in_rows_outside_sequences_never_leaks(kv_dtype, P, qh, kvh):
     """Rows past a sequence's end are loaded with its last tile (box rows,
@@ -173,11 +173,27 @@ def test_head_groupings(qh, kvh):
     check_workload(w)
 
 
-@pytest.mark.parametrize("P", [1, 2, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16, 32, 64, 128, 256])
 def test_paged_page_sizes(P):
     lens = [1, P - 1 if P > 1 else 2, P, P + 1, 3 * P + 5, 700]
     base = fw.make_contiguous(f"paged{P}", 300 + P, lens, 16, 2, 128, "f16", "e4m3")
     w = fw.to_paged(base, P, 301 + P, extra_stride=2)
+    check_workload(w)
+
+
+@pytest.mark.parametrize("P,D,kv,qh,kvh", [(2, 64, "e4m3", 16, 2), (8, 64, "e4m3", 64, 8),
+                                           (4, 128, "bf16", 32, 8), (1, 64, "f16", 8, 8),
+                                           (4, 128, "i8", 64, 8)])
+def test_small_pages_on_tensor_cores(P, D, kv, qh, kvh):
+    """Pages too small for a TMA box to start on a swizzle atom: the
+    tensor-core kernel gathers their rows itself, and is what AUTO picks."""
+    q = "bf16" if kv == "bf16" else "f16"
+    base = fw.make_contiguous(f"small-pages{P}-{D}-{kv}", 330 + P + D, [1, 3, 9, 31, 200, 1100],
+                              qh, kvh, D, q, kv)
+    w = fw.to_paged(base, P, 331 + P)
+    fda = lib()
+    assert fda.fd_selected_kernel(w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                  0 if q == "f16" else 1, fda.DTYPE_CODES[kv], 1, P) == MMA
     check_workload(w)
 
 
