@@ -3,6 +3,7 @@ the same seeded inputs, for the five decode workloads at full size and for
 edge cases (empty and one-token sequences, lengths around tile and page
 boundaries, poisoned gaps and pages, every head grouping, both head
 dimensions, every dtype pair, page sizes 1 .. 256)."""
+import dataclasses
 import functools
 
 import numpy as np
@@ -152,6 +153,18 @@ def test_config_full_size_int8(n, kind):
     if kind:
         w = fw.with_scales(w, kind, 74 + n)
     check_workload(w, label=f"config{n}-i8-scales{kind}")
+
+
+@pytest.mark.parametrize("D,kvh", [(128, 8), (64, 1)])
+def test_int8_one_signed_queries(D, kvh):
+    """INT8 keys with f16 queries are widened biased (1152 + code) and the
+    score subtracts 1152 * sum(q): queries of one sign make sum(q) large,
+    the hardest case for that fold's fp32 accumulation."""
+    w = fw.make_contiguous(f"i8-posq-{D}-{kvh}", 90 + D + kvh, [5, 600, 4000, 33], 8 * kvh, kvh, D,
+                           "f16", "i8", gap=1)
+    q = np.abs(w.q.view(np.float16).astype(np.float32)) * 2.0
+    w = dataclasses.replace(w, q=fw.f32_to_f16_bits(q).view(w.q.dtype))
+    check_workload(w)
 
 
 @pytest.mark.parametrize("qh,kvh,D,P", [(16, 1, 64, 0), (64, 8, 128, 32), (40, 5, 128, 0),
