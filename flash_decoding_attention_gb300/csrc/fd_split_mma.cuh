@@ -132,7 +132,7 @@ inline Shape make_shape(int group, int num_kv_heads, int head_dim, int kv_dtype,
   // CTA beside the split kernel's on the 64/8-head shape).
   (void)token_scales;
   s.qrows = group <= 8 ? 8 : 16;
-  s.flip = elem == 1 && head_dim == 128 && group <= 8 && s.wph == 1 ? 1 : 0;
+  s.flip = head_dim == 128 && group <= 8 && s.wph == 1 ? 1 : 0;
   s.qfrag_bytes = s.mt * s.hc * (head_dim / 16) * (s.qrows == 8 ? 256 : 512);
   s.scale_bytes = token_scales ? 2 * s.hc * s.tile * 4 : 0;
   int st = (kSmemBudget - 1024 - s.merge_bytes - s.qfrag_bytes) / (2 * s.kv_bytes + s.scale_bytes);
@@ -356,6 +356,15 @@ __device__ __forceinline__ uint2 widen8x4(uint32_t w) {
   }
 }
 
+// FLIP form, head_dim 128: head dim of row r of the O^T accumulator's
+// m-tile j (row r + 8 is the next dim).  8-bit caches: 16 r + 2 j (a lane's
+// V bytes are one 16-byte chunk); 16-bit caches: 64 (j / 4) + 8 r + 2 (j % 4)
+// (one 16-byte chunk of each 128-byte region).
+template <int ELEM>
+__device__ __forceinline__ int flip_dim(int j, int r) {
+  return ELEM == 1 ? 16 * r + 2 * j : 64 * (j >> 2) + 8 * r + 2 * (j & 3);
+}
+
 // Transpose of an 8x8 matrix of 16-bit values held one row pair per lane
 // (lane l: row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1) into the same
 // fragment layout.
@@ -455,9 +464,9 @@ struct Shared {
 // consumer multiplies each score by its token's K scale and each probability
 // by its token's V scale before the P V product (the softmax sum keeps the
 // unscaled probabilities).
-// FLIP: at most 8 query heads per KV head, one warp per head tile (8-bit
-// caches, head_dim 128, one query token): the MMAs take tokens as M and the
-// heads as N (see the FLIP branch of the sub-tile loop).
+// FLIP: at most 8 query heads per KV head, one warp per head tile
+// (head_dim 128, one query token): the MMAs take tokens as M and the heads
+// as N (see the FLIP branch of the sub-tile loop).
 template <int KVT, typename QT, int D, bool TOK, int QROWS, bool CAUSAL, bool FLIP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mma_split_kernel(const Params p, const Shape sh, const __grid_constant__ CUtensorMap tmk,
@@ -864,43 +873,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool edge = min(left0, left1) < SUB;
             if constexpr (FLIP) {
-              // ---- S^T = K Q^T: two m-tiles of 16 tokens (this lane: tokens
-              //      r, r + 8, r + 16, r + 24 of the sub-tile) by the 8 heads
-              //      (this lane: heads 2q, 2q + 1).  K is the A operand,
-              //      widened from the same 32-byte row slices (head dims
-              //      32q .. 32q + 31, 4 per k-step) as in the unflipped form;
-              //      Q of head r is the B operand (the 8-row fragment store).
-              uint32_t w[4][8];
+              // ---- S^T = K Q^T: MT m-tiles of 16 tokens (8-bit: this lane's
+              //      tokens r, r + 8, r + 16, r + 24 of the sub-tile; 16-bit:
+              //      r, r + 8) by the 8 heads (this lane: heads 2q, 2q + 1).
+              //      K is the A operand, from the same row slices as in the
+              //      unflipped form (the same head-dim order, kdim); Q of
+              //      head r is the B operand (the 8-row fragment store).
+              constexpr int MT = SUB / 16;
+              float st[MT][4];
 #pragma unroll
-              for (int jn = 0; jn < 4; ++jn) {
-                const int tk = sub + 8 * jn + r;
-                const uint4 a0 = lds128(chunk_addr(kreg, tk, 2 * q, sh.row_bytes));
-                const uint4 a1 = lds128(chunk_addr(kreg, tk, 2 * q + 1, sh.row_bytes));
-                w[jn][0] = a0.x; w[jn][1] = a0.y; w[jn][2] = a0.z; w[jn][3] = a0.w;
-                w[jn][4] = a1.x; w[jn][5] = a1.y; w[jn][6] = a1.z; w[jn][7] = a1.w;
-              }
-              float st[2][4];
+              for (int mt = 0; mt < MT; ++mt) st[mt][0] = st[mt][1] = st[mt][2] = st[mt][3] = 0.f;
+              if constexpr (ELEM == 1) {
+                uint32_t w[4][8];
 #pragma unroll
-              for (int mt = 0; mt < 2; ++mt) st[mt][0] = st[mt][1] = st[mt][2] = st[mt][3] = 0.f;
+                for (int jn = 0; jn < 4; ++jn) {
+                  const int tk = sub + 8 * jn + r;
+                  const uint4 a0 = lds128(chunk_addr(kreg, tk, 2 * q, sh.row_bytes));
+                  const uint4 a1 = lds128(chunk_addr(kreg, tk, 2 * q + 1, sh.row_bytes));
+                  w[jn][0] = a0.x; w[jn][1] = a0.y; w[jn][2] = a0.z; w[jn][3] = a0.w;
+                  w[jn][4] = a1.x; w[jn][5] = a1.y; w[jn][6] = a1.z; w[jn][7] = a1.w;
+                }
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint2 qb = lds64(qf + kk * 256);
+                for (int kk = 0; kk < 8; ++kk) {
+                  const uint2 qb = lds64(qf + kk * 256);
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                  const uint2 ka = widen8x4<KVT, BF16>(w[2 * mt][kk]);       // token r
-                  const uint2 kb = widen8x4<KVT, BF16>(w[2 * mt + 1][kk]);   // token r + 8
-                  mma16816<BF16>(st[mt], ka.x, kb.x, ka.y, kb.y, qb.x, qb.y);
+                  for (int mt = 0; mt < MT; ++mt) {
+                    const uint2 ka = widen8x4<KVT, BF16>(w[2 * mt][kk]);       // token r
+                    const uint2 kb = widen8x4<KVT, BF16>(w[2 * mt + 1][kk]);   // token r + 8
+                    mma16816<BF16>(st[mt], ka.x, kb.x, ka.y, kb.y, qb.x, qb.y);
+                  }
+                }
+              } else {   // 16-bit: chunk pairs (2q, 2q + 1) of each 128-byte region
+#pragma unroll
+                for (int x2 = 0; x2 < D / 64; ++x2) {
+                  const uint32_t reg = kreg + x2 * xstride;
+                  const uint4 c00 = lds128(chunk_addr(reg, sub + r, 2 * q, sh.row_bytes));
+                  const uint4 c01 = lds128(chunk_addr(reg, sub + r, 2 * q + 1, sh.row_bytes));
+                  const uint4 c10 = lds128(chunk_addr(reg, sub + r + 8, 2 * q, sh.row_bytes));
+                  const uint4 c11 = lds128(chunk_addr(reg, sub + r + 8, 2 * q + 1, sh.row_bytes));
+#pragma unroll
+                  for (int k4 = 0; k4 < 4; ++k4) {
+                    const uint2 qb = lds64(qf + (x2 * 4 + k4) * 256);
+                    const uint4 t0 = k4 < 2 ? c00 : c01, t1 = k4 < 2 ? c10 : c11;
+                    const uint32_t a0 = (k4 & 1) ? t0.z : t0.x, a2 = (k4 & 1) ? t0.w : t0.y;
+                    const uint32_t a1 = (k4 & 1) ? t1.z : t1.x, a3 = (k4 & 1) ? t1.w : t1.y;
+                    mma16816<BF16>(st[0], a0, a1, a2, a3, qb.x, qb.y);
+                  }
                 }
               }
               // ---- online softmax per head: st[mt][e] is token 16 mt + r
               //      (+ 8 for e >= 2) of head 2q + (e & 1); the 8 lanes of a
-              //      head (r = 0..7) hold its 32 tokens
+              //      head (r = 0..7) hold its tokens
               const uint32_t tsk =
                   smem_u32(scl) + 4u * (uint32_t)(stg * (sh.scale_bytes / 4) + sub * sh.hc + kvl);
               const uint32_t tsv = tsk + 4u * (uint32_t)(sh.hc * sh.tile);
               float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-              for (int mt = 0; mt < 2; ++mt) {
+              for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                   const int tok = 16 * mt + r + 8 * hf;
@@ -927,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               m1 = mn1;
               float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-              for (int mt = 0; mt < 2; ++mt) {
+              for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                   st[mt][2 * hf] = fast_exp2(st[mt][2 * hf] - base0);
@@ -940,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               l1 = fmaf(l1, a1, ps1);
               if constexpr (TOK) {   // V scales weight the probabilities, not their sum
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
+                for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
                   for (int hf = 0; hf < 2; ++hf) {
                     const int tok = 16 * mt + r + 8 * hf;
@@ -963,37 +992,48 @@ __global__ void __launch_bounds__(kThreads, 1)
               //      at a time.  P^T (B operand): the probabilities packed per
               //      token row and transposed by movmatrix, so that this
               //      lane holds tokens 2q, 2q + 1 (+ 8) of head r.  V^T (A
-              //      operand): m-tile j holds head dims 16 r + 2 j (row r)
-              //      and 16 r + 2 j + 1 (row r + 8), so this lane's V bytes
-              //      are one 16-byte chunk of each of its four token rows.
+              //      operand): rows r and r + 8 of m-tile j are head dims
+              //      flip_dim(j, r) and flip_dim(j, r) + 1, so this lane's V
+              //      values are one 16-byte chunk of each of its four token
+              //      rows (per 128-byte region).
 #pragma unroll
-              for (int kt = 0; kt < 2; ++kt) {
+              for (int kt = 0; kt < MT; ++kt) {
                 const uint32_t pb0 =
                     movmatrix_trans(pack_f32x2(st[kt][0], st[kt][1], BF16));   // token r
                 const uint32_t pb1 =
                     movmatrix_trans(pack_f32x2(st[kt][2], st[kt][3], BF16));   // token r + 8
                 const int u0 = sub + 16 * kt + 2 * q, u1 = u0 + 1, u2 = u0 + 8, u3 = u0 + 9;
-                uint4 w0 = lds128(chunk_addr(vreg, u0, r, sh.row_bytes));
-                uint4 w1 = lds128(chunk_addr(vreg, u1, r, sh.row_bytes));
-                uint4 w2 = lds128(chunk_addr(vreg, u2, r, sh.row_bytes));
-                uint4 w3 = lds128(chunk_addr(vreg, u3, r, sh.row_bytes));
-                if (left < SUB) zero_rows_past_end(w0, w1, w2, w3, 16 * kt + 2 * q, left);
-                const uint32_t A[4] = {w0.x, w0.y, w0.z, w0.w}, B[4] = {w1.x, w1.y, w1.z, w1.w};
-                const uint32_t C[4] = {w2.x, w2.y, w2.z, w2.w}, E[4] = {w3.x, w3.y, w3.z, w3.w};
 #pragma unroll
-                for (int wd = 0; wd < 4; ++wd) {
-                  const uint32_t lo01 = __byte_perm(A[wd], B[wd], 0x5140);
-                  const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
-                  const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
-                  const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
-                  const uint2 l01 = widen8x4<KVT, BF16>(lo01), l89 = widen8x4<KVT, BF16>(lo89);
-                  const uint2 h01 = widen8x4<KVT, BF16>(hi01), h89 = widen8x4<KVT, BF16>(hi89);
-                  mma16816<BF16>(o[2 * wd], l01.x, l01.y, l89.x, l89.y, pb0, pb1);
-                  mma16816<BF16>(o[2 * wd + 1], h01.x, h01.y, h89.x, h89.y, pb0, pb1);
+                for (int x2 = 0; x2 < (ELEM == 1 ? 1 : D / 64); ++x2) {
+                  const uint32_t reg = vreg + x2 * xstride;
+                  uint4 w0 = lds128(chunk_addr(reg, u0, r, sh.row_bytes));
+                  uint4 w1 = lds128(chunk_addr(reg, u1, r, sh.row_bytes));
+                  uint4 w2 = lds128(chunk_addr(reg, u2, r, sh.row_bytes));
+                  uint4 w3 = lds128(chunk_addr(reg, u3, r, sh.row_bytes));
+                  if (left < SUB) zero_rows_past_end(w0, w1, w2, w3, 16 * kt + 2 * q, left);
+                  const uint32_t A[4] = {w0.x, w0.y, w0.z, w0.w}, B[4] = {w1.x, w1.y, w1.z, w1.w};
+                  const uint32_t C[4] = {w2.x, w2.y, w2.z, w2.w}, E[4] = {w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+                  for (int wd = 0; wd < 4; ++wd) {
+                    if constexpr (ELEM == 1) {
+                      const uint32_t lo01 = __byte_perm(A[wd], B[wd], 0x5140);
+                      const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
+                      const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
+                      const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
+                      const uint2 l01 = widen8x4<KVT, BF16>(lo01), l89 = widen8x4<KVT, BF16>(lo89);
+                      const uint2 h01 = widen8x4<KVT, BF16>(hi01), h89 = widen8x4<KVT, BF16>(hi89);
+                      mma16816<BF16>(o[2 * wd], l01.x, l01.y, l89.x, l89.y, pb0, pb1);
+                      mma16816<BF16>(o[2 * wd + 1], h01.x, h01.y, h89.x, h89.y, pb0, pb1);
+                    } else {   // two head dims per word
+                      mma16816<BF16>(o[4 * x2 + wd], __byte_perm(A[wd], B[wd], 0x5410),
+                                     __byte_perm(A[wd], B[wd], 0x7632),
+                                     __byte_perm(C[wd], E[wd], 0x5410),
+                                     __byte_perm(C[wd], E[wd], 0x7632), pb0, pb1);
+                    }
+                  }
                 }
               }
-              continue;
-            }
+            } else {
             // ---- S = Q K^T over NJ n-tiles of 8 tokens.  Each Q fragment is
             //      read from shared memory once and used for every n-tile.
             float s[NJ][4];
@@ -1225,6 +1265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
+            }   // FLIP
           }
         }
         __syncwarp();
@@ -1245,8 +1286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* lsep = p.lse ? p.lse + qrow0 : nullptr;
       if constexpr (FLIP) {
         // ---- end of segment: a head's sum over its 8 lanes; head 2q + hh
-        //      holds head dims 16 r + 2 j (o[j][hh]) and 16 r + 2 j + 1
-        //      (o[j][2 + hh]), 16 consecutive dims per lane
+        //      holds head dims flip_dim(j, r) (o[j][hh]) and flip_dim(j, r) + 1
+        //      (o[j][2 + hh]); m-tiles j, j + 1 (j even) are 4 consecutive dims
 #pragma unroll
         for (int o2 = 4; o2 < 32; o2 <<= 1) {
           l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
@@ -1260,19 +1301,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float L = hh ? l1 : l0, M = hh ? m1 : m0;
           if (seg.complete) {
             const float rs = L > 0.f ? vsc / L : 0.f;
-            uint32_t pk[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) pk[j] = pack_f32x2(o[j][hh] * rs, o[j][2 + hh] * rs, BF16);
-            uint4* dst = reinterpret_cast<uint4*>(outp + li * D + 16 * r);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            for (int j = 0; j < 8; j += 2)
+              *reinterpret_cast<uint2*>(outp + li * D + flip_dim<ELEM>(j, r)) =
+                  make_uint2(pack_f32x2(o[j][hh] * rs, o[j][2 + hh] * rs, BF16),
+                             pack_f32x2(o[j + 1][hh] * rs, o[j + 1][2 + hh] * rs, BF16));
             if (lsep && r == 0) lsep[li] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
           } else {
-            float4* dst = reinterpret_cast<float4*>(part + li * D + 16 * r);
 #pragma unroll
-            for (int j4 = 0; j4 < 4; ++j4)
-              dst[j4] = make_float4(o[2 * j4][hh], o[2 * j4][2 + hh], o[2 * j4 + 1][hh],
-                                    o[2 * j4 + 1][2 + hh]);
+            for (int j = 0; j < 8; j += 2)
+              *reinterpret_cast<float4*>(part + li * D + flip_dim<ELEM>(j, r)) =
+                  make_float4(o[j][hh], o[j][2 + hh], o[j + 1][hh], o[j + 1][2 + hh]);
             if (r == 0) pml[li] = make_float2(M, L);
           }
         }
@@ -1448,7 +1487,7 @@ cudaError_t launch_t(const Params& p, const Shape& sh, const Maps& m, cudaStream
 // 16 Q rows, or 8.
 template <int KVT, typename QT, int D>
 cudaError_t launch_plain(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st) {
-  if constexpr (kv_elem_bytes(KVT) == 1 && D == 128)
+  if constexpr (D == 128)
     if (sh.flip && p.q_len == 1) return launch_t<KVT, QT, D, false, 8, false, true>(p, sh, m, st);
   if (sh.qrows == 8)
     return p.q_len > 1 ? launch_t<KVT, QT, D, false, 8, true>(p, sh, m, st)
