@@ -300,7 +300,9 @@ class ClockSampler:
 
 
 # sources that make up each split kernel (its traffic changes only with them)
-KERNEL_SOURCES = {"mma": ("fd_common.cuh", "fd_split_mma.cu"),
+KERNEL_SOURCES = {"mma": ("fd_common.cuh", "fd_split_mma.cuh", "fd_split_mma.cu",
+                          "fd_split_mma_e4m3.cu", "fd_split_mma_i8.cu",
+                          "fd_split_mma_16bit.cu"),
                   "simt": ("fd_common.cuh", "fd_split_simt.cu")}
 
 
