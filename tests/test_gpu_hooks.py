@@ -25,11 +25,14 @@ def _plan_cases():
         fw.make_contiguous("p5", 6, list(rng.integers(0, 300, 700)), 8, 8, 64, "f16", "e4m3"),
         # 250 streams: one pass of the plan, most threads busy
         fw.make_contiguous("p6", 7, list(rng.integers(0, 900, 250)), 64, 8, 128, "f16", "e4m3"),
+        # a paged pool (the plan reads seq_len only; the block table is not consulted)
+        fw.to_paged(fw.make_contiguous("p7", 8, list(rng.integers(0, 3000, 24)), 32, 8, 128,
+                                       "f16", "e4m3"), 16, 9),
     ]
 
 
 @pytest.mark.parametrize("kernel", [1, 2])
-@pytest.mark.parametrize("case", range(7))
+@pytest.mark.parametrize("case", range(8))
 def test_device_plan_matches_restatement(kernel, case):
     fda = lib()
     w = _plan_cases()[case]
@@ -62,7 +65,7 @@ def test_device_plan_matches_restatement(kernel, case):
 
 
 @pytest.mark.parametrize("kernel", [1, 2])
-@pytest.mark.parametrize("case", range(7))
+@pytest.mark.parametrize("case", range(8))
 def test_device_segments_match_restatement(kernel, case):
     """Every CTA's segments (stream, token range, complete, partial slot), as
     the split kernels' own plan and segment walk produce them on the device,
