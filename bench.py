@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma", "tc"])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -300,7 +300,11 @@ class ClockSampler:
 
 
 # sources that make up each split kernel (its traffic changes only with them)
-KERNEL_SOURCES = {"mma": ("fd_common.cuh", "fd_split_mma.cuh", "fd_split_mma.cu",
+# arithmetic of each split kernel, for the dtype label
+TENSOR_LABEL = {"mma": "mma", "tc": "tcgen05"}
+
+KERNEL_SOURCES = {"tc": ("fd_common.cuh", "fd_split_mma.cuh", "fd_split_tc.cu"),
+                  "mma": ("fd_common.cuh", "fd_split_mma.cuh", "fd_split_mma.cu",
                           "fd_split_mma_e4m3.cu", "fd_split_mma_i8.cu",
                           "fd_split_mma_16bit.cu"),
                   "simt": ("fd_common.cuh", "fd_split_simt.cu")}
@@ -491,7 +495,7 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     fda.load_library()
-    fda.fd_set_kernel({"auto": 0, "simt": 1, "mma": 2}[args.kernel])
+    fda.fd_set_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3}[args.kernel])
 
     w = make_workload(args)
     t = fw.to_torch(w, dev)
@@ -503,7 +507,7 @@ def run_gpu(args):
     sel = fda.fd_selected_kernel(QH * w.q_len, KVH, D, 0 if w.q_dtype == "f16" else 1,
                                  fda.DTYPE_CODES[w.kv_dtype], w.paged,
                                  max(w.page_size, 1))
-    kname = {1: "simt", 2: "mma"}.get(sel, "none")
+    kname = {1: "simt", 2: "mma", 3: "tc"}.get(sel, "none")
 
     if args.append:
         k_new, v_new = fw.new_tokens(w, 500 + args.config, n_new=w.q_len)
@@ -635,9 +639,9 @@ def run_gpu(args):
         "us_per_step_max": round(max(step_ms) * 1e3, 2),
         "slow_steps": int(sum(1 for x in step_ms if x > 1.5 * float(np.median(step_ms)))),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": (f"{w.kv_dtype}->{w.q_dtype} {'mma' if kname == 'mma' else 'fma'}, f32 acc"
+        "dtype": (f"{w.kv_dtype}->{w.q_dtype} {TENSOR_LABEL.get(kname, 'fma')}, f32 acc"
                   if w.kv_dtype in ("e4m3", "i8")
-                  else f"{w.kv_dtype} {'mma' if kname == 'mma' else 'fma'}, f32 acc"),
+                  else f"{w.kv_dtype} {TENSOR_LABEL.get(kname, 'fma')}, f32 acc"),
         "data": "synthetic",
         "config": {**workload_config(args), "kernel": kname,
                    "algorithmic_bytes_per_step": alg, "sum_seq_len": int(w.seq_len.sum()),

@@ -43,6 +43,7 @@ DTYPE_CODES = {"f16": FD_F16, "bf16": FD_BF16, "e4m3": FD_E4M3, "i8": FD_I8}
 FD_KERNEL_AUTO = 0
 FD_KERNEL_SIMT = 1
 FD_KERNEL_MMA = 2
+FD_KERNEL_TC = 3
 
 FD_SCALE_TENSOR = 0
 FD_SCALE_HEAD = 1

@@ -28,6 +28,10 @@ bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv
                   int paged, int page_size);
 void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms, int* hc,
                 int* tile, int* grid, int* seg_units);
+// tcgen05 kernel (fd_split_tc.cu)
+bool tc_supports(int group, int head_dim, int q_dtype, int kv_dtype, int paged, int page_size,
+                 bool token_scales);
+void tc_config(int group, int sms, int* hc, int* tile, int* grid, int* seg_units);
 
 namespace {
 
@@ -72,10 +76,25 @@ bool dtypes_ok(int q_dtype, int kv_dtype) {
 
 // Chooses the split kernel and its plan shape; false if unsupported.
 bool choose(int pref, int num_q_heads, int num_kv_heads, int head_dim, int q_dtype, int kv_dtype,
-            int paged, int page_size, int sms, Config* c) {
+            int paged, int page_size, int sms, Config* c, bool token_scales = false) {
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return false;
   const int group = num_q_heads / num_kv_heads;
   if (!dtypes_ok(q_dtype, kv_dtype) || (head_dim != 64 && head_dim != 128)) return false;
+  const bool tc_ok = tc_supports(group, head_dim, q_dtype, kv_dtype, paged, page_size, token_scales);
+  // Automatic choice of the tcgen05 kernel where it measured faster than the
+  // mma.sync one: a single KV head with at least 64 query rows (the
+  // long-context MQA workload with 4 and 8 query tokens).  With several KV
+  // heads the mma.sync kernel carries two to eight of them per stream and
+  // stays ahead.
+  const bool tc_auto = tc_ok && num_kv_heads == 1 && group >= 64;
+  if (pref == FD_KERNEL_TC || (pref == FD_KERNEL_AUTO && tc_auto)) {
+    if (!tc_ok) return false;
+    c->kernel = FD_KERNEL_TC;
+    tc_config(group, sms, &c->hc, &c->tile, &c->grid, &c->seg_units);
+    c->hg = num_kv_heads;
+    c->hq = group;
+    return true;
+  }
   const bool mma_ok = mma_supports(group, num_kv_heads, head_dim, q_dtype, kv_dtype, paged, page_size);
   if (pref == FD_KERNEL_MMA || (pref == FD_KERNEL_AUTO && mma_ok)) {
     if (!mma_ok) return false;
@@ -261,7 +280,8 @@ const char* fd_status_string(fd_status status) {
 }
 
 fd_status fd_set_kernel(fd_kernel kernel) {
-  if (kernel != FD_KERNEL_AUTO && kernel != FD_KERNEL_SIMT && kernel != FD_KERNEL_MMA)
+  if (kernel != FD_KERNEL_AUTO && kernel != FD_KERNEL_SIMT && kernel != FD_KERNEL_MMA &&
+      kernel != FD_KERNEL_TC)
     return FD_ERR_INVALID_ARG;
   g_kernel.store(kernel);
   return FD_OK;
@@ -295,7 +315,7 @@ size_t fd_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head
   // Largest layout over every kernel and dtype choice for these sizes.
   const int dts[6][2] = {{FD_F16, FD_F16}, {FD_BF16, FD_BF16}, {FD_F16, FD_E4M3},
                          {FD_BF16, FD_E4M3}, {FD_F16, FD_I8}, {FD_BF16, FD_I8}};
-  for (int pref : {FD_KERNEL_SIMT, FD_KERNEL_MMA}) {
+  for (int pref : {FD_KERNEL_SIMT, FD_KERNEL_MMA, FD_KERNEL_TC}) {
     for (auto& dt : dts) {
       for (int paged : {0, 1}) {
         Config c;
@@ -352,7 +372,7 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
   if (sms <= 0) return FD_ERR_CUDA;
   Config c;
   if (!choose(g_kernel.load(), virt_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, paged,
-              page_size, sms, &c))
+              page_size, sms, &c, scale_kind == FD_SCALE_TOKEN))
     return FD_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(batch * c.hg, c.grid, c.hq, head_dim);
   if (workspace_bytes < L.total) return FD_ERR_WORKSPACE_TOO_SMALL;
@@ -412,7 +432,7 @@ static fd_status decode_impl(const void* q, const void* k_cache, const void* v_c
   if (timed && cudaEventRecord(t_ev_before, st) != cudaSuccess) return FD_ERR_CUDA;
   {
     FD_RANGE("fd.split");
-    cudaError_t e = c.kernel == FD_KERNEL_MMA ? launch_split_mma(p, st) : launch_split_simt(p, st);
+    cudaError_t e = c.kernel == FD_KERNEL_SIMT ? launch_split_simt(p, st) : launch_split_mma(p, st);
     if (e != cudaSuccess) return FD_ERR_CUDA;
   }
   if (timed && cudaEventRecord(t_ev_after, st) != cudaSuccess) return FD_ERR_CUDA;
@@ -658,7 +678,9 @@ int fd_debug_empty_launch(int grid, int threads, int smem, fd_stream_t stream) {
 
 int fd_debug_read_stamps(int which, unsigned long long* host, int n) {
   if (!host || n <= 0) return FD_ERR_INVALID_ARG;
-  const cudaError_t e = which == 0 ? read_split_stamps(host, n) : read_combine_stamps(host, n);
+  const cudaError_t e = which == 0   ? read_split_stamps(host, n)
+                        : which == 1 ? read_combine_stamps(host, n)
+                                     : read_tc_stamps(host, n);
   return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 #endif

@@ -136,6 +136,7 @@ __device__ __forceinline__ unsigned long long stamp_ns() {
 }
 cudaError_t read_split_stamps(unsigned long long* host, int n);
 cudaError_t read_combine_stamps(unsigned long long* host, int n);
+cudaError_t read_tc_stamps(unsigned long long* host, int n);
 cudaError_t launch_empty(int grid, int threads, int smem, cudaStream_t st);
 #else
 #define FD_STAMP(arr, i, v) ((void)0)
@@ -463,6 +464,7 @@ fd_status check_decode_args(const void* q, const void* k_cache, const void* v_ca
 
 // Launchers (defined in their .cu files).
 cudaError_t launch_split_simt(const Params& p, cudaStream_t stream);
+// the tensor-core kernels: mma.sync, or tcgen05 when p.kernel is FD_KERNEL_TC
 cudaError_t launch_split_mma(const Params& p, cudaStream_t stream);
 cudaError_t launch_combine(const Params& p, cudaStream_t stream);
 cudaError_t launch_append(const Params& p, cudaStream_t stream);

@@ -6,6 +6,11 @@
 #include "fd_split_mma.cuh"
 
 namespace fd {
+
+// the tcgen05 split kernel (fd_split_tc.cu)
+cudaError_t launch_split_tc(const Params& p, const CUtensorMap& mk, const CUtensorMap& mv,
+                            cudaStream_t stream);
+
 namespace mma {
 namespace {
 
@@ -191,6 +196,15 @@ void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms
 
 cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {
   if (p.kv_rows >= (1ll << 31)) return cudaErrorInvalidValue;
+  if (p.kernel == FD_KERNEL_TC) {
+    // one KV head per box, 64-token tiles (or the page's rows)
+    const int box_rows = p.block_table && p.page_size < p.tile ? p.page_size : p.tile;
+    CUtensorMap mk, mv;
+    if (!get_map(p.k, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, box_rows, 128, 0, &mk) ||
+        !get_map(p.v, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, box_rows, 128, 0, &mv))
+      return cudaErrorInvalidValue;
+    return launch_split_tc(p, mk, mv, stream);
+  }
   Shape sh = make_shape(p.group, p.num_kv_heads, p.head_dim, p.kv_dtype,
                         p.block_table ? p.page_size : 0, p.scale_kind == FD_SCALE_TOKEN);
   if (sh.stages < 2 || sh.tile != p.tile || sh.hc != p.hc) return cudaErrorInvalidValue;

@@ -84,9 +84,17 @@ typedef enum { FD_F16 = 0, FD_BF16 = 1, FD_E4M3 = 2, FD_I8 = 3 } fd_dtype;
 
 /* Kernel selection for the split (partial attention) phase. */
 typedef enum {
-  FD_KERNEL_AUTO = 0,  /* tensor-core kernel where supported, else CUDA-core kernel */
+  FD_KERNEL_AUTO = 0,  /* FD_KERNEL_TC for one KV head with at least 64 query rows (query
+                          heads times q_len), else FD_KERNEL_MMA where supported, else the
+                          CUDA-core kernel */
   FD_KERNEL_SIMT = 1,  /* CUDA-core FMA kernel (every supported shape) */
-  FD_KERNEL_MMA = 2    /* tensor-core kernel; FD_ERR_UNSUPPORTED where it does not apply */
+  FD_KERNEL_MMA = 2,   /* tensor-core kernel with warp-level mma.sync products, operands
+                          widened in registers; FD_ERR_UNSUPPORTED where it does not apply */
+  FD_KERNEL_TC = 3     /* tensor-core kernel with tcgen05 products (accumulators in tensor
+                          memory, FP8 widened once per tile into shared memory): e4m3
+                          caches, fp16 queries, head_dim 128, 17..128 query rows per KV
+                          head (query heads per KV head times q_len), no per-token scales,
+                          page sizes 8..256; FD_ERR_UNSUPPORTED elsewhere */
 } fd_kernel;
 
 /*
@@ -325,8 +333,9 @@ fd_status fd_set_kernel(fd_kernel kernel);
 
 /*
  * Kernel that fd_decode_attention would run for these sizes under the
- * current fd_set_kernel choice: FD_KERNEL_SIMT or FD_KERNEL_MMA, or -1 if
- * the sizes are unsupported.  Host function.
+ * current fd_set_kernel choice: FD_KERNEL_SIMT, FD_KERNEL_MMA or FD_KERNEL_TC,
+ * or -1 if the sizes are unsupported (num_q_heads counts every query token:
+ * query heads times q_len).  Host function.
  */
 int fd_selected_kernel(int num_q_heads, int num_kv_heads, int head_dim, fd_dtype q_dtype,
                        fd_dtype kv_dtype, int paged, int page_size);

@@ -28,21 +28,38 @@ def _plan_cases():
         # a paged pool (the plan reads seq_len only; the block table is not consulted)
         fw.to_paged(fw.make_contiguous("p7", 8, list(rng.integers(0, 3000, 24)), 32, 8, 128,
                                        "f16", "e4m3"), 16, 9),
+        # query groups above 16 rows (the tcgen05 kernel's shapes)
+        fw.make_contiguous("p8", 10, list(rng.integers(0, 9000, 12)), 64, 2, 128, "f16", "e4m3"),
+        fw.to_paged(fw.make_contiguous("p9", 11, [0, 700, 40000, 5, 64], 128, 1, 128, "f16",
+                                       "e4m3"), 16, 12),
     ]
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
-@pytest.mark.parametrize("case", range(8))
+def _takes(kernel, w):
+    """Whether a forced kernel takes a plan case: the CUDA-core and mma.sync
+    kernels take every case here; the tcgen05 kernel takes e4m3 caches with
+    fp16 queries, head_dim 128 and 17..128 query rows per KV head."""
+    if kernel != 3:
+        return True
+    rows = w.num_q_heads * w.q_len // w.num_kv_heads
+    return (w.kv_dtype == "e4m3" and w.q_dtype == "f16" and w.head_dim == 128
+            and 16 < rows <= 128 and (not w.paged or 8 <= w.page_size <= 256))
+
+
+@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("case", range(10))
 def test_device_plan_matches_restatement(kernel, case):
     fda = lib()
     w = _plan_cases()[case]
     fda.fd_set_kernel(kernel)
-    ok = fda.fd_selected_kernel(w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                0 if w.q_dtype == "f16" else 1,
-                                fda.DTYPE_CODES[w.kv_dtype], w.paged, 1) == kernel
+    sel = fda.fd_selected_kernel(w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                 0 if w.q_dtype == "f16" else 1,
+                                 fda.DTYPE_CODES[w.kv_dtype], w.paged, max(w.page_size, 1))
     fda.fd_set_kernel(0)
-    if not ok:
-        pytest.skip("kernel does not support this shape")
+    if sel != kernel:
+        # a forced kernel that does not take the shape refuses it outright
+        assert sel == -1 and not _takes(kernel, w)
+        return
     ws = fda.alloc_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim)
     run(w, kernel, workspace=ws)
     head, prefix = fda.fd_debug_read_plan(ws)
@@ -53,7 +70,7 @@ def test_device_plan_matches_restatement(kernel, case):
     group = w.num_q_heads // w.num_kv_heads
     assert hq % group == 0 or group % hq == 0      # a stream never splits a KV head's reads
     assert S == w.batch * hg
-    assert seg_units >= 0 and (kernel == 2 or seg_units == 0)
+    assert seg_units >= 0 and (kernel in (2, 3) or seg_units == 0)
     # the host's choice of shape, restated
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     elem = 1 if w.kv_dtype in ("e4m3", "i8") else 2
@@ -64,8 +81,8 @@ def test_device_plan_matches_restatement(kernel, case):
     assert (total, per_cta) == (p_total, p_per_cta)
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
-@pytest.mark.parametrize("case", range(8))
+@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("case", range(10))
 def test_device_segments_match_restatement(kernel, case):
     """Every CTA's segments (stream, token range, complete, partial slot), as
     the split kernels' own plan and segment walk produce them on the device,
@@ -76,9 +93,12 @@ def test_device_segments_match_restatement(kernel, case):
     try:
         qd = 0 if w.q_dtype == "f16" else 1
         kd = fda.DTYPE_CODES[w.kv_dtype]
-        if fda.fd_selected_kernel(w.num_q_heads, w.num_kv_heads, w.head_dim, qd, kd, w.paged,
-                                  1) != kernel:
-            pytest.skip("kernel does not support this shape")
+        sel = fda.fd_selected_kernel(w.num_q_heads, w.num_kv_heads, w.head_dim, qd, kd, w.paged,
+                                     max(w.page_size, 1))
+        if sel != kernel:
+            # a forced kernel that does not take the shape refuses it outright
+            assert sel == -1 and not _takes(kernel, w)
+            return
         ws = fda.alloc_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim)
         seq = torch.from_numpy(w.seq_len).cuda()
         kvs = None if w.paged else torch.from_numpy(w.kv_start_idx).cuda()

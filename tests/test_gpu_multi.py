@@ -1,6 +1,6 @@
 """GPU parity of multi-token query decode (fd_decode_attention_multi: q_len
 query tokens per sequence, causal among the last q_len cached tokens) against
-the oracle, on both split kernels."""
+the oracle, on every split kernel that takes the shape."""
 import functools
 
 import pytest
@@ -11,13 +11,13 @@ from gpu_util import lib, parity, run
 
 pytestmark = pytest.mark.gpu
 
-SIMT, MMA = 1, 2
+SIMT, MMA, TC = 1, 2, 3
 
 
 def kernels_for(w):
     fda = lib()
     ks = []
-    for k in (SIMT, MMA):
+    for k in (SIMT, MMA, TC):
         fda.fd_set_kernel(k)
         sel = fda.fd_selected_kernel(w.num_q_heads * w.q_len, w.num_kv_heads, w.head_dim,
                                      0 if w.q_dtype == "f16" else 1,
