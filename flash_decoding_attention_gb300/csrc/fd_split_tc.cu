@@ -55,15 +55,17 @@ constexpr int kCols = 64;                         // scores per softmax thread p
 template <int M>
 struct TcShape {
   static constexpr int kTile = M == 64 ? 128 : 64;               // tokens per tile
-  static constexpr int kStages = M == 64 ? 2 : 4;                // e4m3 stages
+  static constexpr int kStages = M == 64 ? 2 : 6;                // e4m3 stages
   static constexpr uint32_t kStageBytes = 2u * kTile * kRowBytes;    // K then V
   static constexpr uint32_t kF16Bytes = (uint32_t)kTile * 256u;      // one f16 tile
-  static constexpr uint32_t kOffF16 = kStages * kStageBytes;
-  static constexpr uint32_t kOffQ = kOffF16 + 2u * 2u * kF16Bytes;   // two K/V f16 buffers
+  // one f16 K buffer (read only by the S product of its tile), two V buffers
+  static constexpr uint32_t kOffK16 = kStages * kStageBytes;
+  static constexpr uint32_t kOffV16 = kOffK16 + kF16Bytes;
+  static constexpr uint32_t kOffQ = kOffV16 + 2u * kF16Bytes;
   static constexpr uint32_t kQBytes = (uint32_t)M * 256u;
   static constexpr uint32_t kOffP = kOffQ + kQBytes;
   static constexpr uint32_t kPBytes = (uint32_t)M * kTile * 2u;
-  static constexpr uint32_t kSmem = 1024u + kOffP + kPBytes;
+  static constexpr uint32_t kSmem = 1024u + kOffP + 2u * kPBytes;   // two P buffers
   static constexpr int kTmemCols = M == 64 ? 512 : 256;         // S: 2 x tile, O: 128
 };
 static_assert(TcShape<64>::kSmem <= (uint32_t)mma::kSmemBudget, "shared memory");
@@ -218,12 +220,12 @@ __device__ __forceinline__ uint32_t vmn_chunk(uint32_t tile, int t, int c16) {
          (uint32_t)(t & 7) * 128u + ((uint32_t)((c16 & 7) ^ (t & 7)) << 4);
 }
 
-constexpr int kMaxStagesTC = 4;
+constexpr int kMaxStagesTC = 6;
 
 struct SharedTC {
   uint64_t e_full[kMaxStagesTC], e_empty[kMaxStagesTC];
   uint64_t k_full[2], v_full[2], s_full[2], s_free[2], done[2];
-  uint64_t p_full, o_free, fin;
+  uint64_t p_full[2], o_free, fin;
   int bad[kMaxStagesTC];   // stage held a row outside the cache (producer)
   // tile j came from such a stage (converters, slot j mod 4: the converters
   // run at most three tiles ahead of the softmax warps that read it)
@@ -304,7 +306,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(base);
-  const uint32_t sF16 = sbase + SH::kOffF16;
+  const uint32_t sK16 = sbase + SH::kOffK16;
+  const uint32_t sV16 = sbase + SH::kOffV16;
   const uint32_t sQ = sbase + SH::kOffQ;
   const uint32_t sP = sbase + SH::kOffP;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -323,7 +326,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       mbar_init(&sm.s_free[i], 4);    // the softmax warps
       mbar_init(&sm.done[i], 1);      // MMA commit after P V
     }
-    mbar_init(&sm.p_full, 4);         // the softmax warps
+    mbar_init(&sm.p_full[0], 4);      // the softmax warps
+    mbar_init(&sm.p_full[1], 4);
     mbar_init(&sm.o_free, 4);
     mbar_init(&sm.fin, 1);
     sm.abort_flag = 0;
@@ -462,10 +466,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const int valid = min(TILE, ts.seg.t_end - ts.t0);
       const int bad = sm.bad[stg];
       const uint32_t k8 = sbase + (uint32_t)stg * SH::kStageBytes, v8 = k8 + TILE * kRowBytes;
-      const uint32_t k16 = sF16 + (uint32_t)bi * 2u * SH::kF16Bytes, v16 = k16 + SH::kF16Bytes;
-      // K of tile j into f16 once S of tile j - 2 (the last reader of this
+      const uint32_t k16 = sK16, v16 = sV16 + (uint32_t)bi * SH::kF16Bytes;
+      // K of tile j into f16 once S of tile j - 1 (the last reader of the
       // buffer) is done; V once P V of tile j - 2 is done
-      if (j >= 2 && !wait_or_abort(sm, p, &sm.s_full[bi], (uint32_t)(((j >> 1) & 1) ^ 1), 4)) break;
+      if (j >= 1 && !ts.first() &&
+          !wait_or_abort(sm, p, &sm.s_full[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), 4))
+        break;
 #pragma unroll 2
       for (int u = 0; u < TILE / 16; ++u) {
         const int qi = ct + 128 * u;
@@ -528,7 +534,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             mbar_test(&sm.s_free[js & 1], (uint32_t)(((js >> 1) & 1) ^ 1))) {
           TC_STAMP(1, js);
           tc_fence_after();
-          const uint32_t kb16 = sF16 + (uint32_t)(js & 1) * 2u * SH::kF16Bytes;
+          const uint32_t kb16 = sK16;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t offq = (uint32_t)(ks >> 2) * M * 128u + (uint32_t)(ks & 3) * 32u;
@@ -545,16 +551,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         if (jp < js) {
           const bool first = b.first();
           if ((!first || kb < 0 || mbar_test(&sm.o_free, (uint32_t)(kb & 1))) &&
-              mbar_test(&sm.p_full, (uint32_t)(jp & 1)) &&
+              mbar_test(&sm.p_full[jp & 1], (uint32_t)((jp >> 1) & 1)) &&
               mbar_test(&sm.v_full[jp & 1], (uint32_t)((jp >> 1) & 1))) {
             if (first) ++kb;
             TC_STAMP(8, jp);
             tc_fence_after();
-            const uint32_t vb16 = sF16 + (uint32_t)(jp & 1) * 2u * SH::kF16Bytes + SH::kF16Bytes;
+            const uint32_t vb16 = sV16 + (uint32_t)(jp & 1) * SH::kF16Bytes;
 #pragma unroll
             for (int ks = 0; ks < TILE / 16; ++ks)
               umma(tO,
-                   sdesc(sP + (uint32_t)(ks >> 2) * M * 128u + (uint32_t)(ks & 3) * 32u, 0, 1024),
+                   sdesc(sP + (uint32_t)(jp & 1) * SH::kPBytes + (uint32_t)(ks >> 2) * M * 128u +
+                             (uint32_t)(ks & 3) * 32u,
+                         0, 1024),
                    sdesc(vb16 + (uint32_t)ks * 2048u, TILE * 128u, 1024), id_o, !(first && ks == 0));
             umma_commit(&sm.done[jp & 1]);
             TC_STAMP(9, jp);
@@ -637,23 +645,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       int lim = *(volatile int*)&sm.fbad[j & 3] ? 0 : min(TILE, seg.t_end - ts.t0);
       if constexpr (CAUSAL) lim = min(lim, seg.T - cut - ts.t0);
       lim -= colbase;
-      // row maximum of sc * s over the valid keys (sc may be negative)
-      float mx[2] = {-INFINITY, -INFINITY}, mn[2] = {INFINITY, INFINITY};
-      if (lim >= kCols) {
+      // row maximum of sc * s over the valid keys (sc may be negative: then
+      // the minimum of s)
+      float mt;
+      {
+        const float sg = sc >= 0.f ? 1.f : -1.f;
+        float mx[2] = {-INFINITY, -INFINITY};
+        if (lim >= kCols) {
 #pragma unroll
-        for (int i = 0; i < kCols; ++i) {
-          mx[i & 1] = fmaxf(mx[i & 1], s[i]);
-          mn[i & 1] = fminf(mn[i & 1], s[i]);
-        }
-      } else {
+          for (int i = 0; i < kCols; ++i) mx[i & 1] = fmaxf(mx[i & 1], sg * s[i]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < kCols; ++i) {
-          mx[i & 1] = fmaxf(mx[i & 1], i < lim ? s[i] : -INFINITY);
-          mn[i & 1] = fminf(mn[i & 1], i < lim ? s[i] : INFINITY);
+          for (int i = 0; i < kCols; ++i) mx[i & 1] = fmaxf(mx[i & 1], i < lim ? sg * s[i] : -INFINITY);
         }
+        const float smax = fmaxf(mx[0], mx[1]);
+        mt = smax == -INFINITY ? -INFINITY : smax * fabsf(sc);
       }
-      const float smax = fmaxf(mx[0], mx[1]), smin = fminf(mn[0], mn[1]);
-      float mt = lim <= 0 ? -INFINITY : (sc >= 0.f ? smax * sc : smin * sc);
       if constexpr (M == 64) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
       float fac = 1.f;
       bool resc = false;
@@ -675,23 +682,34 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
       const bool live = m_ref != -INFINITY;
       const float nm = live ? -m_ref : 0.f;
+      if (live && lim >= kCols) {
 #pragma unroll
-      for (int i = 0; i < kCols; i += 2) {
-        float p0 = fast_exp2(fmaf(s[i], sc, nm)), p1 = fast_exp2(fmaf(s[i + 1], sc, nm));
-        if (!live || i >= lim) p0 = 0.f;
-        if (!live || i + 1 >= lim) p1 = 0.f;
-        ps[(i >> 1) & 3] += p0 + p1;
-        pk[i / 2] = pack_half2(p0, p1);
+        for (int i = 0; i < kCols; i += 2) {
+          const float p0 = fast_exp2(fmaf(s[i], sc, nm)), p1 = fast_exp2(fmaf(s[i + 1], sc, nm));
+          ps[(i >> 1) & 3] += p0 + p1;
+          pk[i / 2] = pack_half2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kCols; i += 2) {
+          float p0 = fast_exp2(fmaf(s[i], sc, nm)), p1 = fast_exp2(fmaf(s[i + 1], sc, nm));
+          if (!live || i >= lim) p0 = 0.f;
+          if (!live || i + 1 >= lim) p1 = 0.f;
+          ps[(i >> 1) & 3] += p0 + p1;
+          pk[i / 2] = pack_half2(p0, p1);
+        }
       }
       float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
       if constexpr (M == 64) psum += __shfl_xor_sync(0xffffffffu, psum, 16);
       l += psum;
       if (warp == 0 && lane == 0) TC_STAMP(5, j);
-      // O and the P buffer are settled once P V of tile j - 1 is done
-      if (j > 0 &&
-          !wait_or_abort(sm, p, &sm.done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), 13))
+      // this P buffer is free once P V of tile j - 2 is done
+      if (j > 1 && !wait_or_abort(sm, p, &sm.done[j & 1], (uint32_t)(((j >> 1) & 1) ^ 1), 13))
         break;
       if (__any_sync(0xffffffffu, resc)) {
+        // O holds P V of tile j - 1 before it is rescaled
+        if (!wait_or_abort(sm, p, &sm.done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), 14))
+          break;
         tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < (M == 128 ? 128 : 64); c0 += 32) {
@@ -707,13 +725,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // this thread's scores are the K-block `half` of row `row` of P
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        sts128(sP + kmajor_chunk(M, row, 8 * half + c),
+        sts128(sP + (uint32_t)(j & 1) * SH::kPBytes + kmajor_chunk(M, row, 8 * half + c),
                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
       if (warp == 0 && lane == 0) TC_STAMP(6, j);
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full);
+      if (lane == 0) mbar_arrive(&sm.p_full[j & 1]);
       if (warp == 0 && lane == 0) TC_STAMP(7, j);
       if (last) {
         // the segment's output: O after P V of this tile
