@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma", "tc"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma", "tc", "fma"])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -303,7 +303,8 @@ class ClockSampler:
 # arithmetic of each split kernel, for the dtype label
 TENSOR_LABEL = {"mma": "mma", "tc": "tcgen05"}
 
-KERNEL_SOURCES = {"tc": ("fd_common.cuh", "fd_split_mma.cuh", "fd_split_tc.cu"),
+KERNEL_SOURCES = {"fma": ("fd_common.cuh", "fd_split_mma.cuh", "fd_split_fma.cu"),
+                  "tc": ("fd_common.cuh", "fd_split_mma.cuh", "fd_split_tc.cu"),
                   "mma": ("fd_common.cuh", "fd_split_mma.cuh", "fd_split_mma.cu",
                           "fd_split_mma_e4m3.cu", "fd_split_mma_i8.cu",
                           "fd_split_mma_16bit.cu"),
@@ -495,7 +496,7 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     fda.load_library()
-    fda.fd_set_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3}[args.kernel])
+    fda.fd_set_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3, "fma": 4}[args.kernel])
 
     w = make_workload(args)
     t = fw.to_torch(w, dev)
@@ -507,7 +508,7 @@ def run_gpu(args):
     sel = fda.fd_selected_kernel(QH * w.q_len, KVH, D, 0 if w.q_dtype == "f16" else 1,
                                  fda.DTYPE_CODES[w.kv_dtype], w.paged,
                                  max(w.page_size, 1))
-    kname = {1: "simt", 2: "mma", 3: "tc"}.get(sel, "none")
+    kname = {1: "simt", 2: "mma", 3: "tc", 4: "fma"}.get(sel, "none")
 
     if args.append:
         k_new, v_new = fw.new_tokens(w, 500 + args.config, n_new=w.q_len)

@@ -44,6 +44,7 @@ FD_KERNEL_AUTO = 0
 FD_KERNEL_SIMT = 1
 FD_KERNEL_MMA = 2
 FD_KERNEL_TC = 3
+FD_KERNEL_FMA = 4
 
 FD_SCALE_TENSOR = 0
 FD_SCALE_HEAD = 1

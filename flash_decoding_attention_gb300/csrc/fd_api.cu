@@ -28,6 +28,9 @@ bool mma_supports(int group, int num_kv_heads, int head_dim, int q_dtype, int kv
                   int paged, int page_size);
 void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms, int* hc,
                 int* tile, int* grid, int* seg_units);
+// CUDA-core form of the mma.sync kernel (fd_split_fma.cu, fd_split_mma.cu)
+bool fma_supports(int group, int num_kv_heads, int head_dim, int kv_dtype, int paged,
+                  int page_size, bool token_scales);
 // tcgen05 kernel (fd_split_tc.cu)
 bool tc_supports(int group, int head_dim, int q_dtype, int kv_dtype, int paged, int page_size,
                  bool token_scales);
@@ -93,6 +96,17 @@ bool choose(int pref, int num_q_heads, int num_kv_heads, int head_dim, int q_dty
     tc_config(group, sms, &c->hc, &c->tile, &c->grid, &c->seg_units);
     c->hg = num_kv_heads;
     c->hq = group;
+    return true;
+  }
+  if (pref == FD_KERNEL_FMA) {
+    // the mma.sync kernel's plan shape, CUDA-core arithmetic
+    if (!fma_supports(group, num_kv_heads, head_dim, kv_dtype, paged, page_size, token_scales))
+      return false;
+    c->kernel = FD_KERNEL_FMA;
+    mma_config(group, num_kv_heads, head_dim, kv_dtype, sms, &c->hc, &c->tile, &c->grid,
+               &c->seg_units);
+    c->hg = num_kv_heads / c->hc;
+    c->hq = c->hc * group;
     return true;
   }
   const bool mma_ok = mma_supports(group, num_kv_heads, head_dim, q_dtype, kv_dtype, paged, page_size);
@@ -281,7 +295,7 @@ const char* fd_status_string(fd_status status) {
 
 fd_status fd_set_kernel(fd_kernel kernel) {
   if (kernel != FD_KERNEL_AUTO && kernel != FD_KERNEL_SIMT && kernel != FD_KERNEL_MMA &&
-      kernel != FD_KERNEL_TC)
+      kernel != FD_KERNEL_TC && kernel != FD_KERNEL_FMA)
     return FD_ERR_INVALID_ARG;
   g_kernel.store(kernel);
   return FD_OK;
@@ -315,7 +329,7 @@ size_t fd_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head
   // Largest layout over every kernel and dtype choice for these sizes.
   const int dts[6][2] = {{FD_F16, FD_F16}, {FD_BF16, FD_BF16}, {FD_F16, FD_E4M3},
                          {FD_BF16, FD_E4M3}, {FD_F16, FD_I8}, {FD_BF16, FD_I8}};
-  for (int pref : {FD_KERNEL_SIMT, FD_KERNEL_MMA, FD_KERNEL_TC}) {
+  for (int pref : {FD_KERNEL_SIMT, FD_KERNEL_MMA, FD_KERNEL_TC, FD_KERNEL_FMA}) {
     for (auto& dt : dts) {
       for (int paged : {0, 1}) {
         Config c;

@@ -194,8 +194,39 @@ void mma_config(int group, int num_kv_heads, int head_dim, int kv_dtype, int sms
   *seg_units = (s.wph > 1 ? 2 : 1) * ((131072 + stage - 1) / stage);
 }
 
+bool fma_supports(int group, int num_kv_heads, int head_dim, int kv_dtype, int paged,
+                  int page_size, bool token_scales) {
+  if (kv_dtype != FD_E4M3 || head_dim != 128 || group < 1 || group > 8 || token_scales)
+    return false;
+  if (paged && (page_size < 1 || page_size > 256)) return false;
+  Shape s;
+  if (!fma_shape(group, num_kv_heads, paged ? page_size : 0, &s)) return false;
+  return encode_fn() != nullptr;
+}
+
 cudaError_t launch_split_mma(const Params& p, cudaStream_t stream) {
   if (p.kv_rows >= (1ll << 31)) return cudaErrorInvalidValue;
+  if (p.kernel == FD_KERNEL_FMA) {
+    Shape sh;
+    if (!fma_shape(p.group, p.num_kv_heads, p.block_table ? p.page_size : 0, &sh) ||
+        sh.tile != p.tile || sh.hc != p.hc)
+      return cudaErrorInvalidValue;
+    Maps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (sh.box_rows == sh.tile &&
+        get_map(p.k, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
+                sh.hc, &maps.k) &&
+        get_map(p.v, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows, sh.row_bytes,
+                sh.hc, &maps.v)) {
+      sh.heads_box = 1;
+    } else if (!get_map(p.k, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows,
+                        sh.row_bytes, 0, &maps.k) ||
+               !get_map(p.v, p.kv_rows, p.num_kv_heads, p.head_dim, p.kv_dtype, sh.box_rows,
+                        sh.row_bytes, 0, &maps.v)) {
+      return cudaErrorInvalidValue;
+    }
+    return launch_fma(p, sh, maps, stream);
+  }
   if (p.kernel == FD_KERNEL_TC) {
     // one KV head per box, 64-token tiles (or the page's rows)
     const int box_rows = p.block_table && p.page_size < p.tile ? p.page_size : p.tile;

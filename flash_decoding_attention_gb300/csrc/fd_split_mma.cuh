@@ -1523,6 +1523,9 @@ cudaError_t launch_8bit(const Params& p, const Shape& sh, const Maps& m, cudaStr
 cudaError_t launch_e4m3(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st);
 cudaError_t launch_i8(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st);
 cudaError_t launch_16bit(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st);
+// The CUDA-core form (fd_split_fma.cu): its shape for a group, and its launch.
+bool fma_shape(int group, int num_kv_heads, int page_size, Shape* out);
+cudaError_t launch_fma(const Params& p, const Shape& sh, const Maps& m, cudaStream_t st);
 #ifdef FD_STAMPS
 cudaError_t read_stamps_e4m3(unsigned long long* host, int n);
 #endif

@@ -90,11 +90,16 @@ typedef enum {
   FD_KERNEL_SIMT = 1,  /* CUDA-core FMA kernel (every supported shape) */
   FD_KERNEL_MMA = 2,   /* tensor-core kernel with warp-level mma.sync products, operands
                           widened in registers; FD_ERR_UNSUPPORTED where it does not apply */
-  FD_KERNEL_TC = 3     /* tensor-core kernel with tcgen05 products (accumulators in tensor
+  FD_KERNEL_TC = 3,    /* tensor-core kernel with tcgen05 products (accumulators in tensor
                           memory, FP8 widened once per tile into shared memory): e4m3
                           caches, fp16 queries, head_dim 128, 17..128 query rows per KV
                           head (query heads per KV head times q_len), no per-token scales,
                           page sizes 8..256; FD_ERR_UNSUPPORTED elsewhere */
+  FD_KERNEL_FMA = 4    /* the mma.sync kernel's TMA pipeline, plan and shapes with CUDA-core
+                          FMA arithmetic instead of tensor cores (the comparison arm): e4m3
+                          caches, head_dim 128, at most 8 query rows per KV head, KV heads a
+                          multiple of 8, no per-token scales, page sizes of at least 8;
+                          FD_ERR_UNSUPPORTED elsewhere; never chosen by FD_KERNEL_AUTO */
 } fd_kernel;
 
 /*
@@ -333,7 +338,7 @@ fd_status fd_set_kernel(fd_kernel kernel);
 
 /*
  * Kernel that fd_decode_attention would run for these sizes under the
- * current fd_set_kernel choice: FD_KERNEL_SIMT, FD_KERNEL_MMA or FD_KERNEL_TC,
+ * current fd_set_kernel choice: FD_KERNEL_SIMT, FD_KERNEL_MMA, FD_KERNEL_TC or FD_KERNEL_FMA,
  * or -1 if the sizes are unsupported (num_q_heads counts every query token:
  * query heads times q_len).  Host function.
  */

@@ -103,11 +103,14 @@ def host_shape(kernel: int, num_q_heads: int, num_kv_heads: int, head_dim: int, 
     a head tile merge at every segment end); grid = one CTA per SM.
     kernel 1 (CUDA cores): streams of min(group, 16) query heads of one KV
     head, 32-token tiles, one CTA per SM, no start cost.
+    kernel 4 (CUDA-core FMA form of kernel 2): kernel 2's shape.
     kernel 3 (tcgen05): a stream is one KV head with all its query rows;
     128-token tiles for groups of up to 64 rows, else 64-token tiles; one CTA
     per SM; a segment start costs ceil(128 KiB / stage bytes) tiles.
     """
     group = num_q_heads * q_len // num_kv_heads
+    if kernel == 4:   # the CUDA-core form of kernel 2: the same plan shape
+        kernel = 2
     if kernel == 3:
         tile = 128 if group <= 64 else 64
         return num_kv_heads, tile, sms, -(-131072 // (2 * tile * head_dim * kv_elem))

@@ -39,14 +39,17 @@ def _takes(kernel, w):
     """Whether a forced kernel takes a plan case: the CUDA-core and mma.sync
     kernels take every case here; the tcgen05 kernel takes e4m3 caches with
     fp16 queries, head_dim 128 and 17..128 query rows per KV head."""
+    rows = w.num_q_heads * w.q_len // w.num_kv_heads
+    if kernel == 4:   # FMA form: e4m3, head_dim 128, <= 8 rows, 8 KV heads per stream
+        return (w.kv_dtype == "e4m3" and w.head_dim == 128 and rows <= 8
+                and w.num_kv_heads % 8 == 0 and (not w.paged or w.page_size >= 8))
     if kernel != 3:
         return True
-    rows = w.num_q_heads * w.q_len // w.num_kv_heads
     return (w.kv_dtype == "e4m3" and w.q_dtype == "f16" and w.head_dim == 128
             and 16 < rows <= 128 and (not w.paged or 8 <= w.page_size <= 256))
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("case", range(10))
 def test_device_plan_matches_restatement(kernel, case):
     fda = lib()
@@ -70,7 +73,7 @@ def test_device_plan_matches_restatement(kernel, case):
     group = w.num_q_heads // w.num_kv_heads
     assert hq % group == 0 or group % hq == 0      # a stream never splits a KV head's reads
     assert S == w.batch * hg
-    assert seg_units >= 0 and (kernel in (2, 3) or seg_units == 0)
+    assert seg_units >= 0 and (kernel in (2, 3, 4) or seg_units == 0)
     # the host's choice of shape, restated
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     elem = 1 if w.kv_dtype in ("e4m3", "i8") else 2
@@ -81,7 +84,7 @@ def test_device_plan_matches_restatement(kernel, case):
     assert (total, per_cta) == (p_total, p_per_cta)
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("case", range(10))
 def test_device_segments_match_restatement(kernel, case):
     """Every CTA's segments (stream, token range, complete, partial slot), as
