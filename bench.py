@@ -422,13 +422,20 @@ def pct(xs, q):
 # Workloads timed next to the headline one (same protocol): the other
 # configurations, and the per-token-scale, INT8 and verify-step variants of
 # the headline workloads.  name -> (config, kv format, scale kind, q_len)
+# name: (workload, KV dtype, scale kind, query tokens, split kernel: 0 = the
+# library's own choice, else an fd_kernel value timed for comparison)
 PER_CONFIG = {
-    "config1": (1, "e4m3", "tensor", 1), "config2": (2, "e4m3", "tensor", 1),
-    "config3": (3, "e4m3", "tensor", 1), "config4": (4, "e4m3", "tensor", 1),
-    "config5": (5, "e4m3", "tensor", 1),
-    "config4_token_scales": (4, "e4m3", "token", 1), "config4_int8": (4, "i8", "tensor", 1),
-    "config5_q_len4": (5, "e4m3", "tensor", 4),
+    "config1": (1, "e4m3", "tensor", 1, 0), "config2": (2, "e4m3", "tensor", 1, 0),
+    "config3": (3, "e4m3", "tensor", 1, 0), "config4": (4, "e4m3", "tensor", 1, 0),
+    "config5": (5, "e4m3", "tensor", 1, 0),
+    "config4_token_scales": (4, "e4m3", "token", 1, 0), "config4_int8": (4, "i8", "tensor", 1, 0),
+    "config5_q_len4": (5, "e4m3", "tensor", 4, 0),
+    # the same steps on other split kernels: mma.sync for the 4-token MQA step
+    # (the library takes tcgen05 there), CUDA-core FMAs for the FP8 paged one
+    "config5_q_len4_mma_sync": (5, "e4m3", "tensor", 4, 2),
+    "config4_cuda_core_fma": (4, "e4m3", "tensor", 1, 4),
 }
+KERNEL_IDS = {1: "simt", 2: "mma", 3: "tc", 4: "fma"}
 
 
 def per_config_timings(args, dev, stream, flush, peak, kernel_name):
@@ -439,8 +446,8 @@ def per_config_timings(args, dev, stream, flush, peak, kernel_name):
     import flash_decoding_attention_gb300 as fda
     K = max(100, min(args.steps, 400))
     res = {}
-    for name, (cfg, kv, scales, q_len) in PER_CONFIG.items():
-        if (cfg, kv, scales, q_len) == (args.config, args.kv, args.scales, args.q_len):
+    for name, (cfg, kv, scales, q_len, kern) in PER_CONFIG.items():
+        if (cfg, kv, scales, q_len, kern) == (args.config, args.kv, args.scales, args.q_len, 0):
             continue
         a = argparse.Namespace(**vars(args))
         a.config, a.kv, a.scales, a.q_len, a.shared_prefix = cfg, kv, scales, q_len, 0
@@ -451,6 +458,11 @@ def per_config_timings(args, dev, stream, flush, peak, kernel_name):
         ws = fda.alloc_workspace(w.batch, w.num_q_heads * w.q_len, w.num_kv_heads, w.head_dim,
                                  dev)
         step = make_step(fda, w, t, out, lse, ws, stream)
+        fda.fd_set_kernel(kern if kern else {"auto": 0, "simt": 1, "mma": 2, "tc": 3,
+                                             "fma": 4}[args.kernel])
+        sel = fda.fd_selected_kernel(w.num_q_heads * w.q_len, w.num_kv_heads, w.head_dim,
+                                     0 if w.q_dtype == "f16" else 1, fda.DTYPE_CODES[w.kv_dtype],
+                                     w.paged, max(w.page_size, 1))
         for _ in range(5):
             flush()
             step()
@@ -462,7 +474,8 @@ def per_config_timings(args, dev, stream, flush, peak, kernel_name):
         alg = w.algorithmic_bytes()
         mean_ms = sum(ms) / K
         e = {"workload": fw.WORKLOAD_NAMES[cfg], "steps": K, "us_per_step": round(mean_ms * 1e3, 2),
-             "us_per_step_p10_p50_p90": [pct(ms, 10), pct(ms, 50), pct(ms, 90)]}
+             "us_per_step_p10_p50_p90": [pct(ms, 10), pct(ms, 50), pct(ms, 90)],
+             "kernel": KERNEL_IDS.get(sel, "none")}
         if kv != "e4m3":
             e["kv_dtype"] = kv
         if scales != "tensor":
@@ -479,6 +492,7 @@ def per_config_timings(args, dev, stream, flush, peak, kernel_name):
                       "frac": round(gbs / peak, 4), "split_us": round(split_ms * 1e3, 2),
                       "split_frac": round(alg / (split_ms * 1e-3) / 1e9 / peak, 4)})
         res[name] = e
+        fda.fd_set_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3, "fma": 4}[args.kernel])
         del t, out, lse, ws
         torch.cuda.empty_cache()
     return res
