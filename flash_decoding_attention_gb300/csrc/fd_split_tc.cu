@@ -230,6 +230,7 @@ struct SharedTC {
   // tile j came from such a stage (converters, slot j mod 4: the converters
   // run at most three tiles ahead of the softmax warps that read it)
   int fbad[4];
+  int tfirst[4];   // tile j (slot j mod 4) starts a segment (converters -> MMA thread)
   int abort_flag;
   uint32_t tmem_base;
   long long red[35];
@@ -482,7 +483,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         sts128(k16 + kmajor_chunk(TILE, t, 2 * c), make_uint4(k0.x, k0.y, k1.x, k1.y));
         sts128(k16 + kmajor_chunk(TILE, t, 2 * c + 1), make_uint4(k2.x, k2.y, k3.x, k3.y));
       }
-      if (ct == 0) sm.fbad[j & 3] = bad;
+      if (ct == 0) {
+        sm.fbad[j & 3] = bad;
+        sm.tfirst[j & 3] = ts.first() ? 1 : 0;
+      }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.k_full[bi]);
@@ -522,51 +526,55 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       constexpr uint32_t id_s = idesc_f16(M, TILE, 0);
       constexpr uint32_t id_o = idesc_f16(M, 128, 1);
       const uint32_t tS = tbase, tO = tbase + 2 * TILE;
-      TileSeq a, b;   // a: S products, b: P V products
-      a.init(p, plan);
-      b.init(p, plan);
+      // the CTA's tile count; whether a tile starts a segment comes from the
+      // converters (slot j mod 4, written before the tile's K is released)
+      int ntiles = 0;
+      {
+        SegmentIter it;
+        it.init(p, plan);
+        Segment sg;
+        while (it.next(p, sg)) ntiles += (sg.t_end - sg.t_begin + TILE - 1) / TILE;
+      }
+      // descriptors: one Q and one K buffer for S; P and V by tile parity.
+      // A descriptor's low field is the address / 16, so an operand offset
+      // inside shared memory (below 256 KB) is added as offset / 16.
+      const uint64_t dq = sdesc(sQ, 0, 1024), dk = sdesc(sK16, 0, 1024);
+      const uint64_t dp = sdesc(sP, 0, 1024), dv = sdesc(sV16, TILE * 128u, 1024);
       int js = 0, jp = 0, kb = -1;
       unsigned long long t_prog = 0;
       uint32_t spins = 0;
-      while (b.have) {
+      while (jp < ntiles) {
         bool prog = false;
-        if (a.have && mbar_test(&sm.k_full[js & 1], (uint32_t)((js >> 1) & 1)) &&
+        if (js < ntiles && mbar_test(&sm.k_full[js & 1], (uint32_t)((js >> 1) & 1)) &&
             mbar_test(&sm.s_free[js & 1], (uint32_t)(((js >> 1) & 1) ^ 1))) {
           TC_STAMP(1, js);
           tc_fence_after();
-          const uint32_t kb16 = sK16;
+          const uint32_t ds = tS + (uint32_t)(js & 1) * TILE;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t offq = (uint32_t)(ks >> 2) * M * 128u + (uint32_t)(ks & 3) * 32u;
-            const uint32_t offk = (uint32_t)(ks >> 2) * TILE * 128u + (uint32_t)(ks & 3) * 32u;
-            umma(tS + (uint32_t)(js & 1) * TILE, sdesc(sQ + offq, 0, 1024),
-                 sdesc(kb16 + offk, 0, 1024), id_s, ks > 0);
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            umma(ds, dq + (((ks >> 2) * M * 128 + (ks & 3) * 32) >> 4),
+                 dk + (((ks >> 2) * TILE * 128 + (ks & 3) * 32) >> 4), id_s, ks > 0);
           umma_commit(&sm.s_full[js & 1]);
           TC_STAMP(2, js);
-          a.next(p, TILE);
           ++js;
           prog = true;
         }
         if (jp < js) {
-          const bool first = b.first();
+          const bool first = *(volatile int*)&sm.tfirst[jp & 3] != 0;
           if ((!first || kb < 0 || mbar_test(&sm.o_free, (uint32_t)(kb & 1))) &&
               mbar_test(&sm.p_full[jp & 1], (uint32_t)((jp >> 1) & 1)) &&
               mbar_test(&sm.v_full[jp & 1], (uint32_t)((jp >> 1) & 1))) {
             if (first) ++kb;
             TC_STAMP(8, jp);
             tc_fence_after();
-            const uint32_t vb16 = sV16 + (uint32_t)(jp & 1) * SH::kF16Bytes;
+            const uint64_t dpj = dp + (((jp & 1) * SH::kPBytes) >> 4);
+            const uint64_t dvj = dv + (((jp & 1) * SH::kF16Bytes) >> 4);
 #pragma unroll
             for (int ks = 0; ks < TILE / 16; ++ks)
-              umma(tO,
-                   sdesc(sP + (uint32_t)(jp & 1) * SH::kPBytes + (uint32_t)(ks >> 2) * M * 128u +
-                             (uint32_t)(ks & 3) * 32u,
-                         0, 1024),
-                   sdesc(vb16 + (uint32_t)ks * 2048u, TILE * 128u, 1024), id_o, !(first && ks == 0));
+              umma(tO, dpj + (((ks >> 2) * M * 128 + (ks & 3) * 32) >> 4), dvj + ((ks * 2048) >> 4),
+                   id_o, !(first && ks == 0));
             umma_commit(&sm.done[jp & 1]);
             TC_STAMP(9, jp);
-            b.next(p, TILE);
             ++jp;
             prog = true;
           }
