@@ -155,8 +155,10 @@ def test_decode_with_append_validates_the_append(fda):
 
 
 def test_set_kernel_rejects_unknown(fda):
-    assert fda.load_library().fd_set_kernel(7) == 1
-    assert fda.load_library().fd_set_kernel(0) == 0
+    lib = fda.load_library()
+    assert lib.fd_set_kernel(7) == 1 and lib.fd_set_kernel(5) == 1 and lib.fd_set_kernel(-1) == 1
+    for k in (1, 2, 3, 4, 0):
+        assert lib.fd_set_kernel(k) == 0
 
 
 def test_header_enums_match_the_binding(fda):
@@ -164,7 +166,8 @@ def test_header_enums_match_the_binding(fda):
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     enums = dict((k, int(v)) for k, v in re.findall(r"\b(FD_[A-Z0-9_]+)\s*=\s*(\d+)", text))
     for name in ("FD_F16", "FD_BF16", "FD_E4M3", "FD_I8", "FD_SCALE_TENSOR", "FD_SCALE_HEAD",
-                 "FD_SCALE_TOKEN", "FD_KERNEL_AUTO", "FD_KERNEL_SIMT", "FD_KERNEL_MMA", "FD_OK",
+                 "FD_SCALE_TOKEN", "FD_KERNEL_AUTO", "FD_KERNEL_SIMT", "FD_KERNEL_MMA",
+                 "FD_KERNEL_TC", "FD_KERNEL_FMA", "FD_OK",
                  "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE_TOO_SMALL",
                  "FD_ERR_CUDA", "FD_ERR_DEVICE_BOUNDS", "FD_ERR_DEVICE_TIMEOUT"):
         assert enums[name] == getattr(fda, name), name
