@@ -49,6 +49,30 @@ def test_starved_pipeline_reports_timeout_then_recovers(case, orc):
     parity(w, out, lse, ref_out, ref_lse, label=w.name)
 
 
+@pytest.mark.parametrize("kernel,qh,kvh,q_len", [(3, 16, 1, 4), (3, 128, 2, 1), (4, 64, 8, 1)])
+def test_starved_pipeline_other_split_kernels(kernel, qh, kvh, q_len, orc):
+    """The same on the tcgen05 kernel (its converter, softmax and MMA-issue
+    waits are bounded alike; whichever runs out first is recorded) and on
+    the CUDA-core FMA form (its consumers' waits)."""
+    fda = lib()
+    w = fw.make_contiguous(f"timeout-k{kernel}-{qh}-{kvh}", 45 + kernel, [3000, 700, 9000], qh, kvh,
+                           128, "f16", "e4m3", q_len=q_len)
+    ws = fda.alloc_workspace(w.batch, w.num_q_heads * q_len, w.num_kv_heads, w.head_dim)
+    try:
+        fda.fd_debug_set_wait_limit(3_000_000, True)      # 3 ms, no copy issued
+        run(w, kernel, workspace=ws, check_errors=False)
+        st, info = fda.fd_check_device_error(ws)
+    finally:
+        fda.fd_debug_set_wait_limit(0, False)
+    assert st == fda.FD_ERR_DEVICE_TIMEOUT, fda.fd_status_string(st)
+    # tcgen05: a converter (6), the MMA thread (7) or a softmax warp (11); FMA form: a consumer
+    assert info in ({6, 7, 11} if kernel == 3 else {2}), info
+    assert fda.fd_check_device_error(ws)[0] == fda.FD_OK
+    out, lse, _, _ = run(w, kernel, workspace=ws)
+    ref_out, ref_lse = orc.decode_attention(w)
+    parity(w, out, lse, ref_out, ref_lse, label=w.name)
+
+
 def test_wait_limit_alone_changes_nothing(orc):
     """A shortened bound that no wait reaches leaves the result exact."""
     fda = lib()
