@@ -340,7 +340,10 @@ fd_status fd_set_kernel(fd_kernel kernel);
  * Kernel that fd_decode_attention would run for these sizes under the
  * current fd_set_kernel choice: FD_KERNEL_SIMT, FD_KERNEL_MMA, FD_KERNEL_TC or FD_KERNEL_FMA,
  * or -1 if the sizes are unsupported (num_q_heads counts every query token:
- * query heads times q_len).  Host function.
+ * query heads times q_len).  The answer is for per-tensor or per-KV-head
+ * scales; with per-token scales (FD_SCALE_TOKEN) FD_KERNEL_AUTO never takes
+ * FD_KERNEL_TC, and a forced FD_KERNEL_TC or FD_KERNEL_FMA call returns
+ * FD_ERR_UNSUPPORTED.  Host function.
  */
 int fd_selected_kernel(int num_q_heads, int num_kv_heads, int head_dim, fd_dtype q_dtype,
                        fd_dtype kv_dtype, int paged, int page_size);
