@@ -15,6 +15,7 @@ pytestmark = pytest.mark.gpu
 
 KERNELS = (0, 1, 2, 3, 4)   # the library's choice, then each kernel forced
 N_CASES = 40
+N_LARGE = 24
 
 
 def _case(i):
@@ -42,10 +43,39 @@ def _case(i):
     return w
 
 
+def _large_group_case(i):
+    """One or two KV heads with 16 to 128 query rows each (query heads times
+    query tokens), FP8-e4m3 or 16-bit caches, longer sequences: the shapes
+    on which the library's own choice can be the tcgen05 kernel."""
+    rng = np.random.default_rng(9500 + i)
+    kvh = int(rng.choice([1, 1, 2]))
+    q_len = int(rng.choice([1, 1, 2, 4, 8]))
+    g = int(rng.choice([g for g in (8, 16, 32, 64, 128) if g * q_len <= 128]))
+    kv = str(rng.choice(["e4m3", "e4m3", "e4m3", "f16"]))
+    qdt = "f16" if kv == "e4m3" and rng.random() < 0.8 else ("f16" if kv == "f16" else "bf16")
+    B = int(rng.integers(1, 6))
+    lens = [int(x) for x in rng.choice([0, 1, 63, 64, 65, 127, 128, 129, 700, 4000, 9000], size=B)]
+    w = fw.make_contiguous(f"fuzz-large-{i}", 9600 + i, lens, kvh * g, kvh, 128, qdt, kv,
+                           gap=int(rng.integers(0, 3)), lead=int(rng.integers(0, 2)), q_len=q_len)
+    if rng.random() < 0.5:
+        w = fw.to_paged(w, int(rng.choice([8, 16, 32, 64, 128, 256])), 9700 + i)
+    if kv == "e4m3" and rng.random() < 0.3:
+        w = fw.with_scales(w, fw.SCALE_HEAD, 9800 + i, span=(0.5, 2.0) if qdt == "f16" else (0.25, 1.0))
+    return w
+
+
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_case_every_kernel(i):
+    _every_kernel(_case(i))
+
+
+@pytest.mark.parametrize("i", range(N_LARGE))
+def test_random_large_group_every_kernel(i):
+    _every_kernel(_large_group_case(i))
+
+
+def _every_kernel(w):
     fda = lib()
-    w = _case(i)
     ref = oracle.decode_attention(w)
     ran = 0
     for k in KERNELS:
