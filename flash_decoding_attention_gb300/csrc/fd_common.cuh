@@ -123,7 +123,7 @@ struct Params {
 // slot i of CTA c in a kernel's stamp array holds %globaltimer (ns) when the
 // CTA passed phase i; fd_debug_read_stamps copies them out.
 #ifdef FD_STAMPS
-constexpr int kStampCtas = 4096, kStampSlots = 32;
+constexpr int kStampCtas = 4096, kStampSlots = 24;
 #define FD_STAMP_ARRAY(name) __device__ unsigned long long name[kStampCtas * kStampSlots]
 #define FD_STAMP(arr, i, v)                                                        \
   do {                                                                             \

@@ -540,10 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // K/V lines are read once: they leave L2 first, before Q rows, index
     // data and partial states
 
-    if (lane == 0) FD_STAMP(g_split_stamps, 24, stamp_ns());
     SegmentIter it;
     it.init(p, plan);
-    if (lane == 0) FD_STAMP(g_split_stamps, 25, stamp_ns());
     Segment seg;
     int n = 0;
     bool stop = p.starve != 0;   // test switch: issue nothing, the consumers' waits run out
@@ -598,10 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int bad = 0;
             uint32_t bytes = 0;
             // pass 1: validate rows, count bytes; pass 2: issue
-            if (n == 0) FD_STAMP(g_split_stamps, 26, stamp_ns());
             for (int pass = 0; pass < 2; ++pass) {
               if (pass == 1) {
-                if (n == 0) FD_STAMP(g_split_stamps, 27, stamp_ns());
                 sm.bad[stg] = bad;
                 mbar_arrive_tx(&sm.full[stg], bytes);
               }
