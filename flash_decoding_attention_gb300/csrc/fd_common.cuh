@@ -8,6 +8,8 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "fd_attention.h"
 
 namespace fd {
@@ -450,6 +452,23 @@ inline cudaError_t launch_split(const Params& p, Kernel kern, dim3 grid, dim3 bl
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device: the limit belongs to the function on each device,
+// so a process driving several GPUs sets it on each.  `done` holds one bit per
+// device ordinal below 64 (higher ordinals set the limit on every call).
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kern, int bytes,
+                                     std::atomic<unsigned long long>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done->load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done->fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 // Host-side argument checks shared by the decode entry points (fd_api.cu).

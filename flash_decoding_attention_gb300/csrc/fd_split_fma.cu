@@ -392,7 +392,8 @@ template <typename QT>
 cudaError_t launch_q(const Params& p, const Shape& sh, const Maps& m, cudaStream_t stream) {
   auto kern = fma_split_kernel<QT>;
   const int smem = sh.smem_bytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<unsigned long long> limit_set{0};
+  cudaError_t e = ensure_smem_limit(kern, kSmemBudget, &limit_set);
   if (e != cudaSuccess) return e;
   return launch_split(p, kern, dim3(p.grid), dim3(kThreads), smem, stream, p, sh, m.k, m.v);
 }

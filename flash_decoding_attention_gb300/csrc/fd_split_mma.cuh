@@ -1472,13 +1472,9 @@ template <int KVT, typename QT, int D, bool TOK, int QROWS = 16, bool CAUSAL = f
           bool FLIP = false>
 cudaError_t launch_t(const Params& p, const Shape& sh, const Maps& m, cudaStream_t stream) {
   auto kern = mma_split_kernel<KVT, QT, D, TOK, QROWS, CAUSAL, FLIP>;
-  static int configured = 0;
-  if (configured < sh.smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBudget);
-    if (e != cudaSuccess) return e;
-    configured = kSmemBudget;
-  }
+  static std::atomic<unsigned long long> limit_set{0};
+  cudaError_t e = ensure_smem_limit(kern, kSmemBudget, &limit_set);
+  if (e != cudaSuccess) return e;
   return launch_split(p, kern, dim3(p.grid), dim3(kThreads), sh.smem_bytes, stream, p, sh, m.k,
                       m.v, m.ks, m.vs);
 }

@@ -223,14 +223,11 @@ template <int KVT, typename QT, int D>
 cudaError_t launch_t(const Params& p, cudaStream_t stream) {
   auto kern = simt_split_kernel<KVT, QT, D>;
   const size_t smem = sizeof(float) * (2 * kSimtWarps * p.hq + kSimtWarps * p.hq * D);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(float) * (2 * kSimtWarps * kSimtMaxGroup +
-                                                                kSimtWarps * kSimtMaxGroup * D)));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> limit_set{0};
+  cudaError_t e = ensure_smem_limit(
+      kern, (int)(sizeof(float) * (2 * kSimtWarps * kSimtMaxGroup + kSimtWarps * kSimtMaxGroup * D)),
+      &limit_set);
+  if (e != cudaSuccess) return e;
   return launch_split(p, kern, dim3(p.grid), dim3(kSimtThreads), smem, stream, p);
 }
 

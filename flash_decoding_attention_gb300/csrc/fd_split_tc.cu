@@ -801,8 +801,8 @@ template <int M, bool CAUSAL>
 cudaError_t launch_m(const Params& p, const CUtensorMap& mk, const CUtensorMap& mv,
                      cudaStream_t stream) {
   constexpr uint32_t smem = TcShape<M>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(tc_split_kernel<M, CAUSAL>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<unsigned long long> limit_set{0};
+  cudaError_t e = ensure_smem_limit(tc_split_kernel<M, CAUSAL>, (int)smem, &limit_set);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid);
