@@ -50,6 +50,14 @@
  * the caller must keep between calls except the sticky device-error word
  * read by fd_check_device_error.  Calls that share one workspace must be
  * ordered on one stream.
+ *
+ * Devices and host threads: calls run on the CUDA device current in the
+ * calling thread, and several devices may be used from one process.  The
+ * library keeps, per device, the SM count and whether each kernel's
+ * shared-memory limit has been raised, and per process a small cache of TMA
+ * descriptors keyed by cache pointer and shape; all of these are guarded for
+ * concurrent calls from several host threads.  They are kept for the life of
+ * the process: do not use the library on a device after cudaDeviceReset.
  */
 #ifndef FD_ATTENTION_H_
 #define FD_ATTENTION_H_
