@@ -356,6 +356,15 @@ __device__ __forceinline__ uint2 widen8x4(uint32_t w) {
   }
 }
 
+// Four int8 codes -> two registers of f16 pairs holding code + 1152 (the
+// sign flip and byte permutation of widen8x4 without its subtraction).  The
+// FLIP form feeds V this way and takes 1152 times the sub-tile's probability
+// sums back out of the O^T accumulator after the sub-tile's products.
+__device__ __forceinline__ uint2 widen_i8x4_biased(uint32_t w) {
+  const uint32_t u = w ^ 0x80808080u;
+  return make_uint2(__byte_perm(u, 0x64u, 0x4140), __byte_perm(u, 0x64u, 0x4342));
+}
+
 // FLIP form, head_dim 128: head dim of row r of the O^T accumulator's
 // m-tile j (row r + 8 is the next dim).  8-bit caches: 16 r + 2 j (a lane's
 // V bytes are one 16-byte chunk); 16-bit caches: 64 (j / 4) + 8 r + 2 (j % 4)
@@ -996,12 +1005,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               //      flip_dim(j, r) and flip_dim(j, r) + 1, so this lane's V
               //      values are one 16-byte chunk of each of its four token
               //      rows (per 128-byte region).
+              // INT8 cache, f16 queries: V enters the products as code + 1152
+              // (no subtraction per element); an all-ones row of A sums the
+              // packed probabilities of the sub-tile per head in lanes 0..3,
+              // and 1152 times that sum leaves O^T after the sub-tile.
+              constexpr bool VFOLD = KVT == FD_I8 && !BF16 && ELEM == 1;
+              float psum[4] = {0.f, 0.f, 0.f, 0.f};
+              const uint32_t ones = r == 0 ? 0x3C003C00u : 0u;   // row 0 of A: 1.0
 #pragma unroll
               for (int kt = 0; kt < MT; ++kt) {
                 const uint32_t pb0 =
                     movmatrix_trans(pack_f32x2(st[kt][0], st[kt][1], BF16));   // token r
                 const uint32_t pb1 =
                     movmatrix_trans(pack_f32x2(st[kt][2], st[kt][3], BF16));   // token r + 8
+                if constexpr (VFOLD) mma16816<false>(psum, ones, 0u, ones, 0u, pb0, pb1);
                 const int u0 = sub + 16 * kt + 2 * q, u1 = u0 + 1, u2 = u0 + 8, u3 = u0 + 9;
 #pragma unroll
                 for (int x2 = 0; x2 < (ELEM == 1 ? 1 : D / 64); ++x2) {
@@ -1020,8 +1037,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const uint32_t hi01 = __byte_perm(A[wd], B[wd], 0x7362);
                       const uint32_t lo89 = __byte_perm(C[wd], E[wd], 0x5140);
                       const uint32_t hi89 = __byte_perm(C[wd], E[wd], 0x7362);
-                      const uint2 l01 = widen8x4<KVT, BF16>(lo01), l89 = widen8x4<KVT, BF16>(lo89);
-                      const uint2 h01 = widen8x4<KVT, BF16>(hi01), h89 = widen8x4<KVT, BF16>(hi89);
+                      uint2 l01, l89, h01, h89;
+                      if constexpr (VFOLD) {
+                        l01 = widen_i8x4_biased(lo01);
+                        l89 = widen_i8x4_biased(lo89);
+                        h01 = widen_i8x4_biased(hi01);
+                        h89 = widen_i8x4_biased(hi89);
+                      } else {
+                        l01 = widen8x4<KVT, BF16>(lo01);
+                        l89 = widen8x4<KVT, BF16>(lo89);
+                        h01 = widen8x4<KVT, BF16>(hi01);
+                        h89 = widen8x4<KVT, BF16>(hi89);
+                      }
                       mma16816<BF16>(o[2 * wd], l01.x, l01.y, l89.x, l89.y, pb0, pb1);
                       mma16816<BF16>(o[2 * wd + 1], h01.x, h01.y, h89.x, h89.y, pb0, pb1);
                     } else {   // two head dims per word
@@ -1031,6 +1058,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      __byte_perm(C[wd], E[wd], 0x7632), pb0, pb1);
                     }
                   }
+                }
+              }
+              if constexpr (VFOLD) {
+                // heads 2q and 2q + 1: row 0 of the sums, held by lane q
+                const float s0 = __shfl_sync(0xffffffffu, psum[0], q);
+                const float s1 = __shfl_sync(0xffffffffu, psum[1], q);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  o[j][0] = fmaf(-1152.f, s0, o[j][0]);
+                  o[j][1] = fmaf(-1152.f, s1, o[j][1]);
+                  o[j][2] = fmaf(-1152.f, s0, o[j][2]);
+                  o[j][3] = fmaf(-1152.f, s1, o[j][3]);
                 }
               }
             } else {
