@@ -902,14 +902,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                   w[jn][0] = a0.x; w[jn][1] = a0.y; w[jn][2] = a0.z; w[jn][3] = a0.w;
                   w[jn][4] = a1.x; w[jn][5] = a1.y; w[jn][6] = a1.z; w[jn][7] = a1.w;
                 }
+                // INT8 cache, f16 queries: K enters as code + 1152, and after
+                // each 16-dim k-step a second product with A = -1152 takes
+                // that k-step's bias (1152 times the head's Q sum over those
+                // dims) back out, so the accumulator never holds more than
+                // one k-step's bias
+                constexpr bool KFOLD = KVT == FD_I8 && !BF16;
+                constexpr uint32_t kNeg1152 = 0xE480E480u;   // f16 pair (-1152, -1152)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                   const uint2 qb = lds64(qf + kk * 256);
 #pragma unroll
                   for (int mt = 0; mt < MT; ++mt) {
-                    const uint2 ka = widen8x4<KVT, BF16>(w[2 * mt][kk]);       // token r
-                    const uint2 kb = widen8x4<KVT, BF16>(w[2 * mt + 1][kk]);   // token r + 8
-                    mma16816<BF16>(st[mt], ka.x, kb.x, ka.y, kb.y, qb.x, qb.y);
+                    if constexpr (KFOLD) {
+                      const uint2 ka = widen_i8x4_biased(w[2 * mt][kk]);       // token r
+                      const uint2 kb = widen_i8x4_biased(w[2 * mt + 1][kk]);   // token r + 8
+                      mma16816<false>(st[mt], ka.x, kb.x, ka.y, kb.y, qb.x, qb.y);
+                      mma16816<false>(st[mt], kNeg1152, kNeg1152, kNeg1152, kNeg1152, qb.x, qb.y);
+                    } else {
+                      const uint2 ka = widen8x4<KVT, BF16>(w[2 * mt][kk]);       // token r
+                      const uint2 kb = widen8x4<KVT, BF16>(w[2 * mt + 1][kk]);   // token r + 8
+                      mma16816<BF16>(st[mt], ka.x, kb.x, ka.y, kb.y, qb.x, qb.y);
+                    }
                   }
                 }
               } else {   // 16-bit: chunk pairs (2q, 2q + 1) of each 128-byte region
