@@ -358,8 +358,9 @@ __device__ __forceinline__ uint2 widen8x4(uint32_t w) {
 
 // Four int8 codes -> two registers of f16 pairs holding code + 1152 (the
 // sign flip and byte permutation of widen8x4 without its subtraction).  The
-// FLIP form feeds V this way and takes 1152 times the sub-tile's probability
-// sums back out of the O^T accumulator after the sub-tile's products.
+// FLIP form with f16 queries feeds K and V this way: a second product per
+// 16-dim k-step takes K's bias back out of the scores, and 1152 times the
+// sub-tile's probability sums leave the O^T accumulator after its products.
 __device__ __forceinline__ uint2 widen_i8x4_biased(uint32_t w) {
   const uint32_t u = w ^ 0x80808080u;
   return make_uint2(__byte_perm(u, 0x64u, 0x4140), __byte_perm(u, 0x64u, 0x4342));
