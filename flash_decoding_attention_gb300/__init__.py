@@ -52,7 +52,8 @@ FD_SCALE_TOKEN = 2
 
 EXPORTED = [
     "fd_workspace_bytes", "fd_decode_attention", "fd_check_device_error", "fd_status_string",
-    "fd_set_kernel", "fd_selected_kernel", "fd_set_split_events", "fd_debug_read_plan",
+    "fd_set_kernel", "fd_selected_kernel", "fd_selected_kernel_scaled", "fd_set_split_events",
+    "fd_debug_read_plan",
     "fd_debug_gather_kv", "fd_decode_attention_noalloc", "fd_decode_attention_scaled",
     "fd_append_kv", "fd_decode_attention_append", "fd_decode_attention_multi",
     "fd_debug_set_wait_limit", "fd_debug_plan_segments",
@@ -114,6 +115,8 @@ def load_library(path: Optional[str] = None):
         lib.fd_set_kernel.argtypes = [i32]
         lib.fd_selected_kernel.restype = i32
         lib.fd_selected_kernel.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        lib.fd_selected_kernel_scaled.restype = i32
+        lib.fd_selected_kernel_scaled.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
         lib.fd_set_split_events.restype = i32
         lib.fd_set_split_events.argtypes = [vp, vp]
         lib.fd_debug_read_plan.restype = i32
@@ -351,6 +354,13 @@ def fd_selected_kernel(num_q_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, p
                        page_size) -> int:
     return int(load_library().fd_selected_kernel(num_q_heads, num_kv_heads, head_dim, q_dtype,
                                                  kv_dtype, int(bool(paged)), page_size))
+
+
+def fd_selected_kernel_scaled(num_q_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, paged,
+                              page_size, scale_kind) -> int:
+    return int(load_library().fd_selected_kernel_scaled(num_q_heads, num_kv_heads, head_dim,
+                                                        q_dtype, kv_dtype, int(bool(paged)),
+                                                        page_size, int(scale_kind)))
 
 
 def fd_set_split_events(before: Optional[torch.cuda.Event], after: Optional[torch.cuda.Event]):

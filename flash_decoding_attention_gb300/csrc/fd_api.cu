@@ -303,11 +303,18 @@ fd_status fd_set_kernel(fd_kernel kernel) {
 
 int fd_selected_kernel(int num_q_heads, int num_kv_heads, int head_dim, fd_dtype q_dtype,
                        fd_dtype kv_dtype, int paged, int page_size) {
+  return fd_selected_kernel_scaled(num_q_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, paged,
+                                   page_size, FD_SCALE_TENSOR);
+}
+
+int fd_selected_kernel_scaled(int num_q_heads, int num_kv_heads, int head_dim, fd_dtype q_dtype,
+                              fd_dtype kv_dtype, int paged, int page_size,
+                              fd_scale_kind scale_kind) {
   Config c;
   const int sms = current_sms();
   if (sms <= 0) return -1;
   if (!choose(g_kernel.load(), num_q_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, paged,
-              page_size, sms, &c))
+              page_size, sms, &c, scale_kind == FD_SCALE_TOKEN))
     return -1;
   return c.kernel;
 }

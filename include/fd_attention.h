@@ -349,12 +349,22 @@ fd_status fd_set_kernel(fd_kernel kernel);
  * current fd_set_kernel choice: FD_KERNEL_SIMT, FD_KERNEL_MMA, FD_KERNEL_TC or FD_KERNEL_FMA,
  * or -1 if the sizes are unsupported (num_q_heads counts every query token:
  * query heads times q_len).  The answer is for per-tensor or per-KV-head
- * scales; with per-token scales (FD_SCALE_TOKEN) FD_KERNEL_AUTO never takes
- * FD_KERNEL_TC, and a forced FD_KERNEL_TC or FD_KERNEL_FMA call returns
- * FD_ERR_UNSUPPORTED.  Host function.
+ * scales; fd_selected_kernel_scaled answers for per-token scales too.  Host
+ * function.
  */
 int fd_selected_kernel(int num_q_heads, int num_kv_heads, int head_dim, fd_dtype q_dtype,
                        fd_dtype kv_dtype, int paged, int page_size);
+
+/*
+ * As fd_selected_kernel, for a call with finer K/V scales of `scale_kind`
+ * (FD_SCALE_TENSOR gives the same answer as fd_selected_kernel): the kernel
+ * that fd_decode_attention_scaled (or _multi, _append) would run, or -1 when
+ * the call would return FD_ERR_UNSUPPORTED (for instance a forced
+ * FD_KERNEL_TC or FD_KERNEL_FMA with FD_SCALE_TOKEN).  Host function.
+ */
+int fd_selected_kernel_scaled(int num_q_heads, int num_kv_heads, int head_dim, fd_dtype q_dtype,
+                              fd_dtype kv_dtype, int paged, int page_size,
+                              fd_scale_kind scale_kind);
 
 /*
  * Profiling hook: when both events are non-NULL, fd_decode_attention records

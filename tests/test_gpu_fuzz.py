@@ -81,20 +81,20 @@ def _every_kernel(w):
     for k in KERNELS:
         fda.fd_set_kernel(k)
         try:
-            sel = fda.fd_selected_kernel(w.num_q_heads * w.q_len, w.num_kv_heads, w.head_dim,
-                                         0 if w.q_dtype == "f16" else 1,
-                                         fda.DTYPE_CODES[w.kv_dtype], w.paged,
-                                         max(w.page_size, 1))
+            sel = fda.fd_selected_kernel_scaled(w.num_q_heads * w.q_len, w.num_kv_heads,
+                                                w.head_dim, 0 if w.q_dtype == "f16" else 1,
+                                                fda.DTYPE_CODES[w.kv_dtype], w.paged,
+                                                max(w.page_size, 1), w.scale_kind)
         finally:
             fda.fd_set_kernel(0)
-        if k != 0 and sel != k:
-            continue   # the forced kernel does not take this case (checked elsewhere)
-        if k in (3, 4) and w.scale_kind == fw.SCALE_TOKEN:
-            # per-token scales: the tcgen05 kernel and the FMA form refuse the call
+        if sel == -1:
+            # the selection hook and the call agree: the call is refused
+            assert k != 0, "the library's own choice refused a supported case"
             with pytest.raises(fda.FdError) as e:
                 run(w, k)
             assert e.value.status == fda.FD_ERR_UNSUPPORTED
             continue
+        assert k == 0 or sel == k, (k, sel)
         out, lse, _, _ = run(w, k)
         parity(w, out, lse, ref[0], ref[1], label=f"{w.name} kernel={k} (ran {sel})")
         ran += 1
